@@ -1,0 +1,165 @@
+"""CPU oracle for the MXFP8 expert-MLP forward -- TEST INFRASTRUCTURE ONLY.
+
+A ctypes front end over ``mxfp8_oracle.c`` (plain C, binary64 arithmetic).  It restates what
+the page "Efficient MoE training for biology foundation models with Transformer Engine"
+describes in sections 1-3 (GroupedLinear over split_sizes, MXFP8 blocks of 32, the fused
+GroupedLinear -> ScaledSwiGLU -> GroupedLinear op), with the OCP-MX scale rule as the reading of
+what the page leaves open.  Only ``tests/``, the package smoke check and the bench's CPU
+baseline may import this module.  It shares no code with the CUDA library and never imports it.
+
+Every function takes and returns numpy arrays; bf16 tensors travel as their uint16 bit
+patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mxfp8_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK = 0
+BAD_ARG = 1
+SPLIT_MISMATCH = 6
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no FMA contraction, so x86-64 and aarch64 agree)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i64 = ctypes.c_int64
+            L.ora_e4m3_decode.restype = ctypes.c_double
+            L.ora_e4m3_decode.argtypes = [ctypes.c_uint8]
+            L.ora_e4m3_encode.restype = ctypes.c_uint8
+            L.ora_e4m3_encode.argtypes = [ctypes.c_double]
+            L.ora_block_exponent.restype = ctypes.c_int
+            L.ora_block_exponent.argtypes = [ctypes.c_double]
+            L.ora_quantize_block.restype = ctypes.c_uint8
+            L.ora_quantize_block.argtypes = [P, ctypes.c_int, P]
+            L.ora_e4m3_encode_array.restype = None
+            L.ora_e4m3_encode_array.argtypes = [P, i64, P]
+            L.ora_e4m3_decode_array.restype = None
+            L.ora_e4m3_decode_array.argtypes = [P, i64, P]
+            L.ora_quantize_rowwise.restype = ctypes.c_int
+            L.ora_quantize_rowwise.argtypes = [P, i64, i64, P, P, ctypes.c_int]
+            L.ora_quantize_colwise.restype = ctypes.c_int
+            L.ora_quantize_colwise.argtypes = [P, i64, i64, P, P, ctypes.c_int]
+            L.ora_grouped_mlp_rows.restype = ctypes.c_int
+            L.ora_grouped_mlp_rows.argtypes = [P, i64, i64, i64, ctypes.c_int, P, P, P, P, P, P,
+                                               P, i64, P, P, P, ctypes.c_int]
+            _lib = L
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib().ora_e4m3_decode_array(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def e4m3_encode(values: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 code (ties to even, saturating) of exact binary64 values."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib().ora_e4m3_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def block_exponent(amax: float) -> int:
+    return int(lib().ora_block_exponent(float(amax)))
+
+
+def quantize_block(values) -> tuple[np.ndarray, int]:
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    assert 0 < v.size <= 32
+    codes = np.empty(v.size, dtype=np.uint8)
+    sf = lib().ora_quantize_block(_ptr(v), v.size, _ptr(codes))
+    return codes, int(sf)
+
+
+def quantize_rowwise(x_bf16: np.ndarray, nthreads: int | None = None):
+    """[M, K] bf16 bits -> (codes [M, K] uint8, E8M0 bytes [M, K/32] uint8)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), dtype=np.uint8)
+    sf = np.empty((M, K // 32), dtype=np.uint8)
+    rc = lib().ora_quantize_rowwise(_ptr(x), M, K, _ptr(q), _ptr(sf), nthreads or default_threads())
+    if rc != OK:
+        raise ValueError(f"oracle quantize_rowwise rejected the arguments (status {rc})")
+    return q, sf
+
+
+def quantize_colwise(x_bf16: np.ndarray, nthreads: int | None = None):
+    """[M, K] bf16 bits -> (codes [M, K] uint8, E8M0 bytes [ceil(M/32), K] uint8)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), dtype=np.uint8)
+    sf = np.empty(((M + 31) // 32, K), dtype=np.uint8)
+    rc = lib().ora_quantize_colwise(_ptr(x), M, K, _ptr(q), _ptr(sf), nthreads or default_threads())
+    if rc != OK:
+        raise ValueError(f"oracle quantize_colwise rejected the arguments (status {rc})")
+    return q, sf
+
+
+def dequantize_rowwise(q: np.ndarray, sf: np.ndarray) -> np.ndarray:
+    """Value of row-wise codes under their E8M0 bytes, in binary64."""
+    vals = e4m3_decode(q)
+    return np.ldexp(vals, (np.repeat(sf.astype(np.int64), 32, axis=-1) - 127))
+
+
+def grouped_mlp_rows(x_bf16, split_sizes, gates, w1q, w1sf, w2q, w2sf, rows, nthreads=None,
+                     want_intermediate=True):
+    """Rows of the grouped MLP forward in binary64.
+
+    x_bf16 [R, H] bf16 bits; split_sizes [E]; gates [R] float32 or None (all ones);
+    w1q [E*2F, H] codes + w1sf [E*2F, H/32]; w2q [E*H, F] codes + w2sf [E*H, F/32] (all from
+    the oracle's own quantize_rowwise).  Returns (y [n, H] float64, hq [n, F], hsf [n, F/32]).
+    """
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    R, H = x.shape
+    split = np.ascontiguousarray(split_sizes, dtype=np.int32)
+    E = split.size
+    F = w2q.shape[1]
+    g = None if gates is None else np.ascontiguousarray(gates, dtype=np.float32)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.size
+    y = np.empty((n, H), dtype=np.float64)
+    hq = np.empty((n, F), dtype=np.uint8) if want_intermediate else None
+    hsf = np.empty((n, F // 32), dtype=np.uint8) if want_intermediate else None
+    arrs = [np.ascontiguousarray(a, dtype=np.uint8) for a in (w1q, w1sf, w2q, w2sf)]
+    rc = lib().ora_grouped_mlp_rows(_ptr(x), R, H, F, E, _ptr(split), _ptr(g), *[_ptr(a) for a in arrs],
+                                    _ptr(rows), n, _ptr(y), _ptr(hq), _ptr(hsf),
+                                    nthreads or default_threads())
+    if rc != OK:
+        raise ValueError(f"oracle grouped_mlp_rows rejected the arguments (status {rc})")
+    return y, hq, hsf

@@ -1,0 +1,75 @@
+"""Independent re-derivations used to pin the oracle (test code only).
+
+Nothing here calls the oracle or the CUDA library.  The E4M3 value table comes from PyTorch's
+float8_e4m3fn dtype (a library decoder), and encoding is a nearest-value search over that
+table, so a slip in the oracle's bit arithmetic (a wrong bias, a dropped sign, a tie rule)
+shows up as a disagreement.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+
+def torch_e4m3_values() -> np.ndarray:
+    """Value of every code 0..255 via torch.float8_e4m3fn (NaN for 0x7F / 0xFF)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+_POS = None
+
+
+def _positive_table():
+    global _POS
+    if _POS is None:
+        v = torch_e4m3_values()[:0x7F]      # codes 0x00..0x7E, increasing, 0x7E = 448
+        assert np.all(np.diff(v) > 0)
+        _POS = v
+    return _POS
+
+
+def nearest_code(t: np.ndarray) -> np.ndarray:
+    """Brute-force nearest E4M3 code by search; ties -> even code; |t| > 448 -> 448; sign kept."""
+    t = np.asarray(t, dtype=np.float64)
+    pos = _positive_table()
+    a = np.abs(t)
+    hi = np.clip(np.searchsorted(pos, a, side="left"), 0, len(pos) - 1)
+    lo = np.clip(hi - 1, 0, len(pos) - 1)
+    d_lo = np.abs(a - pos[lo])
+    d_hi = np.abs(pos[hi] - a)
+    pick = np.where(d_lo < d_hi, lo, hi)
+    tie = d_lo == d_hi
+    pick = np.where(tie, np.where(lo % 2 == 0, lo, hi), pick)
+    pick = np.where(a >= pos[-1], len(pos) - 1, pick)
+    sign = np.signbit(t).astype(np.uint8) << 7
+    return (pick.astype(np.uint8) | sign).astype(np.uint8)
+
+
+def block_scale_byte(amax: np.ndarray) -> np.ndarray:
+    """E8M0 byte from block amax through numpy.frexp (mantissa in [0.5,1) -> floor(log2) = e-1)."""
+    amax = np.asarray(amax, dtype=np.float64)
+    _, e = np.frexp(amax)
+    s = np.where(amax == 0, -127, np.clip(e.astype(np.int64) - 1 - 8, -127, 127))
+    return (s + 127).astype(np.uint8)
+
+
+def quantize_rows_bruteforce(v: np.ndarray):
+    """Row-wise MXFP8 of a float64 [M, K] array by frexp + search (independent of the oracle)."""
+    M, K = v.shape
+    blocks = v.reshape(M, K // 32, 32)
+    sf = block_scale_byte(np.abs(blocks).max(axis=2))
+    t = np.ldexp(blocks, -(sf.astype(np.int64) - 127)[:, :, None])
+    return nearest_code(t).reshape(M, K), sf
+
+
+def decode(codes: np.ndarray, sf: np.ndarray) -> np.ndarray:
+    """Dequantize row-wise codes [.., K] with bytes [.., K/32] through the torch table."""
+    vals = torch_e4m3_values()[np.asarray(codes, dtype=np.int64)]
+    return np.ldexp(vals, np.repeat(np.asarray(sf, dtype=np.int64) - 127, 32, axis=-1))
+
+
+def silu(g: float) -> float:
+    return g / (1.0 + math.exp(-g))
