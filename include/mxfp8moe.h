@@ -1,0 +1,140 @@
+/*
+ * mxfp8moe.h -- C ABI of the GB300 (sm_103a) MXFP8 expert-MLP library.
+ *
+ * The operations are those of the page "Efficient MoE training for biological foundation
+ * models" (news summary of NVIDIA's Transformer Engine MoE post), section "Key technical
+ * approaches in the recipe":
+ *   item 1  GroupedLinear: many per-expert linears in one call over tokens grouped by expert,
+ *           with per-expert token counts split_sizes;
+ *   item 2  MXFP8: 8-bit E4M3 values, one scale per block of 32 consecutive values;
+ *   item 3  the fused forward GroupedLinear -> ScaledSwiGLU -> GroupedLinear, which applies the
+ *           routing weight together with the SwiGLU activation and does not keep the
+ *           intermediate in 16-bit memory.
+ * The block scale rule is not printed on the pages; this library uses the OCP MX v1.0 rule:
+ * shared exponent s = floor(log2(block amax)) - 8 clamped to [-127, 127], stored as the E8M0
+ * byte s + 127 (an all-zero block gets byte 0); each element is x * 2^-s rounded to the nearest
+ * E4M3 value, ties to even, saturated to +-448.
+ *
+ * Conventions for every call
+ *   - Pointers marked (device) are CUDA device (or managed) addresses owned by the caller; the
+ *     library never allocates, frees or keeps them after the call returns.  Pointers marked
+ *     (host) are ordinary host memory read during the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All work
+ *     is enqueued on it; no call synchronizes the host except mxfp8_check_device_error.
+ *   - Every device pointer must be 16-byte aligned.  bf16 tensors are row-major IEEE bfloat16.
+ *   - Return value: an mxfp8_status.  Argument errors are detected on the host before anything
+ *     is enqueued and leave all buffers untouched.  Conditions only visible on the device
+ *     (split_sizes that do not add up to R, a pipeline wait that timed out) set bits in the
+ *     error word inside the caller's workspace; read them with mxfp8_check_device_error.
+ *     No call aborts, throws or traps.
+ */
+#ifndef MXFP8MOE_H
+#define MXFP8MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MXFP8_OK = 0,
+    MXFP8_ERR_INVALID_ARG = 1,     /* null/unaligned pointer, negative or inconsistent size   */
+    MXFP8_ERR_UNSUPPORTED = 2,     /* shape outside what the kernels support (see each call)  */
+    MXFP8_ERR_WORKSPACE = 3,       /* workspace smaller than grouped_mlp_workspace_size()     */
+    MXFP8_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed (launch, attribute)   */
+    MXFP8_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device-side wait gave up (from check only)    */
+    MXFP8_ERR_SPLIT_MISMATCH = 6   /* sum(split_sizes) != R or a negative count (check only)  */
+} mxfp8_status;
+
+/* Direction flags for mxfp8_quantize (may be OR-ed). */
+enum { MXFP8_ROWWISE = 1, MXFP8_COLWISE = 2 };
+
+/* Scale-factor layouts.
+ *   MXFP8_SF_COMPACT: row-wise bytes [M, K/32] row-major; column-wise bytes [ceil(M/32), K].
+ *   MXFP8_SF_MMA: the layout the block-scaled tensor-core MMA consumes.  For a matrix of `rows`
+ *     rows and `kb` = K/32 blocks per row, bytes are grouped in 512-byte atoms of 128 rows x 4
+ *     blocks; atom (rt, kt) starts at byte 512 * (rt * ceil(kb/4) + kt) and holds the byte of
+ *     row r = 128*rt + 32*j + i and block 4*kt + b at offset 16*i + 4*j + b.  Column-wise scales
+ *     use it with rows = K (columns of x) and kb = ceil(M/32).                                  */
+enum { MXFP8_SF_COMPACT = 0, MXFP8_SF_MMA = 1 };
+
+/* Bytes of the scale-factor buffer for one direction and layout (0 on bad arguments). */
+size_t mxfp8_sf_bytes(int64_t M, int64_t K, int direction, int sf_layout);
+
+/*
+ * mxfp8_quantize -- MXFP8 quantization of a bf16 matrix (item 2 above).
+ *   x       (device) bf16 [M, K], row-major.
+ *   dirs    MXFP8_ROWWISE and/or MXFP8_COLWISE.  Row-wise blocks are 32 consecutive elements of
+ *           a row; column-wise blocks are 32 consecutive rows of one column (a last block of
+ *           fewer rows uses the rows present).  Both directions are produced from one read of x.
+ *   q_row   (device) E4M3 codes [M, K] (row-wise), or NULL when not requested.
+ *   sf_row  (device) row-wise E8M0 bytes, mxfp8_sf_bytes(M, K, MXFP8_ROWWISE, sf_layout) bytes.
+ *   q_col   (device) E4M3 codes [M, K] in x's layout (column-wise), or NULL.
+ *   sf_col  (device) column-wise E8M0 bytes, mxfp8_sf_bytes(M, K, MXFP8_COLWISE, sf_layout).
+ * Requirements: M >= 0, K % 32 == 0; with MXFP8_SF_MMA also M % 128 == 0 and K % 128 == 0.
+ * M == 0 or K == 0 is a no-op.  Outputs are fully overwritten.  Results are bit-exact with the
+ * rule above.
+ */
+int mxfp8_quantize(const void* x, int64_t M, int64_t K, int dirs, int sf_layout,
+                   uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, void* stream);
+
+/* Workspace bytes grouped_mlp_fwd needs for these sizes (0 on bad arguments).  It holds the
+ * device tile schedule, the error word, the quantized activations and the quantized
+ * intermediate, each in an expert-padded row space of at most R + 127*E rows. */
+size_t grouped_mlp_workspace_size(int64_t R, int64_t H, int64_t F, int E);
+
+/*
+ * grouped_mlp_fwd -- fused MXFP8 grouped expert MLP forward (items 1-3 above):
+ *   for each expert e and each of its rows r (rows are grouped by expert in x_sorted):
+ *     g = xq_r W1[e, 0:F]^T,  u = xq_r W1[e, F:2F]^T            (GroupedLinear 1, fp32 accum.)
+ *     h = gate_r * silu(g) * u,  silu(g) = g / (1 + exp(-g))    (ScaledSwiGLU)
+ *     hq = MXFP8(h) row-wise along F                            (never stored in bf16)
+ *     y_r = bf16( hq W2[e]^T )                                  (GroupedLinear 2)
+ *   where xq_r is the row-wise MXFP8 quantization of x_sorted[r] (done inside the call).
+ * Arguments:
+ *   x_sorted    (device) bf16 [R, H], rows grouped by expert in expert order.
+ *   split_sizes (device) int32 [E], rows per expert; may contain zeros; must sum to R.
+ *   gates       (device) float [R] per-row routing weight, or NULL for 1.
+ *   w1_q,w1_sf  (device) W1 [E, 2F, H] E4M3 codes + row-wise E8M0 bytes in MXFP8_SF_MMA layout
+ *               for the [E*2F, H] matrix (as mxfp8_quantize(W1, E*2F, H, ROWWISE, SF_MMA)
+ *               writes them).  Rows [0, F) of each expert are the gate projection, [F, 2F) up.
+ *   w2_q,w2_sf  (device) W2 [E, H, F] codes + bytes in MXFP8_SF_MMA layout for [E*H, F].
+ *   y           (device) bf16 [R, H] output, rows in x_sorted's order; fully overwritten.
+ *   workspace   (device) at least grouped_mlp_workspace_size(R, H, F, E) bytes, 256-byte
+ *               aligned.  It must not be shared by two calls in flight at the same time.
+ * Requirements: R >= 0, 1 <= E <= 1024, H % 128 == 0, F % 128 == 0, H, F >= 128.
+ * The call never reads split_sizes on the host.  If they do not sum to R (or one is negative),
+ * the kernels do no work, y is left unspecified and the workspace's error word reports
+ * MXFP8_ERR_SPLIT_MISMATCH.
+ */
+int grouped_mlp_fwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E,
+                    const int32_t* split_sizes, const float* gates,
+                    const uint8_t* w1_q, const uint8_t* w1_sf,
+                    const uint8_t* w2_q, const uint8_t* w2_sf,
+                    void* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Byte offsets of the pieces of a grouped_mlp_fwd workspace, for inspection by tests:
+ *   [0] error word (uint32)   [1] schedule          [2] quantized activations [R_pad, H]
+ *   [3] their E8M0 bytes (MXFP8_SF_MMA layout)      [4] quantized intermediate [R_pad, F]
+ *   [5] its E8M0 bytes (MXFP8_SF_MMA layout)        [6] R_pad (row capacity, not an offset)
+ * Expert e's rows start at padded row sum_{e'<e} 128*ceil(split[e']/128); padding rows are 0.
+ * Returns MXFP8_OK, or MXFP8_ERR_INVALID_ARG for bad sizes.  out must hold 7 entries (host). */
+int grouped_mlp_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_t* out);
+
+/* Copies the workspace's error word to the host (synchronizes `stream`) and maps it to a
+ * status: MXFP8_OK, MXFP8_ERR_SPLIT_MISMATCH or MXFP8_ERR_DEVICE_TIMEOUT.  The raw bits go to
+ * *flags when flags is not NULL (host). */
+int mxfp8_check_device_error(const void* workspace, void* stream, uint32_t* flags);
+
+/* Static description of a status code. */
+const char* mxfp8_status_string(int status);
+
+/* ABI version of this header (bumped on any incompatible change). */
+int mxfp8_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXFP8MOE_H */

@@ -1,0 +1,183 @@
+"""mxfp8_block_scaled_03_gb300 -- MXFP8 expert-MLP forward for GB300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/mxfp8moe.h`` (library
+``_build/libmxfp8moe.so``).  The functions keep the C names and only marshal arguments:
+torch tensors supply device pointers and the current CUDA stream; every step of the computation
+runs in the library's CUDA kernels.  There is no CPU fallback: if the library is missing, calls
+raise ``RuntimeError``.
+
+Operations (page "Efficient MoE training for biological foundation models", Key technical
+approaches, items 1-3):
+  mxfp8_quantize     bf16 -> E4M3 codes + E8M0 scale bytes, row-wise and/or column-wise blocks
+                     of 32.
+  grouped_mlp_fwd    GroupedLinear(split_sizes) -> ScaledSwiGLU -> MXFP8 requant ->
+                     GroupedLinear, in one call.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build_ext
+
+__all__ = [
+    "MXFP8Error", "ROWWISE", "COLWISE", "SF_COMPACT", "SF_MMA", "lib", "library_path",
+    "mxfp8_sf_bytes", "mxfp8_quantize", "grouped_mlp_workspace_size", "grouped_mlp_workspace_layout",
+    "grouped_mlp_fwd", "mxfp8_check_device_error", "mxfp8_status_string", "mxfp8_abi_version",
+]
+
+ROWWISE = 1
+COLWISE = 2
+SF_COMPACT = 0
+SF_MMA = 1
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_SPLIT_MISMATCH = range(7)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MXFP8Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({mxfp8_status_string(status)})")
+
+
+def library_path() -> str:
+    return build_ext.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(build_ext.LIB):
+                raise RuntimeError(f"MXFP8 CUDA library not built ({build_ext.LIB}); run "
+                                   "mxfp8_block_scaled_03_gb300.build_ext.build() or __graft_entry__.build()")
+            L = ctypes.CDLL(build_ext.LIB)
+            P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+            L.mxfp8_abi_version.restype = i32
+            L.mxfp8_abi_version.argtypes = []
+            L.mxfp8_status_string.restype = ctypes.c_char_p
+            L.mxfp8_status_string.argtypes = [i32]
+            L.mxfp8_sf_bytes.restype = sz
+            L.mxfp8_sf_bytes.argtypes = [i64, i64, i32, i32]
+            L.mxfp8_quantize.restype = i32
+            L.mxfp8_quantize.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P]
+            L.grouped_mlp_workspace_size.restype = sz
+            L.grouped_mlp_workspace_size.argtypes = [i64, i64, i64, i32]
+            L.grouped_mlp_workspace_layout.restype = i32
+            L.grouped_mlp_workspace_layout.argtypes = [i64, i64, i64, i32, P]
+            L.grouped_mlp_fwd.restype = i32
+            L.grouped_mlp_fwd.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P]
+            L.mxfp8_check_device_error.restype = i32
+            L.mxfp8_check_device_error.argtypes = [P, P, P]
+            _lib = L
+    return _lib
+
+
+def _stream(stream=None) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise MXFP8Error(status, where)
+
+
+def mxfp8_abi_version() -> int:
+    return int(lib().mxfp8_abi_version())
+
+
+def mxfp8_status_string(status: int) -> str:
+    return lib().mxfp8_status_string(int(status)).decode()
+
+
+def mxfp8_sf_bytes(M: int, K: int, direction: int, sf_layout: int) -> int:
+    return int(lib().mxfp8_sf_bytes(M, K, direction, sf_layout))
+
+
+def mxfp8_quantize(x, rowwise: bool = True, colwise: bool = False, sf_layout: int = SF_COMPACT,
+                   out=None, stream=None):
+    """MXFP8 quantization of a contiguous bf16 CUDA tensor [M, K].
+
+    Returns (q_row, sf_row, q_col, sf_col); entries of a direction not requested are None.  Codes
+    are uint8 [M, K]; scale bytes are uint8 with mxfp8_sf_bytes(...) elements (compact layout:
+    [M, K/32] row-wise, [ceil(M/32), K] column-wise).  `out` may pass preallocated outputs.
+    """
+    import torch
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    M, K = x.shape
+    dirs = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0)
+    if out is None:
+        out = [None] * 4
+        if rowwise:
+            out[0] = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+            n = mxfp8_sf_bytes(M, K, ROWWISE, sf_layout)
+            out[1] = torch.empty(n, dtype=torch.uint8, device=x.device)
+            if sf_layout == SF_COMPACT:
+                out[1] = out[1].view(M, K // 32)
+        if colwise:
+            out[2] = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+            n = mxfp8_sf_bytes(M, K, COLWISE, sf_layout)
+            out[3] = torch.empty(n, dtype=torch.uint8, device=x.device)
+            if sf_layout == SF_COMPACT:
+                out[3] = out[3].view((M + 31) // 32, K)
+    st = lib().mxfp8_quantize(_ptr(x), M, K, dirs, sf_layout, _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+                              _ptr(out[3]), _stream(stream))
+    _check(st, "mxfp8_quantize")
+    return tuple(out)
+
+
+def grouped_mlp_workspace_size(R: int, H: int, F: int, E: int) -> int:
+    return int(lib().grouped_mlp_workspace_size(R, H, F, E))
+
+
+def grouped_mlp_workspace_layout(R: int, H: int, F: int, E: int) -> dict:
+    arr = (ctypes.c_uint64 * 7)()
+    _check(lib().grouped_mlp_workspace_layout(R, H, F, E, arr), "grouped_mlp_workspace_layout")
+    keys = ["error", "schedule", "xq", "xsf", "hq", "hsf", "r_pad"]
+    return {k: int(v) for k, v in zip(keys, arr)}
+
+
+def grouped_mlp_fwd(x_sorted, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y=None, workspace=None,
+                    stream=None):
+    """Fused MXFP8 grouped expert MLP forward.
+
+    x_sorted bf16 [R, H]; split_sizes int32 [E] (device); gates float32 [R] or None; w1_q uint8
+    [E*2F, H] with w1_sf in the tensor-core scale layout; w2_q uint8 [E*H, F] with w2_sf.
+    Returns y bf16 [R, H].  `workspace` (uint8 CUDA tensor) is allocated here when not given.
+    """
+    import torch
+    R, H = x_sorted.shape
+    E = int(split_sizes.numel())
+    F = int(w2_q.shape[1])
+    assert x_sorted.dtype == torch.bfloat16 and split_sizes.dtype == torch.int32
+    assert gates is None or gates.dtype == torch.float32
+    for t in (x_sorted, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf):
+        assert t is None or (t.is_cuda and t.is_contiguous())
+    if y is None:
+        y = torch.empty((R, H), dtype=torch.bfloat16, device=x_sorted.device)
+    need = grouped_mlp_workspace_size(R, H, F, E)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x_sorted.device)
+    st = lib().grouped_mlp_fwd(_ptr(x_sorted), R, H, F, E, _ptr(split_sizes), _ptr(gates), _ptr(w1_q),
+                               _ptr(w1_sf), _ptr(w2_q), _ptr(w2_sf), _ptr(y), _ptr(workspace),
+                               workspace.numel(), _stream(stream))
+    _check(st, "grouped_mlp_fwd")
+    return y
+
+
+def mxfp8_check_device_error(workspace, stream=None) -> tuple[int, int]:
+    """(status, raw error bits) of the last grouped_mlp_fwd on this workspace (synchronizes)."""
+    flags = ctypes.c_uint32(0)
+    st = lib().mxfp8_check_device_error(_ptr(workspace), _stream(stream), ctypes.byref(flags))
+    return int(st), int(flags.value)

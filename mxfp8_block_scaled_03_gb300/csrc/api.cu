@@ -1,0 +1,137 @@
+// api.cu -- the extern "C" boundary declared in include/mxfp8moe.h: argument checks, workspace
+// layout, and dispatch to the kernels' launchers.  No call allocates device memory or
+// synchronizes the host, except mxfp8_check_device_error (which reads the error word).
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "mx_internal.h"
+#include "mxfp8moe.h"
+
+namespace mx {
+
+namespace {
+constexpr size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+bool ws_layout(int64_t R, int64_t H, int64_t F, int E, WsLayout* out) {
+  if (R < 0 || H <= 0 || F <= 0 || E < 1 || E > 1024) return false;
+  if (R > static_cast<int64_t>(INT32_MAX) - 128 * static_cast<int64_t>(E)) return false;
+  WsLayout L{};
+  L.r_pad = ((R + 127 * static_cast<int64_t>(E)) + 127) / 128 * 128;
+  L.meta = 0;
+  L.xq = align256(sizeof(SchedHeader) + 3 * static_cast<size_t>(E + 1) * sizeof(int32_t));
+  L.xsf = align256(L.xq + static_cast<size_t>(L.r_pad) * H);
+  L.hq = align256(L.xsf + static_cast<size_t>(L.r_pad) * H / 32);
+  L.hsf = align256(L.hq + static_cast<size_t>(L.r_pad) * F);
+  L.total = align256(L.hsf + static_cast<size_t>(L.r_pad) * F / 32);
+  *out = L;
+  return true;
+}
+
+}  // namespace mx
+
+using namespace mx;
+
+extern "C" {
+
+int mxfp8_abi_version(void) { return 1; }
+
+const char* mxfp8_status_string(int status) {
+  switch (status) {
+    case MXFP8_OK: return "ok";
+    case MXFP8_ERR_INVALID_ARG: return "invalid argument";
+    case MXFP8_ERR_UNSUPPORTED: return "unsupported shape";
+    case MXFP8_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case MXFP8_ERR_CUDA: return "CUDA call failed";
+    case MXFP8_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MXFP8_ERR_SPLIT_MISMATCH: return "split_sizes do not sum to R (or are negative)";
+    default: return "unknown status";
+  }
+}
+
+size_t mxfp8_sf_bytes(int64_t M, int64_t K, int direction, int sf_layout) {
+  if (M < 0 || K < 0 || K % 32 != 0) return 0;
+  if (sf_layout == MXFP8_SF_COMPACT) {
+    if (direction == MXFP8_ROWWISE) return static_cast<size_t>(M) * (K / 32);
+    if (direction == MXFP8_COLWISE) return static_cast<size_t>((M + 31) / 32) * K;
+    return 0;
+  }
+  if (sf_layout == MXFP8_SF_MMA) {
+    if (direction == MXFP8_ROWWISE) return static_cast<size_t>((M + 127) / 128) * ((K / 32 + 3) / 4) * 512;
+    if (direction == MXFP8_COLWISE) return static_cast<size_t>((K + 127) / 128) * (((M + 31) / 32 + 3) / 4) * 512;
+  }
+  return 0;
+}
+
+int mxfp8_quantize(const void* x, int64_t M, int64_t K, int dirs, int sf_layout, uint8_t* q_row, uint8_t* sf_row,
+                   uint8_t* q_col, uint8_t* sf_col, void* stream) {
+  if (M < 0 || K < 0 || K % 32 != 0) return MXFP8_ERR_INVALID_ARG;
+  if (dirs < 1 || dirs > 3) return MXFP8_ERR_INVALID_ARG;
+  if (sf_layout != MXFP8_SF_COMPACT && sf_layout != MXFP8_SF_MMA) return MXFP8_ERR_INVALID_ARG;
+  const bool row = dirs & MXFP8_ROWWISE, col = dirs & MXFP8_COLWISE;
+  if (sf_layout == MXFP8_SF_MMA && (M % 128 != 0 || K % 128 != 0)) return MXFP8_ERR_UNSUPPORTED;
+  if (M == 0 || K == 0) return MXFP8_OK;
+  if (x == nullptr || !aligned16(x)) return MXFP8_ERR_INVALID_ARG;
+  if (row && (q_row == nullptr || sf_row == nullptr || !aligned16(q_row) || !aligned16(sf_row)))
+    return MXFP8_ERR_INVALID_ARG;
+  if (col && (q_col == nullptr || sf_col == nullptr || !aligned16(q_col) || !aligned16(sf_col)))
+    return MXFP8_ERR_INVALID_ARG;
+  if ((M + 31) / 32 > INT32_MAX || (K + 255) / 256 > 65535) return MXFP8_ERR_UNSUPPORTED;
+  const cudaError_t e =
+      launch_quantize(x, M, K, dirs, sf_layout, q_row, sf_row, q_col, sf_col, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+}
+
+size_t grouped_mlp_workspace_size(int64_t R, int64_t H, int64_t F, int E) {
+  WsLayout L;
+  if (!ws_layout(R, H, F, E, &L)) return 0;
+  return L.total;
+}
+
+int grouped_mlp_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_t* out) {
+  WsLayout L;
+  if (out == nullptr || !ws_layout(R, H, F, E, &L)) return MXFP8_ERR_INVALID_ARG;
+  out[0] = L.meta;  // the error word is the first field of the schedule header
+  out[1] = L.meta;
+  out[2] = L.xq;
+  out[3] = L.xsf;
+  out[4] = L.hq;
+  out[5] = L.hsf;
+  out[6] = static_cast<uint64_t>(L.r_pad);
+  return MXFP8_OK;
+}
+
+int grouped_mlp_fwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
+                    const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
+                    const uint8_t* w2_sf, void* y, void* workspace, size_t workspace_bytes, void* stream) {
+  if (R < 0 || E < 1 || E > 1024 || H <= 0 || F <= 0) return MXFP8_ERR_INVALID_ARG;
+  if (H % 128 != 0 || F % 128 != 0) return MXFP8_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(E) * 2 * F > INT32_MAX || static_cast<int64_t>(E) * H > INT32_MAX)
+    return MXFP8_ERR_UNSUPPORTED;
+  const void* ptrs[] = {x_sorted, split_sizes, w1_q, w1_sf, w2_q, w2_sf, y, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return MXFP8_ERR_INVALID_ARG;
+  if (gates != nullptr && !aligned16(gates)) return MXFP8_ERR_INVALID_ARG;
+  WsLayout L;
+  if (!ws_layout(R, H, F, E, &L)) return MXFP8_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total) return MXFP8_ERR_WORKSPACE;
+  return launch_grouped_mlp(x_sorted, R, H, F, E, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y, workspace, L,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int mxfp8_check_device_error(const void* workspace, void* stream, uint32_t* flags) {
+  if (workspace == nullptr) return MXFP8_ERR_INVALID_ARG;
+  uint32_t w = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&w, workspace, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (flags) *flags = w;
+  if (w & ERR_TIMEOUT_MASK) return MXFP8_ERR_DEVICE_TIMEOUT;
+  if (w & (ERR_SPLIT_SUM | ERR_SPLIT_NEGATIVE)) return MXFP8_ERR_SPLIT_MISMATCH;
+  return MXFP8_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// mx_internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+// Bits of the device error word (first 4 bytes of a grouped_mlp_fwd workspace).
+enum : uint32_t {
+  ERR_SPLIT_SUM = 1u << 0,        // split_sizes do not add up to R
+  ERR_SPLIT_NEGATIVE = 1u << 1,   // a negative split size
+  ERR_TIMEOUT_PRODUCER = 1u << 8, // TMA producer gave up waiting for a free stage
+  ERR_TIMEOUT_MMA = 1u << 9,      // MMA issuer gave up waiting for data or a free accumulator
+  ERR_TIMEOUT_EPILOGUE = 1u << 10,// epilogue gave up waiting for an accumulator
+  ERR_TIMEOUT_DRAIN = 1u << 11,   // teardown gave up waiting for copies / MMAs in flight
+};
+constexpr uint32_t ERR_TIMEOUT_MASK = 0xF00u;
+
+// Device schedule written by the schedule kernel at the start of the workspace.  Arrays of E+1
+// int32 follow the header: row_off (prefix sums of split_sizes), pad_off (prefix sums of
+// 128 * ceil(split/128): each expert's first row in the padded row space), mt_off (prefix sums
+// of ceil(split/128): each expert's first 128-row tile).
+struct SchedHeader {
+  uint32_t error;
+  int32_t num_mtiles;   // total 128-row tiles over all experts (0 on a split error)
+  int32_t pad_rows;     // 128 * num_mtiles
+  int32_t E;
+  int32_t reserved[12];
+};
+static_assert(sizeof(SchedHeader) == 64, "schedule header is 64 bytes");
+
+struct WsLayout {
+  size_t meta, xq, xsf, hq, hsf, total;
+  int64_t r_pad;   // row capacity of the padded row space
+};
+bool ws_layout(int64_t R, int64_t H, int64_t F, int E, WsLayout* out);
+
+// Quantize launchers (quantize.cu).  Return a cudaError_t from the launch.
+cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int dirs, int sf_layout, uint8_t* q_row,
+                            uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, cudaStream_t stream);
+// Row-wise MXFP8 of x_sorted [R, H] into the expert-padded row space (rows beyond an expert's
+// count are written as zeros), scale bytes in the tensor-core layout.
+cudaError_t launch_quantize_gather(const void* x, int64_t R, int64_t H, const SchedHeader* meta, int E,
+                                   int64_t r_pad, uint8_t* xq, uint8_t* xsf, cudaStream_t stream);
+
+// Grouped MLP launchers (grouped_gemm.cu).
+cudaError_t launch_schedule(const int32_t* split, int E, int64_t R, SchedHeader* meta, cudaStream_t stream);
+// Enqueues schedule, activation quantize and both grouped GEMMs; returns an mxfp8_status.
+int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
+                       const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
+                       const uint8_t* w2_sf, void* y, void* workspace, const WsLayout& L, cudaStream_t stream);
+
+}  // namespace mx
