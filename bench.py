@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Throughput of the MXFP8 grouped expert-MLP forward on one GB300 (or N replicas).
+
+One step = one grouped_mlp_fwd call over the whole Mixtral-8x7B-shaped expert layer
+(E=8, top-2, T=16384 tokens -> R=32768 routed rows, H=4096, F=14336): activation quantize,
+device tile schedule, GroupedLinear 1 with the fused ScaledSwiGLU + MXFP8 requant epilogue, and
+GroupedLinear 2 to bf16.  Inputs are synthetic (seeded, shapes of the pages' workload) and
+resident in HBM when the timed region starts; weights are quantized once beforehand (the
+"quantized init" setting), timed separately.
+
+Printed: one JSON line (rank 0).  `value` = 6*R*H*F / step time in TFLOP/s summed over ranks.
+Extra keys: roofline (dominant kernel = GroupedLinear 1), quantize (stand-alone MXFP8 quantize
+of a 16384 x 14336 bf16 matrix, row- and column-wise, GB/s against HBM), e2e (same step with
+host buffers, copies inside the timed region), cpu_baseline (the oracle on a bounded sample),
+clocks, gpu_launches.
+
+--impl reference times the CPU oracle instead (bounded row samples of the same workload).
+Multi-GPU (torchrun): every rank runs an independent replica of the step ("replicas only": the
+path has no exchange), timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GroupedMLP MXFP8 fwd TFLOP/s & % of MXFP8 peak; quantize GB/s & % of HBM"
+WORKLOAD = "mixtral"
+QUANT_SHAPE = (16384, 14336)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 vs 2.25 PFLOP/s per GPU)
+KERNEL_SOURCES = ["mxfp8_block_scaled_03_gb300/csrc/grouped_gemm.cu", "mxfp8_block_scaled_03_gb300/csrc/mx_device.cuh",
+                  "mxfp8_block_scaled_03_gb300/csrc/quantize.cu"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """Per-launch DRAM bytes of the dominant kernels from the committed ncu summary, or None
+    when the kernel sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return {}
+    if d.get("kernel_hash") != kernel_hash():
+        return {}
+    return d
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while active."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons, power = [], [], set(), []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle leg (cpu_baseline and --impl reference)
+# ------------------------------------------------------------------------------------------------
+class OracleSample:
+    """The oracle on `nrows` rows of one expert of the workload (a sub-problem with E=1 holding
+    that expert's rows and weights: the per-row arithmetic is identical)."""
+
+    def __init__(self, w, expert: int = 0, nrows: int = 64):
+        import numpy as np
+        import oracle
+        self.oracle = oracle
+        off = np.concatenate([[0], np.cumsum(w.split_sizes)])
+        n = int(w.split_sizes[expert])
+        self.x = np.ascontiguousarray(w.x_sorted[off[expert]:off[expert] + n])
+        self.gates = None if w.gates is None else np.ascontiguousarray(w.gates[off[expert]:off[expert] + n])
+        F, H = w.F, w.H
+        self.w1q, self.w1s = oracle.quantize_rowwise(w.w1[expert * 2 * F:(expert + 1) * 2 * F])
+        self.w2q, self.w2s = oracle.quantize_rowwise(w.w2[expert * H:(expert + 1) * H])
+        self.split = np.array([n], dtype=np.int32)
+        self.nrows = min(nrows, n)
+        self.flops_per_row = 6.0 * H * F
+        self.threads = oracle.default_threads()
+        self._step = 0
+        self.n_avail = n
+
+    def run(self) -> float:
+        import numpy as np
+        start = (self._step * self.nrows) % max(1, self.n_avail - self.nrows + 1)
+        rows = np.arange(start, start + self.nrows)
+        self._step += 1
+        t0 = time.perf_counter()
+        self.oracle.grouped_mlp_rows(self.x, self.split, self.gates, self.w1q, self.w1s, self.w2q, self.w2s, rows,
+                                     nthreads=self.threads, want_intermediate=False)
+        return time.perf_counter() - t0
+
+    def describe(self):
+        return (f"{self.nrows} consecutive rows of expert 0 of the {WORKLOAD} workload per timed call "
+                f"(binary64 GroupedLinear->ScaledSwiGLU->requant->GroupedLinear, {self.flops_per_row:.3g} flop/row); "
+                "oracle weight quantization excluded")
+
+
+def run_reference(args, world, rank):
+    from mxfp8_block_scaled_03_gb300 import workloads as W
+    if rank != 0:
+        return
+    w = W.moe_workload(WORKLOAD, seed=0)
+    s = OracleSample(w, nrows=args.oracle_rows)
+    for _ in range(args.warmup):
+        s.run()
+    times = [s.run() for _ in range(args.steps)]
+    total = sum(times)
+    value = s.nrows * s.flops_per_row * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": s.threads, "kind": "oracle",
+                         "sample": s.describe()},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": f"{WORKLOAD}-8x7b expert MLP layer: E={w.E} top-{w.topk} T={w.T} (R={w.R} routed rows) "
+                        f"H={w.H} F={w.F}, x~N(0,1), W~N(0,0.02), router logits N(0,1)+bias N(0,0.5)",
+            "R": w.R, "H": w.H, "F": w.F, "E": w.E, "split_sizes": [int(v) for v in w.split_sizes],
+            "l2": "no flush: inputs larger than L2 (x 256 MiB, W1+W2 1.3 GiB quantized)",
+            "parallelism": "replicas"}
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU leg
+# ------------------------------------------------------------------------------------------------
+def run_native(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import mxfp8_block_scaled_03_gb300 as mx
+    from mxfp8_block_scaled_03_gb300 import build_ext
+    from mxfp8_block_scaled_03_gb300 import workloads as W
+
+    build_ext.build()
+    mx.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+
+    w = W.moe_workload(WORKLOAD, seed=0)
+    R, H, F, E = w.R, w.H, w.F, w.E
+    flops = 6.0 * R * H * F
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x = bf(w.x_sorted)
+    split = torch.from_numpy(w.split_sizes).to(dev)
+    gates = torch.from_numpy(w.gates).to(dev)
+    w1 = bf(w.w1)
+    w2 = bf(w.w2)
+    # weights quantized once (timed separately)
+    for _ in range(2):
+        w1q, w1s, _, _ = mx.mxfp8_quantize(w1, sf_layout=mx.SF_MMA)
+        w2q, w2s, _, _ = mx.mxfp8_quantize(w2, sf_layout=mx.SF_MMA)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    mx.mxfp8_quantize(w1, sf_layout=mx.SF_MMA, out=[w1q, w1s, None, None])
+    mx.mxfp8_quantize(w2, sf_layout=mx.SF_MMA, out=[w2q, w2s, None, None])
+    e1.record()
+    torch.cuda.synchronize()
+    weight_quant_ms = e0.elapsed_time(e1)
+    del w1, w2
+    ws = torch.empty(mx.grouped_mlp_workspace_size(R, H, F, E), dtype=torch.uint8, device=dev)
+    y = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+
+    def step(events=None):
+        mx.grouped_mlp_fwd(x, split, gates, w1q, w1s, w2q, w2s, y=y, workspace=ws, stage_events=events)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, bits = mx.mxfp8_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {bits:#x} after warm-up")
+
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for evs in stage_ev:          # torch creates the CUDA event on first record; the library re-records it
+        for ev in evs:
+            ev.record()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start.record()
+        for i in range(args.steps):
+            step(stage_ev[i])
+        t_end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    clocks = clk.summary()
+    step_ms = t_start.elapsed_time(t_end) / args.steps
+    step_ms = max_over_ranks(world, step_ms)
+    names = ["schedule", "quantize_x", "grouped_linear1_swiglu_requant", "grouped_linear2"]
+    kern_ms = {n: sum(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev) / args.steps for j, n in enumerate(names)}
+    st, bits = mx.mxfp8_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {bits:#x} after timed steps")
+
+    value = world * flops / (step_ms * 1e-3) / 1e12
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    traffic = load_traffic()
+    g1_flops = 4.0 * R * H * F
+    g1_tflops = g1_flops / (kern_ms["grouped_linear1_swiglu_requant"] * 1e-3) / 1e12
+    g2_tflops = 2.0 * R * H * F / (kern_ms["grouped_linear2"] * 1e-3) / 1e12
+    roofline = {"kernel": "k_grouped_gemm<GEMM_SWIGLU> (GroupedLinear 1 + ScaledSwiGLU + requant)",
+                "bound": "tensor", "achieved": g1_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": g1_tflops / fp8_peak,
+                "peak_source": f"{peak_src} bf16_tflops {peaks['bf16_tflops']:.1f} x {FP8_OVER_BF16:.0f} "
+                               "(nominal dense fp8/bf16 ratio)",
+                "algorithmic_flops_per_launch": g1_flops,
+                "traffic": traffic.get("grouped_linear1_bytes_per_launch"),
+                "step_frac_of_peak": value / world / fp8_peak,
+                "kernel_ms": kern_ms,
+                "grouped_linear2": {"achieved": g2_tflops, "frac": g2_tflops / fp8_peak}}
+
+    # ---- stand-alone quantize (row + column) ----
+    qx = bf(W.quant_matrix(*QUANT_SHAPE, seed=0))
+    M, K = QUANT_SHAPE
+    qout = list(mx.mxfp8_quantize(qx, rowwise=True, colwise=True))
+    for _ in range(max(3, args.warmup)):
+        mx.mxfp8_quantize(qx, rowwise=True, colwise=True, out=qout)
+    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    qsteps = max(10, args.steps)
+    q0.record()
+    for _ in range(qsteps):
+        mx.mxfp8_quantize(qx, rowwise=True, colwise=True, out=qout)
+    q1.record()
+    torch.cuda.synchronize()
+    q_ms = q0.elapsed_time(q1) / qsteps
+    q_bytes = M * K * (2 + 2 * (1 + 1 / 32))
+    q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
+    quant = {"shape": [M, K], "directions": "row+col", "ms": q_ms, "achieved": q_gbs, "unit": "GB/s",
+             "peak": peaks["hbm_gbs"], "frac": q_gbs / peaks["hbm_gbs"], "bound": "hbm",
+             "algorithmic_bytes_per_launch": q_bytes, "traffic": traffic.get("quantize_bytes_per_launch"),
+             "l2": "no flush: 470 MB input > L2"}
+    del qx, qout
+
+    # ---- end to end through the public API with host buffers ----
+    xh = torch.from_numpy(np.ascontiguousarray(w.x_sorted).view(np.int16)).view(torch.bfloat16).pin_memory()
+    sh = torch.from_numpy(w.split_sizes).pin_memory()
+    gh = torch.from_numpy(w.gates).pin_memory()
+    yh = torch.empty((R, H), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(x)
+    sd = torch.empty_like(split)
+    gd = torch.empty_like(gates)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        sd.copy_(sh, non_blocking=True)
+        gd.copy_(gh, non_blocking=True)
+        mx.grouped_mlp_fwd(xd, sd, gd, w1q, w1s, w2q, w2s, y=y, workspace=ws)
+        yh.copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    a1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, a0.elapsed_time(a1) / args.steps)
+    barrier(world)
+    h2d = xh.numel() * 2 + sh.numel() * 4 + gh.numel() * 4
+    d2h = yh.numel() * 2
+    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "path": "pinned host x/split_sizes/gates -> device, grouped_mlp_fwd, y -> pinned host"}
+
+    # ---- CPU oracle baseline on a bounded sample (rank 0 only, N=1 only) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s = OracleSample(w, nrows=args.oracle_rows)
+        t = s.run()
+        cpu = {"value": s.nrows * s.flops_per_row / t / 1e12, "unit": "TFLOP/s", "cores": s.threads,
+               "kind": "oracle", "sample": s.describe(), "seconds": t}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
+            "config": workload_config(w), "roofline": roofline, "quantize": quant, "e2e": e2e,
+            "cpu_baseline": cpu, "clocks": clocks, "gpu_launches": 4 * args.steps,
+            "weight_quantize_ms": weight_quant_ms, "peaks": {"source": peak_src, **peaks},
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--oracle-rows", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_native(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -115,6 +115,19 @@ int grouped_mlp_fwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E
                     const uint8_t* w2_q, const uint8_t* w2_sf,
                     void* y, void* workspace, size_t workspace_bytes, void* stream);
 
+/* grouped_mlp_fwd with per-kernel timing: identical work and results, and additionally records
+ * the 5 caller-created CUDA events stage_events[0..4] (cudaEvent_t as void*, host array) on
+ * `stream` before the schedule, activation-quantize, GroupedLinear-1 (+ScaledSwiGLU, requant)
+ * and GroupedLinear-2 kernels and after the last one, so cudaEventElapsedTime between
+ * consecutive events gives each kernel's device time.  stage_events must not be NULL (use
+ * grouped_mlp_fwd instead); an individual NULL entry skips that record. */
+int grouped_mlp_fwd_timed(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E,
+                          const int32_t* split_sizes, const float* gates,
+                          const uint8_t* w1_q, const uint8_t* w1_sf,
+                          const uint8_t* w2_q, const uint8_t* w2_sf,
+                          void* y, void* workspace, size_t workspace_bytes, void* stream,
+                          void* const* stage_events);
+
 /* Byte offsets of the pieces of a grouped_mlp_fwd workspace, for inspection by tests:
  *   [0] error word (uint32)   [1] schedule          [2] quantized activations [R_pad, H]
  *   [3] their E8M0 bytes (MXFP8_SF_MMA layout)      [4] quantized intermediate [R_pad, F]

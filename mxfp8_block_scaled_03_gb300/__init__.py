@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L.grouped_mlp_workspace_layout.argtypes = [i64, i64, i64, i32, P]
             L.grouped_mlp_fwd.restype = i32
             L.grouped_mlp_fwd.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P]
+            L.grouped_mlp_fwd_timed.restype = i32
+            L.grouped_mlp_fwd_timed.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P, P]
             L.mxfp8_check_device_error.restype = i32
             L.mxfp8_check_device_error.argtypes = [P, P, P]
             _lib = L
@@ -149,7 +151,7 @@ def grouped_mlp_workspace_layout(R: int, H: int, F: int, E: int) -> dict:
 
 
 def grouped_mlp_fwd(x_sorted, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y=None, workspace=None,
-                    stream=None):
+                    stream=None, stage_events=None):
     """Fused MXFP8 grouped expert MLP forward.
 
     x_sorted bf16 [R, H]; split_sizes int32 [E] (device); gates float32 [R] or None; w1_q uint8
@@ -169,10 +171,18 @@ def grouped_mlp_fwd(x_sorted, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y=No
     need = grouped_mlp_workspace_size(R, H, F, E)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=x_sorted.device)
-    st = lib().grouped_mlp_fwd(_ptr(x_sorted), R, H, F, E, _ptr(split_sizes), _ptr(gates), _ptr(w1_q),
-                               _ptr(w1_sf), _ptr(w2_q), _ptr(w2_sf), _ptr(y), _ptr(workspace),
-                               workspace.numel(), _stream(stream))
-    _check(st, "grouped_mlp_fwd")
+    args = (_ptr(x_sorted), R, H, F, E, _ptr(split_sizes), _ptr(gates), _ptr(w1_q), _ptr(w1_sf), _ptr(w2_q),
+            _ptr(w2_sf), _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream))
+    if stage_events is None:
+        _check(lib().grouped_mlp_fwd(*args), "grouped_mlp_fwd")
+    else:
+        # 5 torch.cuda.Event(enable_timing=True), already recorded once (torch creates the CUDA
+        # event lazily): re-recorded before each of the 4 kernels and after the last
+        handles = [int(ev.cuda_event) for ev in stage_events]
+        if len(handles) != 5 or not all(handles):
+            raise ValueError("stage_events: 5 CUDA events that have been recorded at least once")
+        arr = (ctypes.c_void_p * 5)(*handles)
+        _check(lib().grouped_mlp_fwd_timed(*args, arr), "grouped_mlp_fwd_timed")
     return y
 
 

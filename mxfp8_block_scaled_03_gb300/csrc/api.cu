@@ -104,9 +104,10 @@ int grouped_mlp_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_
   return MXFP8_OK;
 }
 
-int grouped_mlp_fwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
-                    const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
-                    const uint8_t* w2_sf, void* y, void* workspace, size_t workspace_bytes, void* stream) {
+static int grouped_mlp_fwd_impl(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E,
+                                const int32_t* split_sizes, const float* gates, const uint8_t* w1_q,
+                                const uint8_t* w1_sf, const uint8_t* w2_q, const uint8_t* w2_sf, void* y,
+                                void* workspace, size_t workspace_bytes, void* stream, void* const* events) {
   if (R < 0 || E < 1 || E > 1024 || H <= 0 || F <= 0) return MXFP8_ERR_INVALID_ARG;
   if (H % 128 != 0 || F % 128 != 0) return MXFP8_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(E) * 2 * F > INT32_MAX || static_cast<int64_t>(E) * H > INT32_MAX)
@@ -119,7 +120,23 @@ int grouped_mlp_fwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E
   if (!ws_layout(R, H, F, E, &L)) return MXFP8_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total) return MXFP8_ERR_WORKSPACE;
   return launch_grouped_mlp(x_sorted, R, H, F, E, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y, workspace, L,
-                            static_cast<cudaStream_t>(stream));
+                            static_cast<cudaStream_t>(stream), events);
+}
+
+int grouped_mlp_fwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
+                    const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
+                    const uint8_t* w2_sf, void* y, void* workspace, size_t workspace_bytes, void* stream) {
+  return grouped_mlp_fwd_impl(x_sorted, R, H, F, E, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y, workspace,
+                              workspace_bytes, stream, nullptr);
+}
+
+int grouped_mlp_fwd_timed(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
+                          const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
+                          const uint8_t* w2_sf, void* y, void* workspace, size_t workspace_bytes, void* stream,
+                          void* const* stage_events) {
+  if (stage_events == nullptr) return MXFP8_ERR_INVALID_ARG;
+  return grouped_mlp_fwd_impl(x_sorted, R, H, F, E, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y, workspace,
+                              workspace_bytes, stream, stage_events);
 }
 
 int mxfp8_check_device_error(const void* workspace, void* stream, uint32_t* flags) {

@@ -475,7 +475,8 @@ cudaError_t launch_schedule(const int32_t* split, int E, int64_t R, SchedHeader*
 
 int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
                        const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
-                       const uint8_t* w2_sf, void* y, void* workspace, const WsLayout& L, cudaStream_t stream) {
+                       const uint8_t* w2_sf, void* y, void* workspace, const WsLayout& L, cudaStream_t stream,
+                       void* const* events) {
   DeviceInfo* dev = nullptr;
   if (!device_setup(&dev)) return MXFP8_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -490,9 +491,16 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
       !make_map(&mA2, hq, L.r_pad, F) || !make_map(&mB2, w2_q, static_cast<uint64_t>(E) * H, F))
     return MXFP8_ERR_CUDA;
 
+  auto mark = [&](int i) {
+    return events == nullptr || events[i] == nullptr ||
+           cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess;
+  };
+  if (!mark(0)) return MXFP8_ERR_CUDA;
   if (launch_schedule(split, E, R, meta, stream) != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (!mark(1)) return MXFP8_ERR_CUDA;
   if (launch_quantize_gather(x_sorted, R, H, meta, E, L.r_pad, xq, xsf, stream) != cudaSuccess)
     return MXFP8_ERR_CUDA;
+  if (!mark(2)) return MXFP8_ERR_CUDA;
 
   const int max_mtiles = static_cast<int>(L.r_pad / BM);
   GemmParams p1{};
@@ -514,6 +522,7 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   const int grid1 = static_cast<int>(std::min<int64_t>(dev->sms, static_cast<int64_t>(max_mtiles) * p1.NT));
   k_grouped_gemm<GEMM_SWIGLU><<<grid1, NUM_THREADS, SMEM_BYTES, stream>>>(mA1, mB1, p1);
   if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (!mark(3)) return MXFP8_ERR_CUDA;
 
   GemmParams p2{};
   p2.meta = meta;
@@ -532,6 +541,7 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   const int grid2 = static_cast<int>(std::min<int64_t>(dev->sms, static_cast<int64_t>(max_mtiles) * p2.NT));
   k_grouped_gemm<GEMM_OUT><<<grid2, NUM_THREADS, SMEM_BYTES, stream>>>(mA2, mB2, p2);
   if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (!mark(4)) return MXFP8_ERR_CUDA;
   return MXFP8_OK;
 }
 

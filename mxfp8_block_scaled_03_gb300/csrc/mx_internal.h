@@ -47,8 +47,11 @@ cudaError_t launch_quantize_gather(const void* x, int64_t R, int64_t H, const Sc
 // Grouped MLP launchers (grouped_gemm.cu).
 cudaError_t launch_schedule(const int32_t* split, int E, int64_t R, SchedHeader* meta, cudaStream_t stream);
 // Enqueues schedule, activation quantize and both grouped GEMMs; returns an mxfp8_status.
+// `events` (may be null): 5 cudaEvent_t recorded on `stream` before each of the 4 kernels and
+// after the last one.
 int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
                        const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
-                       const uint8_t* w2_sf, void* y, void* workspace, const WsLayout& L, cudaStream_t stream);
+                       const uint8_t* w2_sf, void* y, void* workspace, const WsLayout& L, cudaStream_t stream,
+                       void* const* events);
 
 }  // namespace mx
