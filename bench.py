@@ -182,6 +182,7 @@ class OracleSample:
         self.threads = oracle.default_threads()
         self._step = 0
         self.n_avail = n
+        self.name = w.name
 
     def run(self) -> float:
         import numpy as np
@@ -194,7 +195,7 @@ class OracleSample:
         return time.perf_counter() - t0
 
     def describe(self):
-        return (f"{self.nrows} consecutive rows of expert 0 of the {WORKLOAD} workload per timed call "
+        return (f"{self.nrows} consecutive rows of expert 0 of the {self.name} workload per timed call "
                 f"(binary64 GroupedLinear->ScaledSwiGLU->requant->GroupedLinear, {self.flops_per_row:.3g} flop/row); "
                 "oracle weight quantization excluded")
 
@@ -203,7 +204,7 @@ def run_reference(args, world, rank):
     from mxfp8_block_scaled_03_gb300 import workloads as W
     if rank != 0:
         return
-    w = W.moe_workload(WORKLOAD, seed=0)
+    w = W.moe_workload(args.workload, seed=0)
     s = OracleSample(w, nrows=args.oracle_rows)
     for _ in range(args.warmup):
         s.run()
@@ -222,9 +223,17 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+WORKLOAD_TEXT = {
+    "mixtral": "Mixtral-8x7B-shaped expert MLP layer, router logits N(0,1)+per-expert bias N(0,0.5), top-2 renormalized",
+    "llama": "dense Llama-3.1-8B-shaped SwiGLU MLP as one group, gate 1",
+    "fine": "fine-grained skewed MoE, Zipf(1.2) expert popularity (3 experts empty), top-8, Dirichlet(1) gates",
+    "tiny": "tiny MoE expert MLP, router logits N(0,1), top-2 renormalized",
+}
+
+
 def workload_config(w):
-    return {"workload": f"{WORKLOAD}-8x7b expert MLP layer: E={w.E} top-{w.topk} T={w.T} (R={w.R} routed rows) "
-                        f"H={w.H} F={w.F}, x~N(0,1), W~N(0,0.02), router logits N(0,1)+bias N(0,0.5)",
+    return {"workload": f"{WORKLOAD_TEXT[w.name]}: E={w.E} top-{w.topk} T={w.T} (R={w.R} routed rows) "
+                        f"H={w.H} F={w.F}, x~N(0,1), W~N(0,0.02)",
             "R": w.R, "H": w.H, "F": w.F, "E": w.E, "split_sizes": [int(v) for v in w.split_sizes],
             "l2": "no flush: inputs larger than L2 (x 256 MiB, W1+W2 1.3 GiB quantized)",
             "parallelism": "replicas"}
@@ -247,7 +256,7 @@ def run_native(args, world, rank, local):
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
 
-    w = W.moe_workload(WORKLOAD, seed=0)
+    w = W.moe_workload(args.workload, seed=0)
     R, H, F, E = w.R, w.H, w.F, w.E
     flops = 6.0 * R * H * F
 
@@ -256,7 +265,7 @@ def run_native(args, world, rank, local):
 
     x = bf(w.x_sorted)
     split = torch.from_numpy(w.split_sizes).to(dev)
-    gates = torch.from_numpy(w.gates).to(dev)
+    gates = torch.from_numpy(w.gates).to(dev) if w.gates is not None else None
     w1 = bf(w.w1)
     w2 = bf(w.w2)
     # weights quantized once (timed separately)
@@ -325,6 +334,12 @@ def run_native(args, world, rank, local):
                 "kernel_ms": kern_ms,
                 "grouped_linear2": {"achieved": g2_tflops, "frac": g2_tflops / fp8_peak}}
 
+    if args.only == "fwd":
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, "ms_per_step": step_ms, "value": value,
+                              "roofline": roofline}), flush=True)
+        return
+
     # ---- stand-alone quantize (row + column) ----
     qx = bf(W.quant_matrix(*QUANT_SHAPE, seed=0))
     M, K = QUANT_SHAPE
@@ -351,16 +366,17 @@ def run_native(args, world, rank, local):
     # ---- end to end through the public API with host buffers ----
     xh = torch.from_numpy(np.ascontiguousarray(w.x_sorted).view(np.int16)).view(torch.bfloat16).pin_memory()
     sh = torch.from_numpy(w.split_sizes).pin_memory()
-    gh = torch.from_numpy(w.gates).pin_memory()
+    gh = torch.from_numpy(w.gates).pin_memory() if w.gates is not None else None
     yh = torch.empty((R, H), dtype=torch.bfloat16).pin_memory()
     xd = torch.empty_like(x)
     sd = torch.empty_like(split)
-    gd = torch.empty_like(gates)
+    gd = torch.empty_like(gates) if gates is not None else None
 
     def e2e_step():
         xd.copy_(xh, non_blocking=True)
         sd.copy_(sh, non_blocking=True)
-        gd.copy_(gh, non_blocking=True)
+        if gd is not None:
+            gd.copy_(gh, non_blocking=True)
         mx.grouped_mlp_fwd(xd, sd, gd, w1q, w1s, w2q, w2s, y=y, workspace=ws)
         yh.copy_(y, non_blocking=True)
 
@@ -376,7 +392,7 @@ def run_native(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(world, a0.elapsed_time(a1) / args.steps)
     barrier(world)
-    h2d = xh.numel() * 2 + sh.numel() * 4 + gh.numel() * 4
+    h2d = xh.numel() * 2 + sh.numel() * 4 + (gh.numel() * 4 if gh is not None else 0)
     d2h = yh.numel() * 2
     e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -410,6 +426,10 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--oracle-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["mixtral", "llama", "fine", "tiny"], default=WORKLOAD,
+                    help="workload of the timed step (the headline line uses mixtral)")
+    ap.add_argument("--only", choices=["all", "fwd"], default="all",
+                    help="fwd: time the forward only and print a short line (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
