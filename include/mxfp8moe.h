@@ -128,6 +128,27 @@ int grouped_mlp_fwd_timed(const void* x_sorted, int64_t R, int64_t H, int64_t F,
                           void* y, void* workspace, size_t workspace_bytes, void* stream,
                           void* const* stage_events);
 
+/* grouped_mlp_fwd_noalloc -- grouped_mlp_fwd for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a library convenience, not a step of the method.
+ * Some callers cannot call cudaMalloc where they run the forward (allocator hooks, out-of-memory
+ * handlers, hosts whose memory pool is owned elsewhere).  This variant takes the same inputs and
+ * output as grouped_mlp_fwd but no workspace: its scratch is one 64 MiB file-scope device array
+ * that every GPU loading the library holds until the process exits.
+ *   - Problems whose grouped_mlp_workspace_size() exceeds 64 MiB return MXFP8_ERR_WORKSPACE
+ *     before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the array and leave the last call's contents in it; nothing
+ *     in it needs to start at zero.  Calls that overlap on the GPU race on it.
+ *   - Device-side conditions (split_sizes not summing to R, a timed-out wait) are not reported;
+ *     use grouped_mlp_fwd with a workspace and mxfp8_check_device_error to see them.
+ *   - Nothing is allocated or freed. */
+int grouped_mlp_fwd_noalloc(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E,
+                            const int32_t* split_sizes, const float* gates,
+                            const uint8_t* w1_q, const uint8_t* w1_sf,
+                            const uint8_t* w2_q, const uint8_t* w2_sf,
+                            void* y, void* stream);
+
 /* Byte offsets of the pieces of a grouped_mlp_fwd workspace, for inspection by tests:
  *   [0] error word (uint32)   [1] schedule          [2] quantized activations [R_pad, H]
  *   [3] their E8M0 bytes (MXFP8_SF_MMA layout)      [4] quantized intermediate [R_pad, F]

@@ -24,7 +24,7 @@ from . import build_ext
 __all__ = [
     "MXFP8Error", "ROWWISE", "COLWISE", "SF_COMPACT", "SF_MMA", "lib", "library_path",
     "mxfp8_sf_bytes", "mxfp8_quantize", "grouped_mlp_workspace_size", "grouped_mlp_workspace_layout",
-    "grouped_mlp_fwd", "mxfp8_check_device_error", "mxfp8_status_string", "mxfp8_abi_version",
+    "grouped_mlp_fwd", "grouped_mlp_fwd_noalloc", "mxfp8_check_device_error", "mxfp8_status_string", "mxfp8_abi_version",
 ]
 
 ROWWISE = 1
@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
             L.grouped_mlp_fwd.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P]
             L.grouped_mlp_fwd_timed.restype = i32
             L.grouped_mlp_fwd_timed.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P, P]
+            L.grouped_mlp_fwd_noalloc.restype = i32
+            L.grouped_mlp_fwd_noalloc.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P]
             L.mxfp8_check_device_error.restype = i32
             L.mxfp8_check_device_error.argtypes = [P, P, P]
             _lib = L
@@ -183,6 +185,20 @@ def grouped_mlp_fwd(x_sorted, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y=No
             raise ValueError("stage_events: 5 CUDA events that have been recorded at least once")
         arr = (ctypes.c_void_p * 5)(*handles)
         _check(lib().grouped_mlp_fwd_timed(*args, arr), "grouped_mlp_fwd_timed")
+    return y
+
+
+def grouped_mlp_fwd_noalloc(x_sorted, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y, stream=None):
+    """grouped_mlp_fwd without a workspace, for callers that cannot allocate device memory at the
+    call site: scratch comes from the library's fixed 64 MiB device array (shared by all calls on
+    a device; overlapping calls race).  `y` (bf16 [R, H]) must be passed in; nothing is
+    allocated.  Sizes whose workspace exceeds 64 MiB raise MXFP8Error (status ERR_WORKSPACE)."""
+    R, H = x_sorted.shape
+    E = int(split_sizes.numel())
+    F = int(w2_q.shape[1])
+    st = lib().grouped_mlp_fwd_noalloc(_ptr(x_sorted), R, H, F, E, _ptr(split_sizes), _ptr(gates), _ptr(w1_q),
+                                       _ptr(w1_sf), _ptr(w2_q), _ptr(w2_sf), _ptr(y), _stream(stream))
+    _check(st, "grouped_mlp_fwd_noalloc")
     return y
 
 
