@@ -4,15 +4,18 @@
 // approaches, item 2 (8-bit values, one scale per 32 consecutive values); the scale rule is the
 // OCP MX v1.0 one (see mx_device.cuh).
 //
-// HBM-bound design: one CTA of 256 threads owns a 32-row x 256-column tile.  Each thread loads
-// 8 consecutive bf16 of 4 rows with 128-bit loads (a warp reads 512 contiguous bytes of a row),
-// so the tile is read exactly once for both directions:
-//   - row-wise: a 32-block is 4 neighbouring lanes; its amax takes two xor-shuffles, then each
-//     lane writes its 8 codes as one 8-byte store (a warp writes 256 contiguous bytes);
-//   - column-wise: each thread reduces its 8 columns over its 4 rows, warps exchange the partial
-//     maxima through 8 KB of shared memory, and each thread quantizes its own 4 x 8 values with
-//     the column scales (stores again 256 contiguous bytes per warp and row).
-// No values are staged in shared memory; only the column maxima are.
+// HBM-bound design: one CTA of 256 threads owns a 64-row x 256-column tile.  Each thread loads
+// 8 consecutive bf16 of 8 rows with 128-bit loads (a warp reads 512 contiguous bytes of a row;
+// 128 bytes in flight per thread, 32 KB per CTA, up to 4 CTAs per SM) and keeps them packed, so
+// the tile is read exactly once for both directions:
+//   - row-wise: a 32-block is 4 neighbouring lanes; its amax is a packed bf16x2 max then two
+//     xor-shuffles, and each lane writes its 8 codes as one 8-byte store (a warp writes 256
+//     contiguous bytes);
+//   - column-wise: each thread reduces its 8 columns over its 8 rows (packed), the four warps of
+//     a 32-row block exchange the partial maxima through 4 KB of shared memory, and each thread
+//     quantizes its own 8 x 8 values with the column scales.
+// No values are staged in shared memory; only the column maxima are.  Max of magnitudes is exact
+// in bf16, so the block amax equals the one computed in higher precision.
 #include <cuda_runtime.h>
 
 #include "mx_device.cuh"
@@ -22,9 +25,10 @@
 namespace mx {
 namespace {
 
-constexpr int QT_ROWS = 32;
-constexpr int QT_COLS = 256;
 constexpr int QT_THREADS = 256;
+constexpr int QT_RPT = 8;                              // rows per thread
+constexpr int QT_ROWS = QT_RPT * (QT_THREADS / 32);    // 64 rows per tile
+constexpr int QT_COLS = 256;                           // 8 bf16 per lane
 
 struct QuantArgs {
   const uint16_t* x;
@@ -39,27 +43,55 @@ struct QuantArgs {
   int E;
 };
 
-__device__ __forceinline__ void unpack8(const uint4 w, float* v) {
-  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
-  v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
-  v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+// max of |a| and |b| per bf16 half (sign bits cleared, so the maximum is exact).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a & 0x7FFF7FFFu), "r"(b & 0x7FFF7FFFu));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a) { return a & 0x7FFF7FFFu; }
+
+__device__ __forceinline__ float max_halves(uint32_t m) { return fmaxf(bf16_lo(m), bf16_hi(m)); }
+
+// 8 bf16 (one uint4) times a common inverse scale -> 8 codes.
+__device__ __forceinline__ uint2 quant8_bf16(const uint4 w, float inv) {
+  uint2 o;
+  o.x = e4m3x2(bf16_lo(w.x) * inv, bf16_hi(w.x) * inv) | (e4m3x2(bf16_lo(w.y) * inv, bf16_hi(w.y) * inv) << 16);
+  o.y = e4m3x2(bf16_lo(w.z) * inv, bf16_hi(w.z) * inv) | (e4m3x2(bf16_lo(w.w) * inv, bf16_hi(w.w) * inv) << 16);
+  return o;
+}
+
+// 8 bf16 times 8 per-column inverse scales -> 8 codes.
+__device__ __forceinline__ uint2 quant8_bf16(const uint4 w, const float* inv) {
+  uint2 o;
+  o.x = e4m3x2(bf16_lo(w.x) * inv[0], bf16_hi(w.x) * inv[1]) |
+        (e4m3x2(bf16_lo(w.y) * inv[2], bf16_hi(w.y) * inv[3]) << 16);
+  o.y = e4m3x2(bf16_lo(w.z) * inv[4], bf16_hi(w.z) * inv[5]) |
+        (e4m3x2(bf16_lo(w.w) * inv[6], bf16_hi(w.w) * inv[7]) << 16);
+  return o;
 }
 
 // ROW / COL: directions produced.  MMA: scale bytes in the tensor-core layout instead of the
 // compact one.  GATHER: rows are the expert-padded row space of a grouped MLP; padded row p of
 // expert e reads source row row_off[e] + (p - pad_off[e]) or is a zero row past the expert's
 // count.
+//
+// Thread (warp w, lane l) owns rows 8w..8w+7 of the 64-row tile and columns 8l..8l+7 of the
+// 256-column tile, kept as packed bf16 (8 x 16 bytes in flight per thread).  A column-wise block
+// of 32 rows is warps 4b..4b+3.
 template <bool ROW, bool COL, bool MMA, bool GATHER>
-__global__ void __launch_bounds__(QT_THREADS) k_quantize(const QuantArgs a) {
+__global__ void __launch_bounds__(QT_THREADS, (ROW && COL) ? 3 : 4) k_quantize(const QuantArgs a) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t K = a.K;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * QT_ROWS;
+  const int64_t rw0 = row0 + warp * QT_RPT;             // first row of this thread
   const int64_t col = static_cast<int64_t>(blockIdx.y) * QT_COLS + lane * 8;
   const bool col_ok = col < K;   // K % 32 == 0, so a 4-lane block group is all in or all out
 
-  int64_t src[4];
+  int64_t src0;      // source row of this thread's first row (rows are consecutive)
+  int nsrc;          // how many of its QT_RPT rows exist in the source
   if constexpr (GATHER) {
     const int32_t pad_rows = a.meta->pad_rows;
     if (row0 >= pad_rows) return;  // whole tile past the last expert (pad_rows % 128 == 0)
@@ -70,90 +102,87 @@ __global__ void __launch_bounds__(QT_THREADS) k_quantize(const QuantArgs a) {
       const int mid = (lo + hi) >> 1;
       if (pad_off[mid] <= row0) lo = mid; else hi = mid;
     }
-    const int64_t local0 = row0 - pad_off[lo] + warp * 4;
+    const int64_t local = rw0 - pad_off[lo];
     const int64_t cnt = row_off[lo + 1] - row_off[lo];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) src[i] = (local0 + i < cnt) ? row_off[lo] + local0 + i : -1;
+    src0 = row_off[lo] + local;
+    const int64_t left = cnt - local;
+    nsrc = left <= 0 ? 0 : (left >= QT_RPT ? QT_RPT : static_cast<int>(left));
   } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t r = row0 + warp * 4 + i;
-      src[i] = r < a.M ? r : -1;
-    }
+    src0 = rw0;
+    const int64_t left = a.M - rw0;
+    nsrc = left <= 0 ? 0 : (left >= QT_RPT ? QT_RPT : static_cast<int>(left));
   }
 
-  float v[4][8];
-  uint4 w[4];
+  uint4 w[QT_RPT];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (src[i] >= 0 && col_ok)
-      w[i] = __ldcs(reinterpret_cast<const uint4*>(a.x + src[i] * K + col));
+  for (int i = 0; i < QT_RPT; ++i) {
+    if (i < nsrc && col_ok)
+      w[i] = __ldcs(reinterpret_cast<const uint4*>(a.x + (src0 + i) * K + col));
     else
       w[i] = make_uint4(0u, 0u, 0u, 0u);
   }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) unpack8(w[i], v[i]);
 
   if constexpr (ROW) {
+    // rows written: all QT_RPT in gather mode (padding rows become zeros), else the real ones
+    const int nout = GATHER ? QT_RPT : nsrc;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float m = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(v[i][k]));
+    for (int i = 0; i < QT_RPT; ++i) {
+      const uint32_t m2 = absmax_bf16x2(absmax_bf16x2(w[i].x, w[i].y), absmax_bf16x2(w[i].z, w[i].w));
+      float m = max_halves(m2);
       m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
       const uint32_t sfb = e8m0_from_amax(m);
-      const uint2 q = quant8(v[i], e8m0_inverse_scale(sfb));
-      const int64_t r_out = row0 + warp * 4 + i;
-      const bool row_out_ok = GATHER ? true : (src[i] >= 0);
-      if (row_out_ok && col_ok) {
-        __stcs(reinterpret_cast<uint2*>(a.q_row + r_out * K + col), q);
+      if (i < nout && col_ok) {
+        const int64_t r = rw0 + i;
+        __stcs(reinterpret_cast<uint2*>(a.q_row + r * K + col), quant8_bf16(w[i], e8m0_inverse_scale(sfb)));
         if ((lane & 3) == 0) {
           const int64_t blk = col >> 5;
           if constexpr (MMA)
-            a.sf_row[sf_mma_offset(r_out, blk, a.kt_row)] = static_cast<uint8_t>(sfb);
+            a.sf_row[sf_mma_offset(r, blk, a.kt_row)] = static_cast<uint8_t>(sfb);
           else
-            a.sf_row[r_out * (K >> 5) + blk] = static_cast<uint8_t>(sfb);
+            a.sf_row[r * (K >> 5) + blk] = static_cast<uint8_t>(sfb);
         }
       }
     }
   }
 
   if constexpr (COL) {
-    __shared__ __align__(16) float red[QT_THREADS / 32][QT_COLS];
-    float cm[8];
+    __shared__ __align__(16) uint4 red[QT_THREADS / 32][32];
+    uint4 cm = make_uint4(absmax_bf16x2(w[0].x), absmax_bf16x2(w[0].y), absmax_bf16x2(w[0].z),
+                          absmax_bf16x2(w[0].w));
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      cm[k] = fmaxf(fmaxf(fabsf(v[0][k]), fabsf(v[1][k])), fmaxf(fabsf(v[2][k]), fabsf(v[3][k])));
+    for (int i = 1; i < QT_RPT; ++i) {
+      cm.x = absmax_bf16x2(cm.x, w[i].x);
+      cm.y = absmax_bf16x2(cm.y, w[i].y);
+      cm.z = absmax_bf16x2(cm.z, w[i].z);
+      cm.w = absmax_bf16x2(cm.w, w[i].w);
     }
-    reinterpret_cast<float4*>(&red[warp][lane * 8])[0] = make_float4(cm[0], cm[1], cm[2], cm[3]);
-    reinterpret_cast<float4*>(&red[warp][lane * 8])[1] = make_float4(cm[4], cm[5], cm[6], cm[7]);
+    red[warp][lane] = cm;
     __syncthreads();
+    const int b = warp >> 2;   // column block (32 rows) this warp belongs to
 #pragma unroll
-    for (int ww = 0; ww < QT_THREADS / 32; ++ww) {
-      const float4 lo = reinterpret_cast<const float4*>(&red[ww][lane * 8])[0];
-      const float4 hi = reinterpret_cast<const float4*>(&red[ww][lane * 8])[1];
-      cm[0] = fmaxf(cm[0], lo.x); cm[1] = fmaxf(cm[1], lo.y); cm[2] = fmaxf(cm[2], lo.z); cm[3] = fmaxf(cm[3], lo.w);
-      cm[4] = fmaxf(cm[4], hi.x); cm[5] = fmaxf(cm[5], hi.y); cm[6] = fmaxf(cm[6], hi.z); cm[7] = fmaxf(cm[7], hi.w);
+    for (int ww = 0; ww < 4; ++ww) {
+      const uint4 o = red[4 * b + ww][lane];
+      cm.x = absmax_bf16x2(cm.x, o.x);
+      cm.y = absmax_bf16x2(cm.y, o.y);
+      cm.z = absmax_bf16x2(cm.z, o.z);
+      cm.w = absmax_bf16x2(cm.w, o.w);
     }
+    const float cmax[8] = {bf16_lo(cm.x), bf16_hi(cm.x), bf16_lo(cm.y), bf16_hi(cm.y),
+                           bf16_lo(cm.z), bf16_hi(cm.z), bf16_lo(cm.w), bf16_hi(cm.w)};
     uint32_t sfb[8];
     float inv[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      sfb[k] = e8m0_from_amax(cm[k]);
+      sfb[k] = e8m0_from_amax(cmax[k]);
       inv[k] = e8m0_inverse_scale(sfb[k]);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (src[i] >= 0 && col_ok) {
-        uint2 q;
-        q.x = e4m3x2(v[i][0] * inv[0], v[i][1] * inv[1]) | (e4m3x2(v[i][2] * inv[2], v[i][3] * inv[3]) << 16);
-        q.y = e4m3x2(v[i][4] * inv[4], v[i][5] * inv[5]) | (e4m3x2(v[i][6] * inv[6], v[i][7] * inv[7]) << 16);
-        __stcs(reinterpret_cast<uint2*>(a.q_col + (row0 + warp * 4 + i) * K + col), q);
-      }
-    }
-    if (warp == 0 && col_ok) {
-      const int64_t rb = row0 >> 5;
+    for (int i = 0; i < QT_RPT; ++i)
+      if (i < nsrc && col_ok)
+        __stcs(reinterpret_cast<uint2*>(a.q_col + (rw0 + i) * K + col), quant8_bf16(w[i], inv));
+    const int64_t rb = (row0 >> 5) + b;
+    if ((warp & 3) == 0 && col_ok && rb * 32 < a.M) {
       if constexpr (MMA) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) a.sf_col[sf_mma_offset(col + k, rb, a.kt_col)] = static_cast<uint8_t>(sfb[k]);
@@ -206,7 +235,8 @@ cudaError_t launch_quantize_gather(const void* x, int64_t R, int64_t H, const Sc
   a.kt_row = H / 128;
   a.meta = meta;
   a.E = E;
-  const dim3 grid(static_cast<unsigned>(r_pad / QT_ROWS), static_cast<unsigned>((H + QT_COLS - 1) / QT_COLS));
+  const dim3 grid(static_cast<unsigned>((r_pad + QT_ROWS - 1) / QT_ROWS),
+                  static_cast<unsigned>((H + QT_COLS - 1) / QT_COLS));
   k_quantize<true, false, true, true><<<grid, QT_THREADS, 0, stream>>>(a);
   return cudaGetLastError();
 }
