@@ -18,15 +18,17 @@
 //   4. k_grouped_gemm<GEMM_OUT>     per tile (expert e, 128 rows, BN columns of H):
 //                    y = h_q W2[e]^T -> bf16, stored only for the expert's real rows.
 //
-// GEMM kernel structure (persistent, one 320-thread CTA per SM, 4-stage shared-memory ring):
-//   warp 0      TMA producer: A tile (128 rows x 128 K bytes), B tile (BN rows x 128), and the
-//               512-byte scale atoms of both, all completing on one mbarrier per stage.
-//   warp 1      allocates TMEM; one thread copies the stage's scale atoms to TMEM (tcgen05.cp)
-//               and issues 4 block-scaled MMAs (M=128, N=BN, K=32 each) into one fp32
-//               accumulator of BN columns, then commits the stage back to the producer.
-//   warps 2-9   epilogue: each warp reads its 32 TMEM lanes (rows) and half of the columns into
-//               registers, releases the accumulator at once (so the next tile's MMAs overlap
-//               the epilogue math), then computes and stores.
+// GEMM kernel structure (persistent, one 512-thread CTA per SM, 4-stage shared-memory ring):
+//   TMA producer  A tile (128 rows x 128 K bytes), B tile (BN rows x 128) and the 512-byte scale
+//                 atoms of both, all completing on one mbarrier per stage.
+//   scale warps   four warps copy the stage's scale atoms into TMEM with tcgen05.st (one TMEM lane
+//                 quarter each) and signal the MMA issuer; doing this with tcgen05.cp from the
+//                 MMA thread stalled the tensor pipe (about a third of the kernel's time).
+//   MMA issuer    allocates TMEM; one thread issues 4 block-scaled MMAs (M=128, N=BN, K=32 each)
+//                 per stage into one fp32 accumulator of BN columns and commits the stage back.
+//   epilogue      eight warps read their 32 TMEM lanes (rows) and half of the columns into
+//                 registers, release the accumulator at once (so the next tile's MMAs overlap
+//                 the epilogue math), then compute and store.
 // Every mbarrier wait is bounded; a timeout sets a bit in the workspace error word and all roles
 // drain and exit.
 #include <cuda.h>
@@ -48,10 +50,26 @@ constexpr int BK = 128;                    // K per stage: 128 E4M3 bytes = one 
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;           // 16 KB
 constexpr int B_BYTES_MAX = 256 * BK;      // 32 KB (N = 256)
-constexpr int SF_ATOM = 512;
+constexpr int SF_ATOM = 512;               // 128 rows x 4 scale blocks
 constexpr int STAGE_BYTES = 51200;         // A + B + 3 scale atoms, rounded up to 1 KB
-constexpr int NUM_THREADS = 320;
+// Warp roles (4 warpgroups):
+//   warpgroup 0 (warps 0-3)   scale staging: warp w copies the stage's scale atoms from shared
+//                             memory into TMEM lanes 32w..32w+31 (tcgen05.st)
+//   warpgroup 1 (warps 4-7)   warp 4: TMA producer (lane 0 issues); warp 5: TMEM allocation and
+//                             MMA issue (lane 0); warps 6-7 idle
+//   warpgroups 2-3 (8-15)     epilogue: warp w reads TMEM lanes 32*(w%4).. and half (w-8)/4 of
+//                             the accumulator columns
+// Registers: launched with 128 per thread; warpgroups 0-1 give theirs down to 56 so that the
+// epilogue warpgroups can hold 200 (4*32*56*2 + 8*32*200 = 512*128).
+constexpr int NUM_THREADS = 512;
+constexpr int WARP_PRODUCER = 4;
+constexpr int WARP_MMA = 5;
+constexpr int FIRST_EPI_WARP = 8;
 constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_SF_WARPS = 4;
+constexpr uint32_t REGS_LOW = 56;
+constexpr uint32_t REGS_HIGH = 200;
+static_assert(2 * 128 * REGS_LOW + 256 * REGS_HIGH == NUM_THREADS * 128, "register split must equal the launch pool");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;            // accumulator: up to 256 fp32 columns
 constexpr uint32_t SFA_COL = 256;          // 4 columns per stage
@@ -74,6 +92,7 @@ struct GemmParams {
   int BN;                  // MMA N (256, or 128 for GEMM_OUT when H % 256 != 0)
   int b_rows_per_expert;   // 2F (GEMM_SWIGLU) or H (GEMM_OUT)
   int F;                   // GEMM_SWIGLU: row offset of the up projection inside an expert
+  int n_fastest;           // tile order inside an expert: 1 = column tiles fastest, 0 = row tiles
   // GEMM_SWIGLU epilogue
   const float* gates;
   uint8_t* hq;
@@ -90,6 +109,10 @@ struct TileInfo {
   int e, n, pad_row0, src_row0, valid;
 };
 
+// Work unit u -> (expert, column tile, 128-row tile).  Units are ordered expert by expert; inside
+// an expert either the row tiles or the column tiles run fastest, so the tiles in flight at once
+// share one operand in L2 (GEMM 1: the expert's activations and a few weight column tiles;
+// GEMM 2: one row tile of the intermediate and the expert's whole W2).
 __device__ __forceinline__ void decode_unit(int u, const GemmParams& p, TileInfo& t) {
   const int32_t* row_off = reinterpret_cast<const int32_t*>(p.meta + 1);
   const int32_t* pad_off = row_off + (p.E + 1);
@@ -103,8 +126,14 @@ __device__ __forceinline__ void decode_unit(int u, const GemmParams& p, TileInfo
   const int m0 = __ldg(mt_off + e);
   const int mt_e = __ldg(mt_off + e + 1) - m0;
   const int local = u - m0 * p.NT;
-  const int n = local / mt_e;
-  const int tt = local - n * mt_e;
+  int n, tt;
+  if (p.n_fastest) {
+    tt = local / p.NT;
+    n = local - tt * p.NT;
+  } else {
+    n = local / mt_e;
+    tt = local - n * mt_e;
+  }
   const int r0 = __ldg(row_off + e);
   t.e = e;
   t.n = n;
@@ -113,14 +142,53 @@ __device__ __forceinline__ void decode_unit(int u, const GemmParams& p, TileInfo
   t.valid = min(BM, __ldg(row_off + e + 1) - r0 - BM * tt);
 }
 
+// First row of B box i (128 rows) of a tile: GEMM 1 boxes are the gate rows and the up rows of
+// column tile n; GEMM 2 boxes are consecutive W2 rows.
+template <int MODE>
+__device__ __forceinline__ int b_box_row(const GemmParams& p, const TileInfo& t, int i) {
+  const int brow0 = t.e * p.b_rows_per_expert;
+  return MODE == GEMM_SWIGLU ? brow0 + i * p.F + t.n * 128 : brow0 + t.n * p.BN + i * 128;
+}
+
+// Lane 0 waits, the whole warp learns the outcome (keeps .sync.aligned instructions convergent).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort, uint64_t timeout,
+                                          uint32_t* err, uint32_t err_bit, int lane) {
+  int ok = 1;
+  if (lane == 0) {
+    ok = mbar_wait_bounded(bar, parity, abort, timeout) ? 1 : 0;
+    if (!ok) {
+      atomicOr(err, err_bit);
+      *const_cast<volatile int*>(abort) = 1;
+    }
+  }
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint4 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);  // tiles and scale atoms landed
+  uint64_t* sf_full = full + STAGES;                                            // scales written to TMEM
+  uint64_t* empty = sf_full + STAGES;                                           // MMAs done with the stage
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drained = acc_empty + 1;
@@ -133,6 +201,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
+      mbar_init(&sf_full[s], NUM_SF_WARPS);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
@@ -142,7 +211,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 1) {
+  if (warp == WARP_MMA) {
     tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
   }
@@ -154,131 +223,163 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int total_units = p.meta->num_mtiles * p.NT;
   const int BN = p.BN;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer ----------------
-    uint32_t issued_mask = 0, issued_parity = 0;
+  if (warp < NUM_SF_WARPS) {
+    regs_dec<REGS_LOW>();
+    // ---------------- scale staging: shared memory -> TMEM (lanes of quarter `warp`) ----------------
+    // Doing this with tcgen05.cp from the MMA thread stalled the tensor pipe (about a third of the
+    // kernel's time); reading the atoms from global memory here instead of from the stage was
+    // slower still (load latency under the TMA traffic).
+    const uint32_t t_lanes = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int nsfb = BN / 128;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    const uint32_t stage_tx = A_BYTES + BN * BK + SF_ATOM + (BN / 128) * SF_ATOM;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      TileInfo t;
-      decode_unit(u, p, t);
-      const int a_tile = t.pad_row0 / BM;
       for (int kb = 0; kb < p.KT; ++kb) {
-        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns)) {
-          atomicOr(p.err, ERR_TIMEOUT_PRODUCER);
-          *abort_flag = 1;
+        if (!warp_wait(&full[stage], phase, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_SF, lane)) {
           ok = false;
           break;
         }
-        uint8_t* sA = smem + stage * STAGE_BYTES;
-        uint8_t* sB = sA + A_BYTES;
-        uint8_t* sSFA = sB + B_BYTES_MAX;
-        uint8_t* sSFB = sSFA + SF_ATOM;
-        mbar_arrive_expect_tx(&full[stage], stage_tx);
-        tma_load_2d(sA, &tmA, &full[stage], kb * BK, t.pad_row0);
-        bulk_load(sSFA, p.a_sf + (static_cast<int64_t>(a_tile) * p.KT + kb) * SF_ATOM, SF_ATOM, &full[stage]);
-        const int brow0 = t.e * p.b_rows_per_expert;
-        if (MODE == GEMM_SWIGLU) {
-          const int g0 = brow0 + t.n * 128;          // gate rows
-          const int u0 = brow0 + p.F + t.n * 128;    // up rows
-          tma_load_2d(sB, &tmB, &full[stage], kb * BK, g0);
-          tma_load_2d(sB + 128 * BK, &tmB, &full[stage], kb * BK, u0);
-          bulk_load(sSFB, p.b_sf + (static_cast<int64_t>(g0 / 128) * p.KT + kb) * SF_ATOM, SF_ATOM, &full[stage]);
-          bulk_load(sSFB + SF_ATOM, p.b_sf + (static_cast<int64_t>(u0 / 128) * p.KT + kb) * SF_ATOM, SF_ATOM,
-                    &full[stage]);
-        } else {
-          for (int i = 0; i < BN / 128; ++i) {
-            const int b0 = brow0 + t.n * BN + i * 128;
-            tma_load_2d(sB + i * 128 * BK, &tmB, &full[stage], kb * BK, b0);
-            bulk_load(sSFB + i * SF_ATOM, p.b_sf + (static_cast<int64_t>(b0 / 128) * p.KT + kb) * SF_ATOM, SF_ATOM,
-                      &full[stage]);
+        // row `lane` of each atom -> TMEM lane 32*warp + lane, 4 columns: every lane quarter holds
+        // the whole atom, the layout the block-scaled MMA reads
+        const uint8_t* sSFA = smem + stage * STAGE_BYTES + A_BYTES + B_BYTES_MAX;
+        const uint8_t* sSFB = sSFA + SF_ATOM;
+        tmem_st_32x32b_x4(t_lanes + SFA_COL + 4 * stage, *reinterpret_cast<const uint4*>(sSFA + lane * 16));
+        tmem_st_32x32b_x4(t_lanes + SFB_COL + 8 * stage, *reinterpret_cast<const uint4*>(sSFB + lane * 16));
+        if (nsfb == 2)
+          tmem_st_32x32b_x4(t_lanes + SFB_COL + 8 * stage + 4,
+                            *reinterpret_cast<const uint4*>(sSFB + SF_ATOM + lane * 16));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_full[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp < FIRST_EPI_WARP) {
+    regs_dec<REGS_LOW>();
+    if (warp == WARP_PRODUCER) {
+      // ---------------- TMA producer (lane 0 issues) ----------------
+      uint32_t issued_mask = 0, issued_parity = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t stage_tx = A_BYTES + BN * BK + SF_ATOM + (BN / 128) * SF_ATOM;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        TileInfo t;
+        decode_unit(u, p, t);
+        const int a_tile = t.pad_row0 / BM;
+        for (int kb = 0; kb < p.KT; ++kb) {
+          if (!warp_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_PRODUCER, lane)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            uint8_t* sA = smem + stage * STAGE_BYTES;
+            uint8_t* sB = sA + A_BYTES;
+            uint8_t* sSFA = sB + B_BYTES_MAX;
+            uint8_t* sSFB = sSFA + SF_ATOM;
+            mbar_arrive_expect_tx(&full[stage], stage_tx);
+            tma_load_2d(sA, &tmA, &full[stage], kb * BK, t.pad_row0);
+            bulk_load(sSFA, p.a_sf + (static_cast<int64_t>(a_tile) * p.KT + kb) * SF_ATOM, SF_ATOM, &full[stage]);
+            if (MODE == GEMM_SWIGLU) {
+              const int g0 = b_box_row<MODE>(p, t, 0);   // gate rows
+              const int u0 = b_box_row<MODE>(p, t, 1);   // up rows
+              tma_load_2d(sB, &tmB, &full[stage], kb * BK, g0);
+              tma_load_2d(sB + 128 * BK, &tmB, &full[stage], kb * BK, u0);
+              bulk_load(sSFB, p.b_sf + (static_cast<int64_t>(g0 / 128) * p.KT + kb) * SF_ATOM, SF_ATOM, &full[stage]);
+              bulk_load(sSFB + SF_ATOM, p.b_sf + (static_cast<int64_t>(u0 / 128) * p.KT + kb) * SF_ATOM, SF_ATOM,
+                        &full[stage]);
+            } else {
+              // written out rather than looped: a runtime-count loop around these copies measured
+              // 25% slower (GroupedLinear 1, same copies in the same order)
+              const int b0 = b_box_row<MODE>(p, t, 0);
+              tma_load_2d(sB, &tmB, &full[stage], kb * BK, b0);
+              if (BN == 256) tma_load_2d(sB + 128 * BK, &tmB, &full[stage], kb * BK, b0 + 128);
+              bulk_load(sSFB, p.b_sf + (static_cast<int64_t>(b0 / 128) * p.KT + kb) * SF_ATOM, SF_ATOM, &full[stage]);
+              if (BN == 256)
+                bulk_load(sSFB + SF_ATOM, p.b_sf + (static_cast<int64_t>(b0 / 128 + 1) * p.KT + kb) * SF_ATOM, SF_ATOM,
+                          &full[stage]);
+            }
+          }
+          __syncwarp();
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
-        issued_mask |= 1u << stage;
-        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
       }
-    }
-    // Every copy this thread started must land before the CTA may exit.
-    for (int s = 0; s < STAGES; ++s)
-      if ((issued_mask >> s) & 1u)
-        if (!mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, p.timeout_ns))
-          atomicOr(p.err, ERR_TIMEOUT_DRAIN);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
-    const uint32_t idesc = idesc_mxf8_e4m3(BM, BN);
-    int stage = 0;
-    uint32_t phase = 0, acc_phase = 0;
-    bool issued = false, ok = true;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
-        atomicOr(p.err, ERR_TIMEOUT_MMA);
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
-      for (int kb = 0; kb < p.KT; ++kb) {
-        if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.timeout_ns)) {
-          atomicOr(p.err, ERR_TIMEOUT_MMA);
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
+      // Every copy this warp started must land before the CTA may exit.
+      if (lane == 0)
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued_mask >> s) & 1u)
+            if (!mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, p.timeout_ns))
+              atomicOr(p.err, ERR_TIMEOUT_DRAIN);
+      __syncwarp();
+    } else if (warp == WARP_MMA) {
+      // ---------------- MMA issuer (lane 0 issues) ----------------
+      const uint32_t idesc = idesc_mxf8_e4m3(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool issued = false, ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        if (!warp_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_MMA, lane)) break;
         tc_fence_after();
-        const uint8_t* sA = smem + stage * STAGE_BYTES;
-        const uint8_t* sB = sA + A_BYTES;
-        const uint8_t* sSFA = sB + B_BYTES_MAX;
-        const uint8_t* sSFB = sSFA + SF_ATOM;
-        const uint32_t t_sfa = tmem + SFA_COL + 4 * stage;
-        const uint32_t t_sfb = tmem + SFB_COL + 8 * stage;
-        tc_copy_sf(t_sfa, sdesc_sf_atom(smem_u32(sSFA)));
-        for (int i = 0; i < BN / 128; ++i) tc_copy_sf(t_sfb + 4 * i, sdesc_sf_atom(smem_u32(sSFB + i * SF_ATOM)));
-        const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+        for (int kb = 0; kb < p.KT; ++kb) {
+          // sf_full implies full: the scale warps waited for the stage's data before signalling
+          if (!warp_wait(&sf_full[stage], phase, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_MMA, lane)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint8_t* sA = smem + stage * STAGE_BYTES;
+            const uint8_t* sB = sA + A_BYTES;
+            const uint32_t t_sfa = tmem + SFA_COL + 4 * stage;
+            const uint32_t t_sfb = tmem + SFB_COL + 8 * stage;
+            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
-        for (int k = 0; k < BK / 32; ++k) {
-          tc_mma_mxf8(tmem + ACC_COL, sdesc_kmajor_sw128(a0 + 32 * k), sdesc_kmajor_sw128(b0 + 32 * k),
-                      idesc_with_sf_id(idesc, k), t_sfa, t_sfb, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < BK / 32; ++k) {
+              tc_mma_mxf8(tmem + ACC_COL, sdesc_kmajor_sw128(a0 + 32 * k), sdesc_kmajor_sw128(b0 + 32 * k),
+                          idesc_with_sf_id(idesc, k), t_sfa, t_sfb, (kb | k) != 0 ? 1u : 0u);
+            }
+            tc_commit(&empty[stage]);
+          }
+          __syncwarp();
+          issued = true;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        issued = true;
-        tc_commit(&empty[stage]);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (!ok) break;
+        if (lane == 0) tc_commit(acc_full);
+        __syncwarp();
+        acc_phase ^= 1u;
       }
-      if (!ok) break;
-      tc_commit(acc_full);
-      acc_phase ^= 1u;
+      if (issued && lane == 0) {
+        tc_commit(drained);
+        if (!mbar_wait_bounded(drained, 0, nullptr, p.timeout_ns)) atomicOr(p.err, ERR_TIMEOUT_DRAIN);
+      }
+      __syncwarp();
     }
-    if (issued) {
-      tc_commit(drained);
-      if (!mbar_wait_bounded(drained, 0, nullptr, p.timeout_ns)) atomicOr(p.err, ERR_TIMEOUT_DRAIN);
-    }
-  } else if (warp >= 2) {
+  } else {
+    regs_inc<REGS_HIGH>();
     // ---------------- epilogue ----------------
-    const int quarter = warp & 3;                  // TMEM lanes this warp may read
-    const int half = (warp - 2) >> 2;              // which half of the accumulator columns
-    const int r = quarter * 32 + lane;             // tile row held by this thread
+    const int quarter = warp & 3;                        // TMEM lanes this warp may read
+    const int half = (warp - FIRST_EPI_WARP) >> 2;       // which half of the accumulator columns
+    const int r = quarter * 32 + lane;                   // tile row held by this thread
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
       TileInfo t;
       decode_unit(u, p, t);
-      int ok = 1;
-      if (lane == 0) {
-        ok = mbar_wait_bounded(acc_full, acc_phase, abort_flag, p.timeout_ns) ? 1 : 0;
-        if (!ok) {
-          atomicOr(p.err, ERR_TIMEOUT_EPILOGUE);
-          *abort_flag = 1;
-        }
-      }
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) break;
+      if (!warp_wait(acc_full, acc_phase, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_EPILOGUE, lane)) break;
       tc_fence_after();
       uint32_t v[128];
       if (MODE == GEMM_SWIGLU) {
@@ -323,12 +424,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           const uint32_t sfb = e8m0_from_amax(amax);
           const float inv = e8m0_inverse_scale(sfb);
-          uint4 o0, o1;
-          uint2 t0 = quant8(h + 0, inv), t1 = quant8(h + 8, inv), t2 = quant8(h + 16, inv), t3 = quant8(h + 24, inv);
-          o0 = make_uint4(t0.x, t0.y, t1.x, t1.y);
-          o1 = make_uint4(t2.x, t2.y, t3.x, t3.y);
-          reinterpret_cast<uint4*>(hrow + 32 * b)[0] = o0;
-          reinterpret_cast<uint4*>(hrow + 32 * b)[1] = o1;
+          const uint2 t0 = quant8(h + 0, inv), t1 = quant8(h + 8, inv), t2 = quant8(h + 16, inv),
+                      t3 = quant8(h + 24, inv);
+          reinterpret_cast<uint4*>(hrow + 32 * b)[0] = make_uint4(t0.x, t0.y, t1.x, t1.y);
+          reinterpret_cast<uint4*>(hrow + 32 * b)[1] = make_uint4(t2.x, t2.y, t3.x, t3.y);
           sf_pair |= sfb << (8 * b);
         }
         // scale bytes of blocks (2*half, 2*half+1) of column tile n for padded row pad_row0 + r
@@ -357,7 +456,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == WARP_MMA) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -368,6 +467,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 __global__ void __launch_bounds__(1024) k_schedule(const int32_t* split, int E, int64_t R, SchedHeader* meta) {
   __shared__ long long s_rows[1024];
   __shared__ int s_tiles[1024];
+
   __shared__ int s_neg;
   const int t = threadIdx.x;
   if (t == 0) s_neg = 0;
@@ -513,12 +613,14 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p1.BN = 256;
   p1.b_rows_per_expert = static_cast<int>(2 * F);
   p1.F = static_cast<int>(F);
+  p1.n_fastest = 0;
   p1.gates = gates;
   p1.hq = hq;
   p1.hsf = hsf;
   p1.ldh = F;
   p1.err = &meta->error;
   p1.timeout_ns = kWaitTimeoutNs;
+  // persistent: one CTA per SM (shared memory, registers and TMEM each allow only one)
   const int grid1 = static_cast<int>(std::min<int64_t>(dev->sms, static_cast<int64_t>(max_mtiles) * p1.NT));
   k_grouped_gemm<GEMM_SWIGLU><<<grid1, NUM_THREADS, SMEM_BYTES, stream>>>(mA1, mB1, p1);
   if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
@@ -534,6 +636,7 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p2.NT = static_cast<int>(H / p2.BN);
   p2.b_rows_per_expert = static_cast<int>(H);
   p2.F = static_cast<int>(F);
+  p2.n_fastest = 1;
   p2.y = static_cast<uint16_t*>(y);
   p2.ldy = H;
   p2.err = &meta->error;

@@ -14,8 +14,9 @@ enum : uint32_t {
   ERR_TIMEOUT_MMA = 1u << 9,      // MMA issuer gave up waiting for data or a free accumulator
   ERR_TIMEOUT_EPILOGUE = 1u << 10,// epilogue gave up waiting for an accumulator
   ERR_TIMEOUT_DRAIN = 1u << 11,   // teardown gave up waiting for copies / MMAs in flight
+  ERR_TIMEOUT_SF = 1u << 12,      // scale-staging warps gave up waiting for a free TMEM slot
 };
-constexpr uint32_t ERR_TIMEOUT_MASK = 0xF00u;
+constexpr uint32_t ERR_TIMEOUT_MASK = 0x1F00u;
 
 // Device schedule written by the schedule kernel at the start of the workspace.  Arrays of E+1
 // int32 follow the header: row_off (prefix sums of split_sizes), pad_off (prefix sums of
