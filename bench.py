@@ -363,6 +363,51 @@ def run_native(args, world, rank, local):
              "l2": "no flush: 470 MB input > L2"}
     del qx, qout
 
+    # ---- the MoE layer around the forward: permute -> gathered forward -> combine ----
+    layer = None
+    if w.topk_experts is not None:
+        xt = bf(w.x_tokens)
+        exd = torch.from_numpy(w.topk_experts).to(dev)
+        gtd = torch.from_numpy(w.topk_gates).to(dev)
+        T, k = w.topk_experts.shape
+        pws = torch.empty(max(256, mx.moe_permute_workspace_size(T, k, E)), dtype=torch.uint8, device=dev)
+        p_split = torch.empty(E, dtype=torch.int32, device=dev)
+        p_ros = torch.empty((T, k), dtype=torch.int32, device=dev)
+        p_tor = torch.empty(T * k, dtype=torch.int32, device=dev)
+        p_gs = torch.empty(T * k, dtype=torch.float32, device=dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        p_out = (p_split, p_ros, p_tor, p_gs)
+
+        def layer_step(evs):
+            evs[0].record()
+            mx.moe_permute(exd, gtd, E, workspace=pws, out=p_out)
+            evs[1].record()
+            mx.grouped_mlp_fwd_tokens(xt, p_tor, p_split, p_gs, w1q, w1s, w2q, w2s, y=y, workspace=ws)
+            evs[2].record()
+            mx.moe_combine(y, p_ros, out=out)
+            evs[3].record()
+
+        lev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(max(3, args.steps))]
+        for _ in range(max(3, args.warmup)):
+            layer_step(lev[0])
+        torch.cuda.synchronize()
+        for evs in lev:
+            layer_step(evs)
+        torch.cuda.synchronize()
+        for wsx in (pws, ws):
+            st, bits = mx.mxfp8_check_device_error(wsx)
+            if st != 0:
+                raise RuntimeError(f"device error word {bits:#x} in the MoE layer")
+        part = [sum(e[j].elapsed_time(e[j + 1]) for e in lev) / len(lev) for j in range(3)]
+        c_bytes = T * k * H * 2 + T * H * 2 + T * k * 4
+        layer = {"tokens": T, "topk": k, "ms": sum(part), "permute_ms": part[0], "fwd_tokens_ms": part[1],
+                 "combine_ms": part[2], "tflops": flops / (sum(part) * 1e-3) / 1e12,
+                 "combine": {"bound": "hbm", "algorithmic_bytes_per_launch": c_bytes,
+                             "achieved": c_bytes / (part[2] * 1e-3) / 1e9, "unit": "GB/s",
+                             "frac": c_bytes / (part[2] * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+                 "l2": "no flush: per-launch inputs above L2 except the permute's 128 KB of ids"}
+        del xt, out
+
     # ---- end to end through the public API with host buffers ----
     # Every step copies its inputs from pinned host memory and its output back.  Steps are
     # pipelined over three streams with double-buffered device x / y: the host->device copy of
@@ -423,7 +468,10 @@ def run_native(args, world, rank, local):
     # ---- CPU oracle baseline on a bounded sample (rank 0 only, N=1 only) ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # calibrate on a short call, then time one call sized to about --cpu-seconds
         s = OracleSample(w, nrows=args.oracle_rows)
+        t = s.run()
+        s.nrows = max(1, min(s.n_avail, int(s.nrows * args.cpu_seconds / max(t, 1e-3))))
         t = s.run()
         cpu = {"value": s.nrows * s.flops_per_row / t / 1e12, "unit": "TFLOP/s", "cores": s.threads,
                "kind": "oracle", "sample": s.describe(), "seconds": t}
@@ -433,7 +481,7 @@ def run_native(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
-            "config": workload_config(w), "roofline": roofline, "quantize": quant, "e2e": e2e,
+            "config": workload_config(w), "roofline": roofline, "quantize": quant, "moe_layer": layer, "e2e": e2e,
             "cpu_baseline": cpu, "clocks": clocks, "gpu_launches": 4 * args.steps,
             "weight_quantize_ms": weight_quant_ms, "peaks": {"source": peak_src, **peaks},
         }
@@ -448,6 +496,8 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--oracle-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="length of the timed oracle call behind cpu_baseline")
     ap.add_argument("--workload", choices=["mixtral", "llama", "fine", "tiny"], default=WORKLOAD,
                     help="workload of the timed step (the headline line uses mixtral)")
     ap.add_argument("--only", choices=["all", "fwd"], default="all",

@@ -115,6 +115,53 @@ int grouped_mlp_fwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E
                     const uint8_t* w2_q, const uint8_t* w2_sf,
                     void* y, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Dispatch and combine around the grouped MLP (page section "Dense vs. MoE scaling": each token
+ * uses a few of the experts; item 1: GroupedLinear runs on tokens gathered per expert).  The
+ * router (a small GEMM + top-k) is not part of this library: its choices arrive as expert ids.
+ *
+ * moe_permute -- stable sort of the router's (token, slot) choices by expert, on the device.
+ *   experts      (device) int32 [T, k]: expert of slot j of token t, in [0, E).
+ *   gates        (device) float [T, k] routing weights, or NULL (then gates_sorted must be NULL).
+ *   split_sizes  (device, out) int32 [E]: rows per expert.
+ *   row_of_slot  (device, out) int32 [T, k]: sorted row of each (token, slot).
+ *   token_of_row (device, out) int32 [T*k]: token of each sorted row.
+ *   gates_sorted (device, out) float [T*k] or NULL.
+ *   workspace    (device) moe_permute_workspace_size(T, k, E) bytes, 16-byte aligned; its first
+ *                4 bytes are an error word (mxfp8_check_device_error: MXFP8_ERR_INVALID_ARG when
+ *                an expert id is out of range; such slots are skipped and the outputs are then
+ *                incomplete).
+ * Rows of one expert keep (token, slot) order; experts follow each other in id order, so
+ * sorted row r of expert e is split_sizes[0] + ... + split_sizes[e-1] + (rank of the slot).
+ * Requirements: T >= 0, k >= 1, 1 <= E <= 1024, T*k < 2^31.
+ */
+size_t moe_permute_workspace_size(int64_t T, int k, int E);
+int moe_permute(const int32_t* experts, const float* gates, int64_t T, int k, int E,
+                int32_t* split_sizes, int32_t* row_of_slot, int32_t* token_of_row, float* gates_sorted,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * grouped_mlp_fwd_tokens -- grouped_mlp_fwd reading token rows directly: sorted row r is row
+ * token_of_row[r] of x_tokens [T, H] (the gather is fused into the activation quantize, so the
+ * [R, H] sorted copy of x is never written).  Other arguments as grouped_mlp_fwd (gates are in
+ * sorted order).  token_of_row (device) int32 [R], values in [0, T); out-of-range ids read as
+ * zero rows and set MXFP8_ERR_INVALID_ARG in the workspace error word.
+ */
+int grouped_mlp_fwd_tokens(const void* x_tokens, int64_t T, const int32_t* token_of_row, int64_t R, int64_t H,
+                           int64_t F, int E, const int32_t* split_sizes, const float* gates_sorted,
+                           const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q, const uint8_t* w2_sf,
+                           void* y_rows, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * moe_combine -- out[t] = sum_j y_rows[row_of_slot[t, j]] (fp32 sum, bf16 round to nearest even).
+ * The routing weight is already inside y (grouped_mlp_fwd applies it with the SwiGLU), so the
+ * combine is a plain sum.  y_rows (device) bf16 [T*k, H]; row_of_slot (device) int32 [T, k];
+ * out (device) bf16 [T, H], fully overwritten.  Requirements: H % 8 == 0, 16-byte aligned
+ * pointers.  Row ids outside [0, T*k) contribute nothing.
+ */
+int moe_combine(const void* y_rows, const int32_t* row_of_slot, int64_t T, int k, int64_t H, void* out,
+                void* stream);
+
 /* grouped_mlp_fwd with per-kernel timing: identical work and results, and additionally records
  * the 5 caller-created CUDA events stage_events[0..4] (cudaEvent_t as void*, host array) on
  * `stream` before the schedule, activation-quantize, GroupedLinear-1 (+ScaledSwiGLU, requant)
@@ -158,7 +205,8 @@ int grouped_mlp_fwd_noalloc(const void* x_sorted, int64_t R, int64_t H, int64_t 
 int grouped_mlp_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_t* out);
 
 /* Copies the workspace's error word to the host (synchronizes `stream`) and maps it to a
- * status: MXFP8_OK, MXFP8_ERR_SPLIT_MISMATCH or MXFP8_ERR_DEVICE_TIMEOUT.  The raw bits go to
+ * status: MXFP8_OK, MXFP8_ERR_SPLIT_MISMATCH, MXFP8_ERR_INVALID_ARG (bad expert or token id) or
+ * MXFP8_ERR_DEVICE_TIMEOUT.  Works on grouped_mlp_fwd and moe_permute workspaces.  The raw bits go to
  * *flags when flags is not NULL (host). */
 int mxfp8_check_device_error(const void* workspace, void* stream, uint32_t* flags);
 

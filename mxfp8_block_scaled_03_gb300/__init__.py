@@ -12,6 +12,9 @@ approaches, items 1-3):
                      of 32.
   grouped_mlp_fwd    GroupedLinear(split_sizes) -> ScaledSwiGLU -> MXFP8 requant ->
                      GroupedLinear, in one call.
+  moe_permute / grouped_mlp_fwd_tokens / moe_combine
+                     the MoE layer around it: device sort of the router's choices by expert,
+                     the forward gathering token rows itself, and the per-token sum of outputs.
 """
 from __future__ import annotations
 
@@ -24,7 +27,8 @@ from . import build_ext
 __all__ = [
     "MXFP8Error", "ROWWISE", "COLWISE", "SF_COMPACT", "SF_MMA", "lib", "library_path",
     "mxfp8_sf_bytes", "mxfp8_quantize", "grouped_mlp_workspace_size", "grouped_mlp_workspace_layout",
-    "grouped_mlp_fwd", "grouped_mlp_fwd_noalloc", "mxfp8_check_device_error", "mxfp8_status_string", "mxfp8_abi_version",
+    "grouped_mlp_fwd", "grouped_mlp_fwd_noalloc", "grouped_mlp_fwd_tokens", "moe_permute",
+    "moe_permute_workspace_size", "moe_combine", "mxfp8_check_device_error", "mxfp8_status_string", "mxfp8_abi_version",
 ]
 
 ROWWISE = 1
@@ -76,6 +80,14 @@ def lib() -> ctypes.CDLL:
             L.grouped_mlp_fwd_timed.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P, P]
             L.grouped_mlp_fwd_noalloc.restype = i32
             L.grouped_mlp_fwd_noalloc.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P]
+            L.grouped_mlp_fwd_tokens.restype = i32
+            L.grouped_mlp_fwd_tokens.argtypes = [P, i64, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P]
+            L.moe_permute_workspace_size.restype = sz
+            L.moe_permute_workspace_size.argtypes = [i64, i32, i32]
+            L.moe_permute.restype = i32
+            L.moe_permute.argtypes = [P, P, i64, i32, i32, P, P, P, P, P, sz, P]
+            L.moe_combine.restype = i32
+            L.moe_combine.argtypes = [P, P, i64, i32, i64, P, P]
             L.mxfp8_check_device_error.restype = i32
             L.mxfp8_check_device_error.argtypes = [P, P, P]
             _lib = L
@@ -200,6 +212,65 @@ def grouped_mlp_fwd_noalloc(x_sorted, split_sizes, gates, w1_q, w1_sf, w2_q, w2_
                                        _ptr(w1_sf), _ptr(w2_q), _ptr(w2_sf), _ptr(y), _stream(stream))
     _check(st, "grouped_mlp_fwd_noalloc")
     return y
+
+
+def moe_permute_workspace_size(T: int, k: int, E: int) -> int:
+    return int(lib().moe_permute_workspace_size(T, k, E))
+
+
+def moe_permute(experts, gates, E: int, workspace=None, out=None, stream=None):
+    """Stable device sort of the router's (token, slot) choices by expert.
+
+    experts int32 [T, k] (CUDA), gates float32 [T, k] or None.  Returns (split_sizes [E],
+    row_of_slot [T, k], token_of_row [T*k], gates_sorted [T*k] or None, workspace); `out`
+    may pass the first four to be reused."""
+    import torch
+    T, k = experts.shape
+    dev = experts.device
+    if out is not None:
+        split, row_of_slot, token_of_row, gates_sorted = out
+    else:
+        split = torch.empty(E, dtype=torch.int32, device=dev)
+        row_of_slot = torch.empty((T, k), dtype=torch.int32, device=dev)
+        token_of_row = torch.empty(T * k, dtype=torch.int32, device=dev)
+        gates_sorted = None if gates is None else torch.empty(T * k, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(256, moe_permute_workspace_size(T, k, E)), dtype=torch.uint8, device=dev)
+    st = lib().moe_permute(_ptr(experts), _ptr(gates), T, k, E, _ptr(split), _ptr(row_of_slot), _ptr(token_of_row),
+                           _ptr(gates_sorted), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "moe_permute")
+    return split, row_of_slot, token_of_row, gates_sorted, workspace
+
+
+def grouped_mlp_fwd_tokens(x_tokens, token_of_row, split_sizes, gates_sorted, w1_q, w1_sf, w2_q, w2_sf, y=None,
+                           workspace=None, stream=None):
+    """grouped_mlp_fwd that gathers its rows from x_tokens [T, H] through token_of_row [R] inside
+    the activation quantize.  Returns y [R, H] bf16 in sorted-row order."""
+    import torch
+    T, H = x_tokens.shape
+    R = int(token_of_row.numel())
+    E = int(split_sizes.numel())
+    F = int(w2_q.shape[1])
+    if y is None:
+        y = torch.empty((R, H), dtype=torch.bfloat16, device=x_tokens.device)
+    if workspace is None:
+        workspace = torch.empty(grouped_mlp_workspace_size(R, H, F, E), dtype=torch.uint8, device=x_tokens.device)
+    st = lib().grouped_mlp_fwd_tokens(_ptr(x_tokens), T, _ptr(token_of_row), R, H, F, E, _ptr(split_sizes),
+                                      _ptr(gates_sorted), _ptr(w1_q), _ptr(w1_sf), _ptr(w2_q), _ptr(w2_sf), _ptr(y),
+                                      _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "grouped_mlp_fwd_tokens")
+    return y
+
+
+def moe_combine(y_rows, row_of_slot, out=None, stream=None):
+    """out[t] = sum_j y_rows[row_of_slot[t, j]] (bf16 out, fp32 sum)."""
+    import torch
+    T, k = row_of_slot.shape
+    H = y_rows.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=y_rows.device)
+    _check(lib().moe_combine(_ptr(y_rows), _ptr(row_of_slot), T, k, H, _ptr(out), _stream(stream)), "moe_combine")
+    return out
 
 
 def mxfp8_check_device_error(workspace, stream=None) -> tuple[int, int]:

@@ -107,7 +107,8 @@ int grouped_mlp_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_
 static int grouped_mlp_fwd_impl(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E,
                                 const int32_t* split_sizes, const float* gates, const uint8_t* w1_q,
                                 const uint8_t* w1_sf, const uint8_t* w2_q, const uint8_t* w2_sf, void* y,
-                                void* workspace, size_t workspace_bytes, void* stream, void* const* events) {
+                                void* workspace, size_t workspace_bytes, void* stream, void* const* events,
+                                const int32_t* token_of_row = nullptr, int64_t x_rows = 0) {
   if (R < 0 || E < 1 || E > 1024 || H <= 0 || F <= 0) return MXFP8_ERR_INVALID_ARG;
   if (H % 128 != 0 || F % 128 != 0) return MXFP8_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(E) * 2 * F > INT32_MAX || static_cast<int64_t>(E) * H > INT32_MAX)
@@ -120,7 +121,7 @@ static int grouped_mlp_fwd_impl(const void* x_sorted, int64_t R, int64_t H, int6
   if (!ws_layout(R, H, F, E, &L)) return MXFP8_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total) return MXFP8_ERR_WORKSPACE;
   return launch_grouped_mlp(x_sorted, R, H, F, E, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y, workspace, L,
-                            static_cast<cudaStream_t>(stream), events);
+                            static_cast<cudaStream_t>(stream), events, token_of_row, x_rows);
 }
 
 int grouped_mlp_fwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
@@ -139,6 +140,43 @@ int grouped_mlp_fwd_timed(const void* x_sorted, int64_t R, int64_t H, int64_t F,
                               workspace_bytes, stream, stage_events);
 }
 
+int grouped_mlp_fwd_tokens(const void* x_tokens, int64_t T, const int32_t* token_of_row, int64_t R, int64_t H,
+                           int64_t F, int E, const int32_t* split_sizes, const float* gates_sorted,
+                           const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q, const uint8_t* w2_sf,
+                           void* y_rows, void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || token_of_row == nullptr || !aligned16(token_of_row)) return MXFP8_ERR_INVALID_ARG;
+  return grouped_mlp_fwd_impl(x_tokens, R, H, F, E, split_sizes, gates_sorted, w1_q, w1_sf, w2_q, w2_sf, y_rows,
+                              workspace, workspace_bytes, stream, nullptr, token_of_row, T);
+}
+
+size_t moe_permute_workspace_size(int64_t T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1 || E > 1024 || T * k > INT32_MAX) return 0;
+  return permute_workspace_bytes(T * k, E);
+}
+
+int moe_permute(const int32_t* experts, const float* gates, int64_t T, int k, int E, int32_t* split_sizes,
+                int32_t* row_of_slot, int32_t* token_of_row, float* gates_sorted, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  if (T < 0 || k < 1 || E < 1 || E > 1024 || T * k > INT32_MAX) return MXFP8_ERR_INVALID_ARG;
+  if (split_sizes == nullptr || workspace == nullptr || !aligned16(workspace)) return MXFP8_ERR_INVALID_ARG;
+  if (T > 0 && (experts == nullptr || row_of_slot == nullptr || token_of_row == nullptr)) return MXFP8_ERR_INVALID_ARG;
+  if ((gates == nullptr) != (gates_sorted == nullptr)) return MXFP8_ERR_INVALID_ARG;
+  if (workspace_bytes < permute_workspace_bytes(T * k, E)) return MXFP8_ERR_WORKSPACE;
+  const cudaError_t e = launch_permute(experts, gates, T, k, E, split_sizes, row_of_slot, token_of_row, gates_sorted,
+                                       workspace, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+}
+
+int moe_combine(const void* y_rows, const int32_t* row_of_slot, int64_t T, int k, int64_t H, void* out,
+                void* stream) {
+  if (T < 0 || k < 1 || H <= 0 || H % 8 != 0 || T * k > INT32_MAX) return MXFP8_ERR_INVALID_ARG;
+  if (T == 0) return MXFP8_OK;
+  if (y_rows == nullptr || row_of_slot == nullptr || out == nullptr || !aligned16(y_rows) || !aligned16(out))
+    return MXFP8_ERR_INVALID_ARG;
+  const cudaError_t e = launch_combine(y_rows, row_of_slot, T, k, H, out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+}
+
 int mxfp8_check_device_error(const void* workspace, void* stream, uint32_t* flags) {
   if (workspace == nullptr) return MXFP8_ERR_INVALID_ARG;
   uint32_t w = 0;
@@ -148,6 +186,7 @@ int mxfp8_check_device_error(const void* workspace, void* stream, uint32_t* flag
   if (flags) *flags = w;
   if (w & ERR_TIMEOUT_MASK) return MXFP8_ERR_DEVICE_TIMEOUT;
   if (w & (ERR_SPLIT_SUM | ERR_SPLIT_NEGATIVE)) return MXFP8_ERR_SPLIT_MISMATCH;
+  if (w & (ERR_EXPERT_RANGE | ERR_TOKEN_RANGE)) return MXFP8_ERR_INVALID_ARG;
   return MXFP8_OK;
 }
 

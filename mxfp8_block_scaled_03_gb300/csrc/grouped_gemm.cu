@@ -576,7 +576,7 @@ cudaError_t launch_schedule(const int32_t* split, int E, int64_t R, SchedHeader*
 int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
                        const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
                        const uint8_t* w2_sf, void* y, void* workspace, const WsLayout& L, cudaStream_t stream,
-                       void* const* events) {
+                       void* const* events, const int32_t* token_of_row, int64_t x_rows) {
   DeviceInfo* dev = nullptr;
   if (!device_setup(&dev)) return MXFP8_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -598,7 +598,8 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   if (!mark(0)) return MXFP8_ERR_CUDA;
   if (launch_schedule(split, E, R, meta, stream) != cudaSuccess) return MXFP8_ERR_CUDA;
   if (!mark(1)) return MXFP8_ERR_CUDA;
-  if (launch_quantize_gather(x_sorted, R, H, meta, E, L.r_pad, xq, xsf, stream) != cudaSuccess)
+  if (launch_quantize_gather(x_sorted, R, H, meta, E, L.r_pad, token_of_row, x_rows, xq, xsf, stream) !=
+      cudaSuccess)
     return MXFP8_ERR_CUDA;
   if (!mark(2)) return MXFP8_ERR_CUDA;
 

@@ -10,6 +10,8 @@ namespace mx {
 enum : uint32_t {
   ERR_SPLIT_SUM = 1u << 0,        // split_sizes do not add up to R
   ERR_SPLIT_NEGATIVE = 1u << 1,   // a negative split size
+  ERR_EXPERT_RANGE = 1u << 2,     // an expert id outside [0, E) given to the permute
+  ERR_TOKEN_RANGE = 1u << 3,      // a token id outside [0, T) in token_of_row
   ERR_TIMEOUT_PRODUCER = 1u << 8, // TMA producer gave up waiting for a free stage
   ERR_TIMEOUT_MMA = 1u << 9,      // MMA issuer gave up waiting for data or a free accumulator
   ERR_TIMEOUT_EPILOGUE = 1u << 10,// epilogue gave up waiting for an accumulator
@@ -40,19 +42,30 @@ bool ws_layout(int64_t R, int64_t H, int64_t F, int E, WsLayout* out);
 // Quantize launchers (quantize.cu).  Return a cudaError_t from the launch.
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int dirs, int sf_layout, uint8_t* q_row,
                             uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, cudaStream_t stream);
-// Row-wise MXFP8 of x_sorted [R, H] into the expert-padded row space (rows beyond an expert's
-// count are written as zeros), scale bytes in the tensor-core layout.
+// Row-wise MXFP8 of the sorted rows into the expert-padded row space (rows beyond an expert's
+// count are written as zeros), scale bytes in the tensor-core layout.  Sorted row r is x row
+// token_of_row[r], or x row r when token_of_row is NULL.
 cudaError_t launch_quantize_gather(const void* x, int64_t R, int64_t H, const SchedHeader* meta, int E,
-                                   int64_t r_pad, uint8_t* xq, uint8_t* xsf, cudaStream_t stream);
+                                   int64_t r_pad, const int32_t* token_of_row, int64_t x_rows, uint8_t* xq,
+                                   uint8_t* xsf, cudaStream_t stream);
+
+// Dispatch and combine around the grouped MLP (moe_routing.cu).
+size_t permute_workspace_bytes(int64_t n, int E);
+cudaError_t launch_permute(const int32_t* experts, const float* gates, int64_t T, int k, int E, int32_t* split_sizes,
+                           int32_t* row_of_slot, int32_t* token_of_row, float* gates_sorted, void* workspace,
+                           cudaStream_t stream);
+cudaError_t launch_combine(const void* y, const int32_t* row_of_slot, int64_t T, int k, int64_t H, void* out,
+                           cudaStream_t stream);
 
 // Grouped MLP launchers (grouped_gemm.cu).
 cudaError_t launch_schedule(const int32_t* split, int E, int64_t R, SchedHeader* meta, cudaStream_t stream);
 // Enqueues schedule, activation quantize and both grouped GEMMs; returns an mxfp8_status.
 // `events` (may be null): 5 cudaEvent_t recorded on `stream` before each of the 4 kernels and
 // after the last one.
+// token_of_row (may be NULL): sorted row r reads x row token_of_row[r] (fused gather).
 int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
                        const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
                        const uint8_t* w2_sf, void* y, void* workspace, const WsLayout& L, cudaStream_t stream,
-                       void* const* events);
+                       void* const* events, const int32_t* token_of_row = nullptr, int64_t x_rows = 0);
 
 }  // namespace mx

@@ -41,6 +41,7 @@ struct QuantArgs {
   int64_t kt_col;      // tensor-core layout: atoms per 128-column tile for column-wise bytes
   const SchedHeader* meta;  // gather mode only
   int E;
+  const int32_t* tok;       // gather mode: source row of every sorted row (NULL: the sorted row itself)
 };
 
 // max of |a| and |b| per bf16 half (sign bits cleared, so the maximum is exact).
@@ -74,14 +75,14 @@ __device__ __forceinline__ uint2 quant8_bf16(const uint4 w, const float* inv) {
 
 // ROW / COL: directions produced.  MMA: scale bytes in the tensor-core layout instead of the
 // compact one.  GATHER: rows are the expert-padded row space of a grouped MLP; padded row p of
-// expert e reads source row row_off[e] + (p - pad_off[e]) or is a zero row past the expert's
-// count.
+// expert e is sorted row r = row_off[e] + (p - pad_off[e]), read from source row tok[r] (or r
+// when tok is NULL), or a zero row past the expert's count.
 //
 // Thread (warp w, lane l) owns rows 8w..8w+7 of the 64-row tile and columns 8l..8l+7 of the
 // 256-column tile, kept as packed bf16 (8 x 16 bytes in flight per thread).  A column-wise block
 // of 32 rows is warps 4b..4b+3.
 template <bool ROW, bool COL, bool MMA, bool GATHER>
-__global__ void __launch_bounds__(QT_THREADS, (ROW && COL) ? 3 : 4) k_quantize(const QuantArgs a) {
+__global__ void __launch_bounds__(QT_THREADS, (ROW && COL) || GATHER ? 3 : 4) k_quantize(const QuantArgs a) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t K = a.K;
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(QT_THREADS, (ROW && COL) ? 3 : 4) k_quantize(c
   const int64_t col = static_cast<int64_t>(blockIdx.y) * QT_COLS + lane * 8;
   const bool col_ok = col < K;   // K % 32 == 0, so a 4-lane block group is all in or all out
 
-  int64_t src0;      // source row of this thread's first row (rows are consecutive)
+  int64_t src0;      // (sorted) row of this thread's first row (rows are consecutive)
   int nsrc;          // how many of its QT_RPT rows exist in the source
   if constexpr (GATHER) {
     const int32_t pad_rows = a.meta->pad_rows;
@@ -113,11 +114,23 @@ __global__ void __launch_bounds__(QT_THREADS, (ROW && COL) ? 3 : 4) k_quantize(c
     nsrc = left <= 0 ? 0 : (left >= QT_RPT ? QT_RPT : static_cast<int>(left));
   }
 
+  int64_t src[QT_RPT];
+#pragma unroll
+  for (int i = 0; i < QT_RPT; ++i) {
+    src[i] = src0 + i;
+    if (GATHER && a.tok != nullptr && i < nsrc) {
+      src[i] = __ldg(a.tok + src0 + i);
+      if (src[i] < 0 || src[i] >= a.M) {   // out-of-range token id: report it, quantize a zero row
+        atomicOr(const_cast<uint32_t*>(&a.meta->error), ERR_TOKEN_RANGE);
+        src[i] = -1;
+      }
+    }
+  }
   uint4 w[QT_RPT];
 #pragma unroll
   for (int i = 0; i < QT_RPT; ++i) {
-    if (i < nsrc && col_ok)
-      w[i] = __ldcs(reinterpret_cast<const uint4*>(a.x + (src0 + i) * K + col));
+    if (i < nsrc && col_ok && src[i] >= 0)
+      w[i] = __ldcs(reinterpret_cast<const uint4*>(a.x + src[i] * K + col));
     else
       w[i] = make_uint4(0u, 0u, 0u, 0u);
   }
@@ -225,10 +238,12 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int dirs, int s
 }
 
 cudaError_t launch_quantize_gather(const void* x, int64_t R, int64_t H, const SchedHeader* meta, int E,
-                                   int64_t r_pad, uint8_t* xq, uint8_t* xsf, cudaStream_t stream) {
+                                   int64_t r_pad, const int32_t* token_of_row, int64_t x_rows, uint8_t* xq,
+                                   uint8_t* xsf, cudaStream_t stream) {
   QuantArgs a{};
+  a.tok = token_of_row;
   a.x = static_cast<const uint16_t*>(x);
-  a.M = R;
+  a.M = token_of_row ? x_rows : R;   // rows of x (token rows when gathering through token_of_row)
   a.K = H;
   a.q_row = xq;
   a.sf_row = xsf;

@@ -94,6 +94,9 @@ class MoEInputs:
     w1: np.ndarray                # [E*2F, H] bf16 bits
     w2: np.ndarray                # [E*H, F] bf16 bits
     token_of_row: np.ndarray      # [R] int64 source token of each sorted row
+    x_tokens: np.ndarray | None = None      # [T, H] bf16 bits before the sort (routed workloads)
+    topk_experts: np.ndarray | None = None  # [T, k] int32 router choices
+    topk_gates: np.ndarray | None = None    # [T, k] float32 routing weights
 
     @property
     def R(self) -> int:
@@ -168,7 +171,10 @@ def moe_workload(name: str, seed: int = 0) -> MoEInputs:
     else:
         raise KeyError(name)
     x_sorted = np.ascontiguousarray(x[token_of_row])
-    return MoEInputs(name, T, k, E, H, F, x_sorted, split, gates, w1, w2, token_of_row)
+    if name == "llama":
+        return MoEInputs(name, T, k, E, H, F, x_sorted, split, gates, w1, w2, token_of_row)
+    return MoEInputs(name, T, k, E, H, F, x_sorted, split, gates, w1, w2, token_of_row, x,
+                     experts.astype(np.int32), w.astype(np.float32))
 
 
 def custom_moe(split_sizes, H: int, F: int, seed: int = 0, with_gates: bool = True,

@@ -68,6 +68,10 @@ def lib() -> ctypes.CDLL:
             L.ora_grouped_mlp_rows.restype = ctypes.c_int
             L.ora_grouped_mlp_rows.argtypes = [P, i64, i64, i64, ctypes.c_int, P, P, P, P, P, P,
                                                P, i64, P, P, P, ctypes.c_int]
+            L.ora_moe_permute.restype = ctypes.c_int
+            L.ora_moe_permute.argtypes = [P, P, i64, ctypes.c_int, ctypes.c_int, P, P, P, P]
+            L.ora_moe_combine.restype = ctypes.c_int
+            L.ora_moe_combine.argtypes = [P, P, i64, ctypes.c_int, i64, P]
             _lib = L
     return _lib
 
@@ -163,3 +167,33 @@ def grouped_mlp_rows(x_bf16, split_sizes, gates, w1q, w1sf, w2q, w2sf, rows, nth
     if rc != OK:
         raise ValueError(f"oracle grouped_mlp_rows rejected the arguments (status {rc})")
     return y, hq, hsf
+
+
+def moe_permute(experts: np.ndarray, gates: np.ndarray | None, E: int):
+    """Stable sort of (token, slot) pairs by expert.  experts [T, k] int ->
+    (split [E], row_of_slot [T, k], token_of_row [T*k], gates_sorted [T*k] or None)."""
+    ex = np.ascontiguousarray(experts, dtype=np.int32)
+    T, k = ex.shape
+    g = None if gates is None else np.ascontiguousarray(gates, dtype=np.float32)
+    split = np.empty(E, dtype=np.int32)
+    row_of_slot = np.empty((T, k), dtype=np.int32)
+    token_of_row = np.empty(T * k, dtype=np.int32)
+    gs = None if g is None else np.empty(T * k, dtype=np.float32)
+    rc = lib().ora_moe_permute(_ptr(ex), _ptr(g), T, k, E, _ptr(split), _ptr(row_of_slot), _ptr(token_of_row),
+                               _ptr(gs))
+    if rc != OK:
+        raise ValueError(f"oracle moe_permute rejected the arguments (status {rc})")
+    return split, row_of_slot, token_of_row, gs
+
+
+def moe_combine(y: np.ndarray, row_of_slot: np.ndarray) -> np.ndarray:
+    """out[t] = sum_j y[row_of_slot[t, j]] in binary64."""
+    yy = np.ascontiguousarray(y, dtype=np.float64)
+    rs = np.ascontiguousarray(row_of_slot, dtype=np.int32)
+    T, k = rs.shape
+    H = yy.shape[1]
+    out = np.empty((T, H), dtype=np.float64)
+    rc = lib().ora_moe_combine(_ptr(yy), _ptr(rs), T, k, H, _ptr(out))
+    if rc != OK:
+        raise ValueError(f"oracle moe_combine rejected the arguments (status {rc})")
+    return out

@@ -331,4 +331,51 @@ int ora_grouped_mlp_rows(const uint16_t* x, int64_t R, int64_t H, int64_t F, int
     return ORA_OK;
 }
 
+/* ------------------------------------------------------------------------------------------ */
+/* Dispatch and combine around the grouped MLP                                                  */
+/* ------------------------------------------------------------------------------------------ */
+/* Page section "Dense vs. MoE scaling": each token uses k of the E experts; item 1: GroupedLinear
+ * runs on the tokens gathered per expert.  Dispatch = stable sort of the (token, slot) pairs by
+ * expert id (ties keep token-then-slot order), written out as a counting sort:
+ *   split[e]          number of pairs choosing expert e
+ *   row_of_slot[t,j]  position of pair (t, j) in the sorted order
+ *   token_of_row[r]   token of sorted row r;  gates_sorted[r] its routing weight. */
+int ora_moe_permute(const int32_t* experts, const float* gates, int64_t T, int k, int E, int32_t* split,
+                    int32_t* row_of_slot, int32_t* token_of_row, float* gates_sorted) {
+    int64_t i, n = T * (int64_t)k;
+    int64_t* next;
+    int e;
+    if (T < 0 || k < 1 || E < 1 || !split || (n > 0 && (!experts || !row_of_slot || !token_of_row)))
+        return ORA_BAD_ARG;
+    for (i = 0; i < n; ++i)
+        if (experts[i] < 0 || experts[i] >= E) return ORA_BAD_ARG;
+    for (e = 0; e < E; ++e) split[e] = 0;
+    for (i = 0; i < n; ++i) split[experts[i]] += 1;
+    next = (int64_t*)malloc(sizeof(int64_t) * (size_t)E);
+    next[0] = 0;
+    for (e = 1; e < E; ++e) next[e] = next[e - 1] + split[e - 1];
+    for (i = 0; i < n; ++i) {                 /* pairs visited in (token, slot) order */
+        const int64_t r = next[experts[i]]++;
+        row_of_slot[i] = (int32_t)r;
+        token_of_row[r] = (int32_t)(i / k);
+        if (gates && gates_sorted) gates_sorted[r] = gates[i];
+    }
+    free(next);
+    return ORA_OK;
+}
+
+/* out[t, :] = sum over j of y[row_of_slot[t, j], :]   (binary64) */
+int ora_moe_combine(const double* y, const int32_t* row_of_slot, int64_t T, int k, int64_t H, double* out) {
+    int64_t t, c;
+    int j;
+    if (T < 0 || k < 1 || H < 1 || (T > 0 && (!y || !row_of_slot || !out))) return ORA_BAD_ARG;
+    for (t = 0; t < T; ++t)
+        for (c = 0; c < H; ++c) {
+            double acc = 0.0;
+            for (j = 0; j < k; ++j) acc += y[(int64_t)row_of_slot[t * k + j] * H + c];
+            out[t * H + c] = acc;
+        }
+    return ORA_OK;
+}
+
 int ora_abi_version(void) { return 1; }
