@@ -82,7 +82,8 @@ int mxfp8_quantize(const void* x, int64_t M, int64_t K, int dirs, int sf_layout,
 
 /* Workspace bytes grouped_mlp_fwd needs for these sizes (0 on bad arguments).  It holds the
  * device tile schedule, the error word, the quantized activations and the quantized
- * intermediate, each in an expert-padded row space of at most R + 127*E rows. */
+ * intermediate, each in an expert-padded row space (every expert's rows rounded up to a multiple
+ * of 256) of at most R + 255*E rows. */
 size_t grouped_mlp_workspace_size(int64_t R, int64_t H, int64_t F, int E);
 
 /*

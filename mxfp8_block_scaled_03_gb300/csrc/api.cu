@@ -20,7 +20,7 @@ bool ws_layout(int64_t R, int64_t H, int64_t F, int E, WsLayout* out) {
   if (R < 0 || H <= 0 || F <= 0 || E < 1 || E > 1024) return false;
   if (R > static_cast<int64_t>(INT32_MAX) - 128 * static_cast<int64_t>(E)) return false;
   WsLayout L{};
-  L.r_pad = ((R + 127 * static_cast<int64_t>(E)) + 127) / 128 * 128;
+  L.r_pad = ((R + 255 * static_cast<int64_t>(E)) + 255) / 256 * 256;   // experts padded to 256 rows
   L.meta = 0;
   L.xq = align256(sizeof(SchedHeader) + 3 * static_cast<size_t>(E + 1) * sizeof(int32_t));
   L.xsf = align256(L.xq + static_cast<size_t>(L.r_pad) * H);

@@ -36,6 +36,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "mx_device.cuh"
@@ -67,6 +68,8 @@ constexpr int WARP_MMA = 5;
 constexpr int FIRST_EPI_WARP = 8;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_SF_WARPS = 4;
+constexpr uint32_t BAR_EPI = 1;            // hardware barrier of the epilogue warps
+constexpr uint32_t BAR_SF = 2;             // hardware barrier of the scale-staging warps
 constexpr uint32_t REGS_LOW = 56;
 constexpr uint32_t REGS_HIGH = 200;
 static_assert(2 * 128 * REGS_LOW + 256 * REGS_HIGH == NUM_THREADS * 128, "register split must equal the launch pool");
@@ -164,6 +167,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
+// Single-thread form for loops that run in one lane only (the MMA issuer).
+__device__ __forceinline__ bool lane_wait(uint64_t* bar, uint32_t parity, const volatile int* abort, uint64_t timeout,
+                                          uint32_t* err, uint32_t err_bit) {
+  if (mbar_wait_bounded(bar, parity, abort, timeout)) return true;
+  atomicOr(err, err_bit);
+  *const_cast<volatile int*>(abort) = 1;
+  return false;
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint4 v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
@@ -178,6 +190,63 @@ __device__ __forceinline__ void regs_dec() {
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Epilogue math of one tile for the thread holding tile row r and column half `half`, from the
+// accumulator values v already read out of TMEM.
+//   GEMM_SWIGLU: v[0..63] gate columns 64*half.., v[64..127] the matching up columns;
+//                h = gate_r * silu(G) * U, two 32-blocks requantized to E4M3 codes + E8M0 bytes
+//                (written straight into the tensor-core scale layout GroupedLinear 2 reads).
+//   GEMM_OUT:    v[0..BN/2) columns BN/2*half.. -> bf16, stored for the expert's real rows only.
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& t, const uint32_t* v, int r,
+                                              int half, int BN) {
+  if (MODE == GEMM_SWIGLU) {
+    const bool real = r < t.valid;
+    const float gate = real ? (p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f) : 0.0f;
+    uint8_t* hrow = p.hq + static_cast<int64_t>(t.pad_row0 + r) * p.ldh + t.n * 128 + 64 * half;
+    uint32_t sf_pair = 0;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      float h[32];
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float g = __uint_as_float(v[32 * b + i]);
+        const float up = __uint_as_float(v[64 + 32 * b + i]);
+        const float s = __fdividef(g, 1.0f + __expf(-g));
+        h[i] = gate * s * up;
+        amax = fmaxf(amax, fabsf(h[i]));
+      }
+      const uint32_t sfb = e8m0_from_amax(amax);
+      const float inv = e8m0_inverse_scale(sfb);
+      const uint2 t0 = quant8(h + 0, inv), t1 = quant8(h + 8, inv), t2 = quant8(h + 16, inv),
+                  t3 = quant8(h + 24, inv);
+      reinterpret_cast<uint4*>(hrow + 32 * b)[0] = make_uint4(t0.x, t0.y, t1.x, t1.y);
+      reinterpret_cast<uint4*>(hrow + 32 * b)[1] = make_uint4(t2.x, t2.y, t3.x, t3.y);
+      sf_pair |= sfb << (8 * b);
+    }
+    // scale bytes of blocks (2*half, 2*half+1) of column tile n for padded row pad_row0 + r
+    const int64_t atom = static_cast<int64_t>(t.pad_row0 / BM) * (p.ldh / 128) + t.n;
+    *reinterpret_cast<uint16_t*>(p.hsf + atom * SF_ATOM + (r & 31) * 16 + (r >> 5) * 4 + 2 * half) =
+        static_cast<uint16_t>(sf_pair);
+  } else {
+    if (r < t.valid) {
+      const int ncols = BN / 2;
+      uint16_t* yrow = p.y + static_cast<int64_t>(t.src_row0 + r) * p.ldy + t.n * BN + ncols * half;
+#pragma unroll
+      for (int c = 0; c < 128; c += 8) {
+        if (c < ncols) {
+          uint4 o;
+          o.x = pack_bf16x2(__uint_as_float(v[c + 0]), __uint_as_float(v[c + 1]));
+          o.y = pack_bf16x2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+          o.z = pack_bf16x2(__uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+          o.w = pack_bf16x2(__uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+          *reinterpret_cast<uint4*>(yrow + c) = o;
+        }
+      }
+    }
+  }
 }
 
 template <int MODE>
@@ -236,7 +305,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
       for (int kb = 0; kb < p.KT; ++kb) {
-        if (!warp_wait(&full[stage], phase, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_SF, lane)) {
+        bool got = true;
+        if (threadIdx.x == 0) got = lane_wait(&full[stage], phase, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_SF);
+        if (!group_and(BAR_SF, NUM_SF_WARPS * 32, got)) {
           ok = false;
           break;
         }
@@ -322,49 +393,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               atomicOr(p.err, ERR_TIMEOUT_DRAIN);
       __syncwarp();
     } else if (warp == WARP_MMA) {
-      // ---------------- MMA issuer (lane 0 issues) ----------------
-      const uint32_t idesc = idesc_mxf8_e4m3(BM, BN);
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool issued = false, ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        if (!warp_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_MMA, lane)) break;
-        tc_fence_after();
-        for (int kb = 0; kb < p.KT; ++kb) {
-          // sf_full implies full: the scale warps waited for the stage's data before signalling
-          if (!warp_wait(&sf_full[stage], phase, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_MMA, lane)) {
-            ok = false;
-            break;
-          }
+      // ---------------- MMA issuer (the loop runs in lane 0 alone) ----------------
+      if (lane == 0) {
+        const uint32_t idesc = idesc_mxf8_e4m3(BM, BN);
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool issued = false, ok = true;
+        for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+          if (!lane_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_MMA)) break;
           tc_fence_after();
-          if (lane == 0) {
-            const uint8_t* sA = smem + stage * STAGE_BYTES;
-            const uint8_t* sB = sA + A_BYTES;
+          for (int kb = 0; kb < p.KT; ++kb) {
+            // sf_full implies full: the scale warps waited for the stage's data before signalling
+            if (!lane_wait(&sf_full[stage], phase, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(smem + stage * STAGE_BYTES), b0 = a0 + A_BYTES;
             const uint32_t t_sfa = tmem + SFA_COL + 4 * stage;
             const uint32_t t_sfb = tmem + SFB_COL + 8 * stage;
-            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
             for (int k = 0; k < BK / 32; ++k) {
               tc_mma_mxf8(tmem + ACC_COL, sdesc_kmajor_sw128(a0 + 32 * k), sdesc_kmajor_sw128(b0 + 32 * k),
                           idesc_with_sf_id(idesc, k), t_sfa, t_sfb, (kb | k) != 0 ? 1u : 0u);
             }
             tc_commit(&empty[stage]);
+            issued = true;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          __syncwarp();
-          issued = true;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (!ok) break;
+          tc_commit(acc_full);
+          acc_phase ^= 1u;
         }
-        if (!ok) break;
-        if (lane == 0) tc_commit(acc_full);
-        __syncwarp();
-        acc_phase ^= 1u;
-      }
-      if (issued && lane == 0) {
-        tc_commit(drained);
-        if (!mbar_wait_bounded(drained, 0, nullptr, p.timeout_ns)) atomicOr(p.err, ERR_TIMEOUT_DRAIN);
+        if (issued) {
+          tc_commit(drained);
+          if (!mbar_wait_bounded(drained, 0, nullptr, p.timeout_ns)) atomicOr(p.err, ERR_TIMEOUT_DRAIN);
+        }
       }
       __syncwarp();
     }
@@ -379,7 +446,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
       TileInfo t;
       decode_unit(u, p, t);
-      if (!warp_wait(acc_full, acc_phase, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_EPILOGUE, lane)) break;
+      bool got = true;
+      if (warp == FIRST_EPI_WARP && lane == 0)
+        got = lane_wait(acc_full, acc_phase, abort_flag, p.timeout_ns, p.err, ERR_TIMEOUT_EPILOGUE);
+      if (!group_and(BAR_EPI, NUM_EPI_WARPS * 32, got)) break;
       tc_fence_after();
       uint32_t v[128];
       if (MODE == GEMM_SWIGLU) {
@@ -405,52 +475,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(acc_empty);   // accumulator may be overwritten from here on
       acc_phase ^= 1u;
 
-      if (MODE == GEMM_SWIGLU) {
-        const bool real = r < t.valid;
-        const float gate = real ? (p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f) : 0.0f;
-        uint8_t* hrow = p.hq + static_cast<int64_t>(t.pad_row0 + r) * p.ldh + t.n * 128 + 64 * half;
-        uint32_t sf_pair = 0;
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          float h[32];
-          float amax = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float g = __uint_as_float(v[32 * b + i]);
-            const float up = __uint_as_float(v[64 + 32 * b + i]);
-            const float s = __fdividef(g, 1.0f + __expf(-g));
-            h[i] = gate * s * up;
-            amax = fmaxf(amax, fabsf(h[i]));
-          }
-          const uint32_t sfb = e8m0_from_amax(amax);
-          const float inv = e8m0_inverse_scale(sfb);
-          const uint2 t0 = quant8(h + 0, inv), t1 = quant8(h + 8, inv), t2 = quant8(h + 16, inv),
-                      t3 = quant8(h + 24, inv);
-          reinterpret_cast<uint4*>(hrow + 32 * b)[0] = make_uint4(t0.x, t0.y, t1.x, t1.y);
-          reinterpret_cast<uint4*>(hrow + 32 * b)[1] = make_uint4(t2.x, t2.y, t3.x, t3.y);
-          sf_pair |= sfb << (8 * b);
-        }
-        // scale bytes of blocks (2*half, 2*half+1) of column tile n for padded row pad_row0 + r
-        const int64_t atom = static_cast<int64_t>(t.pad_row0 / BM) * (p.ldh / 128) + t.n;
-        *reinterpret_cast<uint16_t*>(p.hsf + atom * SF_ATOM + (r & 31) * 16 + (r >> 5) * 4 + 2 * half) =
-            static_cast<uint16_t>(sf_pair);
-      } else {
-        if (r < t.valid) {
-          const int ncols = BN / 2;
-          uint16_t* yrow = p.y + static_cast<int64_t>(t.src_row0 + r) * p.ldy + t.n * BN + ncols * half;
-#pragma unroll
-          for (int c = 0; c < 128; c += 8) {
-            if (c < ncols) {
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(v[c + 0]), __uint_as_float(v[c + 1]));
-              o.y = pack_bf16x2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-              o.z = pack_bf16x2(__uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
-              o.w = pack_bf16x2(__uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
-              *reinterpret_cast<uint4*>(yrow + c) = o;
-            }
-          }
-        }
-      }
+      epilogue_tile<MODE>(p, t, v, r, half, BN);
     }
   }
 
@@ -463,7 +488,384 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-// One block of 1024 threads: inclusive scans of split sizes and of 128-row tile counts.
+// ---------------------------------------------------------------------------------------------
+// CTA-pair kernel: one tcgen05.mma.cta_group::2 computes a 256 x 256 tile on two SMs.
+// CTA rank r of the pair holds row tile 2q + r of the expert (its 128 rows of A) and half of the
+// 256-row B tile (GroupedLinear 1: r = 0 the gate rows, r = 1 the up rows; GroupedLinear 2: W2 rows
+// 256n + 128r ..), so each SM loads 32 KB per K step for the same MMA work that costs the
+// single-CTA kernel 48 KB, and the same shared memory holds 6 stages instead of 4.  Each CTA's
+// TMEM receives its own 128 rows x 256 columns of the accumulator.
+//
+// Synchronization is arranged so that the data ring has one hop per direction:
+//   full[s]      (leader)  both CTAs' tile copies complete on the leader's barrier (.cta_group::2
+//                          copies); the leader's producer posts the byte count of both halves
+//   empty[s]     (both)    the leader's MMA commit, multicast to both CTAs
+// The block scales travel on a separate, deeper ring that runs ahead of the data:
+//   sf_land[j]   (each)    this CTA's scale atoms of K step g (j = g mod 16) landed in shared memory
+//   sf_full[j]   (leader)  both CTAs' scale warps wrote slot j of their TMEM (8 warp arrivals)
+//   sf_empty[i]  (both)    the MMAs that read slots 4i..4i+3 completed (leader's commit, multicast)
+// and the accumulator hand-off:
+//   acc_full     (both)    the tile's MMAs completed (leader's commit, multicast)
+//   acc_empty    (leader)  both CTAs' epilogues read their accumulator out (16 warp arrivals)
+// Warp roles as in the single-CTA kernel, plus warp 6: scale-atom producer.  The MMA warp of the
+// second CTA only takes part in the TMEM allocation.
+// ---------------------------------------------------------------------------------------------
+constexpr int P_STAGES = 6;
+constexpr int P_STAGE_BYTES = 2 * 128 * BK;                   // own A tile + own half of the B tile
+constexpr int P_SF_SLOTS = 16;
+constexpr int P_SF_GROUP = 4;                                 // slots freed by one MMA commit
+constexpr int P_SF_GROUPS = P_SF_SLOTS / P_SF_GROUP;
+constexpr int P_SF_SLOT_BYTES = 3 * SF_ATOM;                  // A atom + both B atoms
+constexpr int P_DATA_BYTES = P_STAGES * P_STAGE_BYTES;
+constexpr int P_BAR_OFFSET = P_DATA_BYTES + P_SF_SLOTS * P_SF_SLOT_BYTES;
+constexpr int P_NUM_BARS = 2 * P_STAGES + 2 * P_SF_SLOTS + P_SF_GROUPS + 3;
+constexpr int P_SMEM_BYTES = P_BAR_OFFSET + P_NUM_BARS * 8 + 8 + 1024;
+constexpr uint32_t P_SFA_COL = 256;                           // 4 columns per slot
+constexpr uint32_t P_SFB_COL = 320;                           // 8 columns per slot
+constexpr int WARP_SF_PRODUCER = 6;
+constexpr uint32_t P_REGS_LOW = 64;
+constexpr uint32_t P_REGS_HIGH = 192;
+static_assert(2 * 128 * P_REGS_LOW + 256 * P_REGS_HIGH == NUM_THREADS * 128, "register split must equal the launch pool");
+static_assert(P_STAGE_BYTES % 1024 == 0, "pair stages keep 1024-byte alignment");
+static_assert(P_SFA_COL + 4 * P_SF_SLOTS <= P_SFB_COL && P_SFB_COL + 8 * P_SF_SLOTS <= TMEM_COLS, "pair TMEM budget");
+static_assert(P_SMEM_BYTES <= 232448, "pair shared memory budget");
+
+// Pair unit u -> (expert, column tile, pair of row tiles); this CTA takes row tile 2q + rank.
+// Experts own an even number of 128-row tiles (their rows are padded to a multiple of 256).
+__device__ __forceinline__ void decode_pair_unit(int u, int rank, const GemmParams& p, TileInfo& t) {
+  const int32_t* row_off = reinterpret_cast<const int32_t*>(p.meta + 1);
+  const int32_t* pad_off = row_off + (p.E + 1);
+  const int32_t* mt_off = pad_off + (p.E + 1);
+  int lo = 0, hi = p.E;  // largest e with (mt_off[e] / 2) * NT <= u (skips empty experts)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((__ldg(mt_off + mid) >> 1) * p.NT <= u) lo = mid; else hi = mid;
+  }
+  const int e = lo;
+  const int q0 = __ldg(mt_off + e) >> 1;
+  const int pairs = (__ldg(mt_off + e + 1) >> 1) - q0;
+  const int local = u - q0 * p.NT;
+  int n, q;
+  if (p.n_fastest) {
+    q = local / p.NT;
+    n = local - q * p.NT;
+  } else {
+    n = local / pairs;
+    q = local - n * pairs;
+  }
+  const int tt = 2 * q + rank;
+  const int r0 = __ldg(row_off + e);
+  t.e = e;
+  t.n = n;
+  t.pad_row0 = __ldg(pad_off + e) + BM * tt;
+  t.src_row0 = r0 + BM * tt;
+  t.valid = min(BM, __ldg(row_off + e + 1) - r0 - BM * tt);
+}
+
+// Bounded wait shared by the warp (lane 0 polls).  On timeout it records `err_bit`, and raises the
+// abort flag of this CTA and of the other CTA of the pair so that every role of both drains.
+__device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, bool cluster_scope, const volatile int* abort,
+                                          uint32_t peer_abort, const GemmParams& p, uint32_t err_bit, int lane) {
+  int ok = 1;
+  if (lane == 0) {
+    ok = (cluster_scope ? mbar_wait_cluster_bounded(bar, parity, abort, p.timeout_ns)
+                        : mbar_wait_bounded(bar, parity, abort, p.timeout_ns))
+             ? 1
+             : 0;
+    if (!ok) {
+      atomicOr(p.err, err_bit);
+      *const_cast<volatile int*>(abort) = 1;
+      st_remote_u32(peer_abort, 1u);
+    }
+  }
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ bool pair_lane_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                               uint32_t peer_abort, const GemmParams& p, uint32_t err_bit) {
+  if (mbar_wait_cluster_bounded(bar, parity, abort, p.timeout_ns)) return true;
+  atomicOr(p.err, err_bit);
+  *const_cast<volatile int*>(abort) = 1;
+  st_remote_u32(peer_abort, 1u);
+  return false;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sf_ring = smem + P_DATA_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_BAR_OFFSET);
+  uint64_t* empty = full + P_STAGES;
+  uint64_t* sf_land = empty + P_STAGES;
+  uint64_t* sf_full = sf_land + P_SF_SLOTS;
+  uint64_t* sf_empty = sf_full + P_SF_SLOTS;
+  uint64_t* acc_full = sf_empty + P_SF_GROUPS;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drained = acc_empty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drained + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_cta_rank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int j = 0; j < P_SF_SLOTS; ++j) {
+      mbar_init(&sf_land[j], 1);
+      mbar_init(&sf_full[j], 2 * NUM_SF_WARPS);
+    }
+    for (int j = 0; j < P_SF_GROUPS; ++j) mbar_init(&sf_empty[j], 1);
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 2 * NUM_EPI_WARPS);
+    mbar_init(drained, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == WARP_MMA) {   // one warp of each CTA of the pair allocates collectively
+    tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // the peer's barriers exist before any remote arrive, copy or commit
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const int total_units = (p.meta->num_mtiles >> 1) * p.NT;
+  const int first_unit = static_cast<int>(cluster_index());
+  const int unit_stride = static_cast<int>(cluster_count());
+  const uint32_t peer_abort = map_to_cta(const_cast<int*>(abort_flag), rank ^ 1u);
+
+  if (warp < NUM_SF_WARPS) {
+    regs_dec<P_REGS_LOW>();
+    // ---------------- scale staging: own shared-memory slot -> own TMEM slot ----------------
+    const uint32_t t_lanes = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t leader_sf_full = map_to_cta(sf_full, 0);
+    int slot = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = first_unit; ok && u < total_units; u += unit_stride) {
+      for (int kb = 0; kb < p.KT; ++kb) {
+        bool got = true;
+        if (threadIdx.x == 0) got = pair_lane_wait(&sf_land[slot], phase, abort_flag, peer_abort, p, ERR_TIMEOUT_SF);
+        if (!group_and(BAR_SF, NUM_SF_WARPS * 32, got)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* src = sf_ring + slot * P_SF_SLOT_BYTES;
+        tmem_st_32x32b_x4(t_lanes + P_SFA_COL + 4 * slot, *reinterpret_cast<const uint4*>(src + lane * 16));
+        tmem_st_32x32b_x4(t_lanes + P_SFB_COL + 8 * slot, *reinterpret_cast<const uint4*>(src + SF_ATOM + lane * 16));
+        tmem_st_32x32b_x4(t_lanes + P_SFB_COL + 8 * slot + 4,
+                          *reinterpret_cast<const uint4*>(src + 2 * SF_ATOM + lane * 16));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(leader_sf_full + slot * 8);
+        if (++slot == P_SF_SLOTS) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp < FIRST_EPI_WARP) {
+    regs_dec<P_REGS_LOW>();
+    if (warp == WARP_PRODUCER) {
+      // ---------------- tile producer (both CTAs; lane 0 issues) ----------------
+      const uint32_t leader_full = map_to_cta(full, 0);
+      uint32_t issued_mask = 0, issued_parity = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = first_unit; ok && u < total_units; u += unit_stride) {
+        TileInfo t;
+        decode_pair_unit(u, static_cast<int>(rank), p, t);
+        const int b_own = b_box_row<MODE>(p, t, static_cast<int>(rank));
+        for (int kb = 0; kb < p.KT; ++kb) {
+          if (!pair_wait(&empty[stage], phase ^ 1u, true, abort_flag, peer_abort, p, ERR_TIMEOUT_PRODUCER, lane)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            uint8_t* sA = smem + stage * P_STAGE_BYTES;
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+            tma_load_2d_pair(sA, &tmA, leader_full + stage * 8, kb * BK, t.pad_row0);
+            tma_load_2d_pair(sA + A_BYTES, &tmB, leader_full + stage * 8, kb * BK, b_own);
+          }
+          __syncwarp();
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Copies must land before the CTA exits.  The leader's barriers count both CTAs' copies and
+      // the MMA warp waits for every stage it consumes; after an abort, the leader waits here
+      // (bounded) and the second CTA, whose copies complete on the leader's barriers, gives its
+      // copies in flight a fixed 200 us to land (they depend on nothing but memory).
+      if (lane == 0) {
+        if (leader) {
+          for (int s = 0; s < P_STAGES; ++s)
+            if ((issued_mask >> s) & 1u)
+              if (!mbar_wait_cluster_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, p.timeout_ns))
+                atomicOr(p.err, ERR_TIMEOUT_DRAIN);
+        } else if (!ok || *abort_flag) {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 200000ull) {
+          }
+        }
+      }
+      __syncwarp();
+    } else if (warp == WARP_SF_PRODUCER) {
+      // ---------------- scale-atom producer (both CTAs; lane 0 issues) ----------------
+      uint32_t issued_mask = 0, issued_parity = 0;
+      int slot = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = first_unit; ok && u < total_units; u += unit_stride) {
+        TileInfo t;
+        decode_pair_unit(u, static_cast<int>(rank), p, t);
+        const int64_t a_atom0 = static_cast<int64_t>(t.pad_row0 / BM) * p.KT;
+        const int64_t b_atom0 = static_cast<int64_t>(b_box_row<MODE>(p, t, 0) / 128) * p.KT;
+        const int64_t b_atom1 = static_cast<int64_t>(b_box_row<MODE>(p, t, 1) / 128) * p.KT;
+        for (int kb = 0; kb < p.KT; ++kb) {
+          if ((slot % P_SF_GROUP) == 0 &&
+              !pair_wait(&sf_empty[slot / P_SF_GROUP], phase ^ 1u, true, abort_flag, peer_abort, p, ERR_TIMEOUT_SF,
+                         lane)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            uint8_t* dst = sf_ring + slot * P_SF_SLOT_BYTES;
+            mbar_arrive_expect_tx(&sf_land[slot], P_SF_SLOT_BYTES);
+            bulk_load(dst, p.a_sf + (a_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[slot]);
+            bulk_load(dst + SF_ATOM, p.b_sf + (b_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[slot]);
+            bulk_load(dst + 2 * SF_ATOM, p.b_sf + (b_atom1 + kb) * SF_ATOM, SF_ATOM, &sf_land[slot]);
+          }
+          __syncwarp();
+          issued_mask |= 1u << slot;
+          issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
+          if (++slot == P_SF_SLOTS) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (lane == 0)
+        for (int j = 0; j < P_SF_SLOTS; ++j)
+          if ((issued_mask >> j) & 1u)
+            if (!mbar_wait_bounded(&sf_land[j], (issued_parity >> j) & 1u, nullptr, p.timeout_ns))
+              atomicOr(p.err, ERR_TIMEOUT_DRAIN);
+      __syncwarp();
+    } else if (warp == WARP_MMA && leader) {
+      // ---------------- pair MMA issuer (leader CTA; the loop runs in lane 0 alone) ----------------
+      if (lane == 0) {
+        const uint32_t idesc = idesc_mxf8_e4m3(2 * BM, 256);
+        int stage = 0, slot = 0;
+        uint32_t phase = 0, sf_phase = 0, acc_phase = 0;
+        bool issued = false, ok = true;
+        for (int u = first_unit; ok && u < total_units; u += unit_stride) {
+          if (!pair_lane_wait(acc_empty, acc_phase ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) break;
+          tc_fence_after();
+          for (int kb = 0; kb < p.KT; ++kb) {
+            if (!pair_lane_wait(&sf_full[slot], sf_phase, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA) ||
+                !pair_lane_wait(&full[stage], phase, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(smem + stage * P_STAGE_BYTES), b0 = a0 + A_BYTES;
+            const uint32_t t_sfa = tmem + P_SFA_COL + 4 * slot;
+            const uint32_t t_sfb = tmem + P_SFB_COL + 8 * slot;
+#pragma unroll
+            for (int k = 0; k < BK / 32; ++k) {
+              tc_mma_mxf8_pair(tmem + ACC_COL, sdesc_kmajor_sw128(a0 + 32 * k), sdesc_kmajor_sw128(b0 + 32 * k),
+                               idesc_with_sf_id(idesc, k), t_sfa, t_sfb, (kb | k) != 0 ? 1u : 0u);
+            }
+            tc_commit_pair_both(&empty[stage]);
+            if (slot % P_SF_GROUP == P_SF_GROUP - 1) tc_commit_pair_both(&sf_empty[slot / P_SF_GROUP]);
+            issued = true;
+            if (++stage == P_STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            if (++slot == P_SF_SLOTS) {
+              slot = 0;
+              sf_phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc_commit_pair_both(acc_full);
+          acc_phase ^= 1u;
+        }
+        if (issued) {
+          tc_commit_pair_local(drained);
+          if (!mbar_wait_bounded(drained, 0, nullptr, p.timeout_ns)) atomicOr(p.err, ERR_TIMEOUT_DRAIN);
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    regs_inc<P_REGS_HIGH>();
+    // ---------------- epilogue (both CTAs, own 128 rows) ----------------
+    const int quarter = warp & 3;
+    const int half = (warp - FIRST_EPI_WARP) >> 2;
+    const int r = quarter * 32 + lane;
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t leader_acc_empty = map_to_cta(acc_empty, 0);
+    uint32_t acc_phase = 0;
+    for (int u = first_unit; u < total_units; u += unit_stride) {
+      TileInfo t;
+      decode_pair_unit(u, static_cast<int>(rank), p, t);
+      bool got = true;
+      if (warp == FIRST_EPI_WARP && lane == 0)
+        got = pair_lane_wait(acc_full, acc_phase, abort_flag, peer_abort, p, ERR_TIMEOUT_EPILOGUE);
+      if (!group_and(BAR_EPI, NUM_EPI_WARPS * 32, got)) break;
+      tc_fence_after();
+      uint32_t v[128];
+      if (MODE == GEMM_SWIGLU) {
+        tmem_ld_32x32b_x32(t_row + ACC_COL + 64 * half, v);
+        tmem_ld_32x32b_x32(t_row + ACC_COL + 64 * half + 32, v + 32);
+        tmem_ld_32x32b_x32(t_row + ACC_COL + 128 + 64 * half, v + 64);
+        tmem_ld_32x32b_x32(t_row + ACC_COL + 128 + 64 * half + 32, v + 96);
+      } else {
+        tmem_ld_32x32b_x32(t_row + ACC_COL + 128 * half, v);
+        tmem_ld_32x32b_x32(t_row + ACC_COL + 128 * half + 32, v + 32);
+        tmem_ld_32x32b_x32(t_row + ACC_COL + 128 * half + 64, v + 64);
+        tmem_ld_32x32b_x32(t_row + ACC_COL + 128 * half + 96, v + 96);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(leader_acc_empty);   // the leader may overwrite TMEM
+      acc_phase ^= 1u;
+      epilogue_tile<MODE>(p, t, v, r, half, 256);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // all pair MMAs are done and no remote arrive targets an exited CTA
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+}
+
+// One block of 1024 threads: inclusive scans of split sizes and of 128-row tile counts.  Every
+// expert gets an even number of tiles (its rows padded to a multiple of 256), so the pair kernel's
+// two row tiles always belong to one expert.
 __global__ void __launch_bounds__(1024) k_schedule(const int32_t* split, int E, int64_t R, SchedHeader* meta) {
   __shared__ long long s_rows[1024];
   __shared__ int s_tiles[1024];
@@ -478,7 +880,7 @@ __global__ void __launch_bounds__(1024) k_schedule(const int32_t* split, int E, 
     v = 0;
   }
   s_rows[t] = v;
-  s_tiles[t] = (v + BM - 1) / BM;
+  s_tiles[t] = 2 * ((v + 2 * BM - 1) / (2 * BM));
   __syncthreads();
   for (int d = 1; d < 1024; d <<= 1) {
     const long long a = t >= d ? s_rows[t - d] : 0;
@@ -542,8 +944,47 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
 
 struct DeviceInfo {
   int sms = 0;
+  int pair_clusters[2] = {0, 0};   // co-resident CTA pairs of each pair-kernel instance (0: none)
   bool attr_set = false;
 };
+
+template <int MODE>
+cudaLaunchConfig_t pair_config(int clusters, cudaLaunchAttribute* attr, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = P_SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <int MODE>
+int max_pair_clusters() {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config<MODE>(64, attr, nullptr);
+  int n = 0;
+  if (cudaFuncSetAttribute(k_grouped_gemm_pair<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, k_grouped_gemm_pair<MODE>, &cfg) != cudaSuccess) {
+    cudaGetLastError();   // clear: the single-CTA kernels are used instead
+    return 0;
+  }
+  return n;
+}
+
+template <int MODE>
+cudaError_t launch_pair(int clusters, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                        cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config<MODE>(clusters, attr, stream);
+  return cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair<MODE>, a, b, p);
+}
 
 bool device_setup(DeviceInfo** out) {
   static DeviceInfo info[64];
@@ -560,6 +1001,12 @@ bool device_setup(DeviceInfo** out) {
     if (cudaFuncSetAttribute(k_grouped_gemm<GEMM_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
         cudaSuccess)
       return false;
+    // MXFP8MOE_SINGLE_CTA=1 selects the single-CTA kernels (also used where no CTA pair fits)
+    const char* single = getenv("MXFP8MOE_SINGLE_CTA");
+    if (single == nullptr || single[0] != '1') {
+      d.pair_clusters[0] = max_pair_clusters<GEMM_SWIGLU>();
+      d.pair_clusters[1] = max_pair_clusters<GEMM_OUT>();
+    }
     d.attr_set = true;
   }
   *out = &d;
@@ -622,9 +1069,15 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p1.err = &meta->error;
   p1.timeout_ns = kWaitTimeoutNs;
   // persistent: one CTA per SM (shared memory, registers and TMEM each allow only one)
-  const int grid1 = static_cast<int>(std::min<int64_t>(dev->sms, static_cast<int64_t>(max_mtiles) * p1.NT));
-  k_grouped_gemm<GEMM_SWIGLU><<<grid1, NUM_THREADS, SMEM_BYTES, stream>>>(mA1, mB1, p1);
-  if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (dev->pair_clusters[0] > 0) {
+    const int c1 = static_cast<int>(
+        std::min<int64_t>(dev->pair_clusters[0], std::max<int64_t>(1, static_cast<int64_t>(max_mtiles / 2) * p1.NT)));
+    if (launch_pair<GEMM_SWIGLU>(c1, mA1, mB1, p1, stream) != cudaSuccess) return MXFP8_ERR_CUDA;
+  } else {
+    const int grid1 = static_cast<int>(std::min<int64_t>(dev->sms, static_cast<int64_t>(max_mtiles) * p1.NT));
+    k_grouped_gemm<GEMM_SWIGLU><<<grid1, NUM_THREADS, SMEM_BYTES, stream>>>(mA1, mB1, p1);
+    if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
+  }
   if (!mark(3)) return MXFP8_ERR_CUDA;
 
   GemmParams p2{};
@@ -642,9 +1095,15 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p2.ldy = H;
   p2.err = &meta->error;
   p2.timeout_ns = kWaitTimeoutNs;
-  const int grid2 = static_cast<int>(std::min<int64_t>(dev->sms, static_cast<int64_t>(max_mtiles) * p2.NT));
-  k_grouped_gemm<GEMM_OUT><<<grid2, NUM_THREADS, SMEM_BYTES, stream>>>(mA2, mB2, p2);
-  if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (p2.BN == 256 && dev->pair_clusters[1] > 0) {
+    const int c2 = static_cast<int>(
+        std::min<int64_t>(dev->pair_clusters[1], std::max<int64_t>(1, static_cast<int64_t>(max_mtiles / 2) * p2.NT)));
+    if (launch_pair<GEMM_OUT>(c2, mA2, mB2, p2, stream) != cudaSuccess) return MXFP8_ERR_CUDA;
+  } else {   // 128-column output tiles (H % 256 != 0), or no CTA pair fits: single-CTA kernel
+    const int grid2 = static_cast<int>(std::min<int64_t>(dev->sms, static_cast<int64_t>(max_mtiles) * p2.NT));
+    k_grouped_gemm<GEMM_OUT><<<grid2, NUM_THREADS, SMEM_BYTES, stream>>>(mA2, mB2, p2);
+    if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
+  }
   if (!mark(4)) return MXFP8_ERR_CUDA;
   return MXFP8_OK;
 }

@@ -49,7 +49,7 @@ def _gpu_intermediate(mx, w, ws, rows):
     L = mx.grouped_mlp_workspace_layout(w.R, w.H, w.F, w.E)
     split = w.split_sizes.astype(np.int64)
     off = np.concatenate([[0], np.cumsum(split)])
-    pad = np.concatenate([[0], np.cumsum((split + 127) // 128 * 128)])
+    pad = np.concatenate([[0], np.cumsum((split + 255) // 256 * 256)])   # experts padded to 256 rows
     e = np.searchsorted(off, rows, side="right") - 1
     prow = pad[e] + (rows - off[e])
     hq_all = ws[L["hq"]:L["hq"] + L["r_pad"] * w.F].reshape(L["r_pad"], w.F)
