@@ -500,10 +500,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //   full[s]      (leader)  both CTAs' tile copies complete on the leader's barrier (.cta_group::2
 //                          copies); the leader's producer posts the byte count of both halves
 //   empty[s]     (both)    the leader's MMA commit, multicast to both CTAs
-// The block scales travel on a separate, deeper ring that runs ahead of the data:
-//   sf_land[j]   (each)    this CTA's scale atoms of K step g (j = g mod 16) landed in shared memory
-//   sf_full[j]   (leader)  both CTAs' scale warps wrote slot j of their TMEM (8 warp arrivals)
-//   sf_empty[i]  (both)    the MMAs that read slots 4i..4i+3 completed (leader's commit, multicast)
+// The block scales travel on a separate, deeper ring (16 slots, K step g in slot g mod 16) that
+// runs ahead of the data, synchronized per group of 4 slots so that the MMA thread waits on it
+// only every fourth K step (each wait in that thread costs the tensor pipe about 80 ns):
+//   sf_land[i]   (each)    this CTA's scale atoms of group i landed in shared memory
+//   sf_full[i]   (leader)  both CTAs' scale warps wrote group i into their TMEM (8 warp arrivals)
+//   sf_empty[i]  (both)    the MMAs that read group i completed (leader's commit, multicast)
 // and the accumulator hand-off:
 //   acc_full     (both)    the tile's MMAs completed (leader's commit, multicast)
 //   acc_empty    (leader)  both CTAs' epilogues read their accumulator out (16 warp arrivals)
@@ -518,7 +520,7 @@ constexpr int P_SF_GROUPS = P_SF_SLOTS / P_SF_GROUP;
 constexpr int P_SF_SLOT_BYTES = 3 * SF_ATOM;                  // A atom + both B atoms
 constexpr int P_DATA_BYTES = P_STAGES * P_STAGE_BYTES;
 constexpr int P_BAR_OFFSET = P_DATA_BYTES + P_SF_SLOTS * P_SF_SLOT_BYTES;
-constexpr int P_NUM_BARS = 2 * P_STAGES + 2 * P_SF_SLOTS + P_SF_GROUPS + 3;
+constexpr int P_NUM_BARS = 2 * P_STAGES + 3 * P_SF_GROUPS + 3;
 constexpr int P_SMEM_BYTES = P_BAR_OFFSET + P_NUM_BARS * 8 + 8 + 1024;
 constexpr uint32_t P_SFA_COL = 256;                           // 4 columns per slot
 constexpr uint32_t P_SFB_COL = 320;                           // 8 columns per slot
@@ -564,14 +566,11 @@ __device__ __forceinline__ void decode_pair_unit(int u, int rank, const GemmPara
 
 // Bounded wait shared by the warp (lane 0 polls).  On timeout it records `err_bit`, and raises the
 // abort flag of this CTA and of the other CTA of the pair so that every role of both drains.
-__device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, bool cluster_scope, const volatile int* abort,
+__device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
                                           uint32_t peer_abort, const GemmParams& p, uint32_t err_bit, int lane) {
   int ok = 1;
   if (lane == 0) {
-    ok = (cluster_scope ? mbar_wait_cluster_bounded(bar, parity, abort, p.timeout_ns)
-                        : mbar_wait_bounded(bar, parity, abort, p.timeout_ns))
-             ? 1
-             : 0;
+    ok = mbar_wait_bounded(bar, parity, abort, p.timeout_ns) ? 1 : 0;
     if (!ok) {
       atomicOr(p.err, err_bit);
       *const_cast<volatile int*>(abort) = 1;
@@ -581,9 +580,15 @@ __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, bool c
   return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
-__device__ __forceinline__ bool pair_lane_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
+// Barriers completed by hardware (tile copies, MMA commits) are waited on with CTA-scope acquire
+// even where the other CTA's copies or the leader's commits complete them: their data is visible
+// once the phase completes.  Barriers that threads of the other CTA arrive on (scale warps after
+// tcgen05.wait::st, epilogue warps after tcgen05.wait::ld) are waited on with cluster-scope acquire.
+__device__ __forceinline__ bool pair_lane_wait(uint64_t* bar, uint32_t parity, bool cluster_scope, const volatile int* abort,
                                                uint32_t peer_abort, const GemmParams& p, uint32_t err_bit) {
-  if (mbar_wait_cluster_bounded(bar, parity, abort, p.timeout_ns)) return true;
+  if (cluster_scope ? mbar_wait_cluster_bounded(bar, parity, abort, p.timeout_ns)
+                    : mbar_wait_bounded(bar, parity, abort, p.timeout_ns))
+    return true;
   atomicOr(p.err, err_bit);
   *const_cast<volatile int*>(abort) = 1;
   st_remote_u32(peer_abort, 1u);
@@ -600,8 +605,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_BAR_OFFSET);
   uint64_t* empty = full + P_STAGES;
   uint64_t* sf_land = empty + P_STAGES;
-  uint64_t* sf_full = sf_land + P_SF_SLOTS;
-  uint64_t* sf_empty = sf_full + P_SF_SLOTS;
+  uint64_t* sf_full = sf_land + P_SF_GROUPS;
+  uint64_t* sf_empty = sf_full + P_SF_GROUPS;
   uint64_t* acc_full = sf_empty + P_SF_GROUPS;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drained = acc_empty + 1;
@@ -618,11 +623,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int j = 0; j < P_SF_SLOTS; ++j) {
+    for (int j = 0; j < P_SF_GROUPS; ++j) {
       mbar_init(&sf_land[j], 1);
       mbar_init(&sf_full[j], 2 * NUM_SF_WARPS);
+      mbar_init(&sf_empty[j], 1);
     }
-    for (int j = 0; j < P_SF_GROUPS; ++j) mbar_init(&sf_empty[j], 1);
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * NUM_EPI_WARPS);
     mbar_init(drained, 1);
@@ -644,36 +649,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int first_unit = static_cast<int>(cluster_index());
   const int unit_stride = static_cast<int>(cluster_count());
   const uint32_t peer_abort = map_to_cta(const_cast<int*>(abort_flag), rank ^ 1u);
+  // K steps this pair runs in all (both CTAs run the same sequence of units)
+  const int my_units = first_unit < total_units ? (total_units - first_unit + unit_stride - 1) / unit_stride : 0;
+  const int total_steps = my_units * p.KT;
 
   if (warp < NUM_SF_WARPS) {
     regs_dec<P_REGS_LOW>();
-    // ---------------- scale staging: own shared-memory slot -> own TMEM slot ----------------
+    // ---------------- scale staging: own shared-memory slots -> own TMEM slots ----------------
     const uint32_t t_lanes = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const uint32_t leader_sf_full = map_to_cta(sf_full, 0);
-    int slot = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int u = first_unit; ok && u < total_units; u += unit_stride) {
-      for (int kb = 0; kb < p.KT; ++kb) {
+    for (int g = 0; g < total_steps; ++g) {
+      const int slot = g % P_SF_SLOTS;
+      const int grp = slot / P_SF_GROUP;
+      if (slot % P_SF_GROUP == 0) {   // one thread waits for the group's atoms, the others learn it here
         bool got = true;
-        if (threadIdx.x == 0) got = pair_lane_wait(&sf_land[slot], phase, abort_flag, peer_abort, p, ERR_TIMEOUT_SF);
-        if (!group_and(BAR_SF, NUM_SF_WARPS * 32, got)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* src = sf_ring + slot * P_SF_SLOT_BYTES;
-        tmem_st_32x32b_x4(t_lanes + P_SFA_COL + 4 * slot, *reinterpret_cast<const uint4*>(src + lane * 16));
-        tmem_st_32x32b_x4(t_lanes + P_SFB_COL + 8 * slot, *reinterpret_cast<const uint4*>(src + SF_ATOM + lane * 16));
-        tmem_st_32x32b_x4(t_lanes + P_SFB_COL + 8 * slot + 4,
-                          *reinterpret_cast<const uint4*>(src + 2 * SF_ATOM + lane * 16));
+        if (threadIdx.x == 0)
+          got = pair_lane_wait(&sf_land[grp], (g / P_SF_SLOTS) & 1u, false, abort_flag, peer_abort, p, ERR_TIMEOUT_SF);
+        if (!group_and(BAR_SF, NUM_SF_WARPS * 32, got)) break;
+      }
+      const uint8_t* src = sf_ring + slot * P_SF_SLOT_BYTES;
+      tmem_st_32x32b_x4(t_lanes + P_SFA_COL + 4 * slot, *reinterpret_cast<const uint4*>(src + lane * 16));
+      tmem_st_32x32b_x4(t_lanes + P_SFB_COL + 8 * slot, *reinterpret_cast<const uint4*>(src + SF_ATOM + lane * 16));
+      tmem_st_32x32b_x4(t_lanes + P_SFB_COL + 8 * slot + 4,
+                        *reinterpret_cast<const uint4*>(src + 2 * SF_ATOM + lane * 16));
+      if (slot % P_SF_GROUP == P_SF_GROUP - 1 || g == total_steps - 1) {
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(leader_sf_full + slot * 8);
-        if (++slot == P_SF_SLOTS) {
-          slot = 0;
-          phase ^= 1u;
-        }
+        if (lane == 0) mbar_arrive_remote(leader_sf_full + grp * 8);
       }
     }
   } else if (warp < FIRST_EPI_WARP) {
@@ -690,7 +693,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         decode_pair_unit(u, static_cast<int>(rank), p, t);
         const int b_own = b_box_row<MODE>(p, t, static_cast<int>(rank));
         for (int kb = 0; kb < p.KT; ++kb) {
-          if (!pair_wait(&empty[stage], phase ^ 1u, true, abort_flag, peer_abort, p, ERR_TIMEOUT_PRODUCER, lane)) {
+          if (!pair_wait(&empty[stage], phase ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_PRODUCER, lane)) {
             ok = false;
             break;
           }
@@ -717,7 +720,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (leader) {
           for (int s = 0; s < P_STAGES; ++s)
             if ((issued_mask >> s) & 1u)
-              if (!mbar_wait_cluster_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, p.timeout_ns))
+              if (!mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, p.timeout_ns))
                 atomicOr(p.err, ERR_TIMEOUT_DRAIN);
         } else if (!ok || *abort_flag) {
           const uint64_t t0 = globaltimer_ns();
@@ -729,40 +732,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == WARP_SF_PRODUCER) {
       // ---------------- scale-atom producer (both CTAs; lane 0 issues) ----------------
       uint32_t issued_mask = 0, issued_parity = 0;
-      int slot = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int u = first_unit; ok && u < total_units; u += unit_stride) {
-        TileInfo t;
-        decode_pair_unit(u, static_cast<int>(rank), p, t);
-        const int64_t a_atom0 = static_cast<int64_t>(t.pad_row0 / BM) * p.KT;
-        const int64_t b_atom0 = static_cast<int64_t>(b_box_row<MODE>(p, t, 0) / 128) * p.KT;
-        const int64_t b_atom1 = static_cast<int64_t>(b_box_row<MODE>(p, t, 1) / 128) * p.KT;
-        for (int kb = 0; kb < p.KT; ++kb) {
-          if ((slot % P_SF_GROUP) == 0 &&
-              !pair_wait(&sf_empty[slot / P_SF_GROUP], phase ^ 1u, true, abort_flag, peer_abort, p, ERR_TIMEOUT_SF,
-                         lane)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            uint8_t* dst = sf_ring + slot * P_SF_SLOT_BYTES;
-            mbar_arrive_expect_tx(&sf_land[slot], P_SF_SLOT_BYTES);
-            bulk_load(dst, p.a_sf + (a_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[slot]);
-            bulk_load(dst + SF_ATOM, p.b_sf + (b_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[slot]);
-            bulk_load(dst + 2 * SF_ATOM, p.b_sf + (b_atom1 + kb) * SF_ATOM, SF_ATOM, &sf_land[slot]);
-          }
-          __syncwarp();
-          issued_mask |= 1u << slot;
-          issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
-          if (++slot == P_SF_SLOTS) {
-            slot = 0;
-            phase ^= 1u;
-          }
+      TileInfo t{};
+      int64_t a_atom0 = 0, b_atom0 = 0, b_atom1 = 0;
+      for (int g = 0; g < total_steps; ++g) {
+        const int kb = g % p.KT;
+        const int slot = g % P_SF_SLOTS;
+        const int grp = slot / P_SF_GROUP;
+        const uint32_t lap = (g / P_SF_SLOTS) & 1u;
+        if (kb == 0) {
+          decode_pair_unit(first_unit + (g / p.KT) * unit_stride, static_cast<int>(rank), p, t);
+          a_atom0 = static_cast<int64_t>(t.pad_row0 / BM) * p.KT;
+          b_atom0 = static_cast<int64_t>(b_box_row<MODE>(p, t, 0) / 128) * p.KT;
+          b_atom1 = static_cast<int64_t>(b_box_row<MODE>(p, t, 1) / 128) * p.KT;
         }
+        if (slot % P_SF_GROUP == 0) {
+          // the previous lap's MMAs are done with the group; post the bytes of its (up to 4) steps
+          if (!pair_wait(&sf_empty[grp], lap ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_SF, lane)) break;
+          if (lane == 0)
+            mbar_arrive_expect_tx(&sf_land[grp], min(P_SF_GROUP, total_steps - g) * P_SF_SLOT_BYTES);
+          issued_mask |= 1u << grp;
+          issued_parity = (issued_parity & ~(1u << grp)) | (lap << grp);
+        }
+        if (lane == 0) {
+          uint8_t* dst = sf_ring + slot * P_SF_SLOT_BYTES;
+          bulk_load(dst, p.a_sf + (a_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
+          bulk_load(dst + SF_ATOM, p.b_sf + (b_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
+          bulk_load(dst + 2 * SF_ATOM, p.b_sf + (b_atom1 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
+        }
+        __syncwarp();
       }
       if (lane == 0)
-        for (int j = 0; j < P_SF_SLOTS; ++j)
+        for (int j = 0; j < P_SF_GROUPS; ++j)
           if ((issued_mask >> j) & 1u)
             if (!mbar_wait_bounded(&sf_land[j], (issued_parity >> j) & 1u, nullptr, p.timeout_ns))
               atomicOr(p.err, ERR_TIMEOUT_DRAIN);
@@ -775,11 +775,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t phase = 0, sf_phase = 0, acc_phase = 0;
         bool issued = false, ok = true;
         for (int u = first_unit; ok && u < total_units; u += unit_stride) {
-          if (!pair_lane_wait(acc_empty, acc_phase ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) break;
+          if (!pair_lane_wait(acc_empty, acc_phase ^ 1u, true, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) break;
           tc_fence_after();
           for (int kb = 0; kb < p.KT; ++kb) {
-            if (!pair_lane_wait(&sf_full[slot], sf_phase, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA) ||
-                !pair_lane_wait(&full[stage], phase, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) {
+            if ((slot % P_SF_GROUP == 0 &&
+                 !pair_lane_wait(&sf_full[slot / P_SF_GROUP], sf_phase, true, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) ||
+                !pair_lane_wait(&full[stage], phase, false, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) {
               ok = false;
               break;
             }
@@ -829,7 +830,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       decode_pair_unit(u, static_cast<int>(rank), p, t);
       bool got = true;
       if (warp == FIRST_EPI_WARP && lane == 0)
-        got = pair_lane_wait(acc_full, acc_phase, abort_flag, peer_abort, p, ERR_TIMEOUT_EPILOGUE);
+        got = pair_lane_wait(acc_full, acc_phase, false, abort_flag, peer_abort, p, ERR_TIMEOUT_EPILOGUE);
       if (!group_and(BAR_EPI, NUM_EPI_WARPS * 32, got)) break;
       tc_fence_after();
       uint32_t v[128];

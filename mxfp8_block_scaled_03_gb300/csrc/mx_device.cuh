@@ -261,18 +261,18 @@ __device__ __forceinline__ uint32_t map_to_cta(const void* p, uint32_t cta) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(cta));
   return r;
 }
-// Arrive on a barrier of another CTA of the cluster.  Default (.release.cta) semantics: the
-// writes this ordering has to cover are TMEM stores and reads, which tcgen05.wait::st/ld and
-// tcgen05.fence::before_thread_sync already order; a .release.cluster arrive cost about a third of
-// the pair kernel's time.
+// Arrive on a barrier of another CTA of the cluster (default .release.cta semantics).  Every use
+// follows tcgen05.wait::st or tcgen05.wait::ld, which block until this thread's TMEM accesses have
+// completed, so the arrive has no pending writes to publish; a .release.cluster arrive here cost
+// about a third of the pair kernel's time.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ void st_remote_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
-// try_wait with cluster-scope acquire: for barriers the other CTA of the pair arrives on (or its
-// copies complete on), so that its writes are visible after the wait.
+// try_wait with cluster-scope acquire, for barriers that threads of the other CTA of the pair
+// arrive on, so that what they wrote before arriving is visible after the wait.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
