@@ -501,8 +501,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //                          copies); the leader's producer posts the byte count of both halves
 //   empty[s]     (both)    the leader's MMA commit, multicast to both CTAs
 // The block scales travel on a separate, deeper ring (16 slots, K step g in slot g mod 16) that
-// runs ahead of the data, synchronized per group of 4 slots so that the MMA thread waits on it
-// only every fourth K step (each wait in that thread costs the tensor pipe about 80 ns):
+// runs ahead of the data, synchronized per group of 4 slots.  The MMA thread never waits on it:
+// the leader's producer waits for a group's scales before its arrival completes the group's first
+// stage (every wait in the MMA thread costs the tensor pipe 30-80 ns; its queue is shallow).
 //   sf_land[i]   (each)    this CTA's scale atoms of group i landed in shared memory
 //   sf_full[i]   (leader)  both CTAs' scale warps wrote group i into their TMEM (8 warp arrivals)
 //   sf_empty[i]  (both)    the MMAs that read group i completed (leader's commit, multicast)
@@ -685,25 +686,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ---------------- tile producer (both CTAs; lane 0 issues) ----------------
       const uint32_t leader_full = map_to_cta(full, 0);
       uint32_t issued_mask = 0, issued_parity = 0;
-      int stage = 0;
+      int stage = 0, g = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int u = first_unit; ok && u < total_units; u += unit_stride) {
         TileInfo t;
         decode_pair_unit(u, static_cast<int>(rank), p, t);
         const int b_own = b_box_row<MODE>(p, t, static_cast<int>(rank));
-        for (int kb = 0; kb < p.KT; ++kb) {
+        for (int kb = 0; kb < p.KT; ++kb, ++g) {
           if (!pair_wait(&empty[stage], phase ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_PRODUCER, lane)) {
             ok = false;
             break;
           }
           if (lane == 0) {
             uint8_t* sA = smem + stage * P_STAGE_BYTES;
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
             tma_load_2d_pair(sA, &tmA, leader_full + stage * 8, kb * BK, t.pad_row0);
             tma_load_2d_pair(sA + A_BYTES, &tmB, leader_full + stage * 8, kb * BK, b_own);
+            if (leader) {
+              // The leader's arrival completes the stage only once the step's scales are in both
+              // CTAs' TMEM, so the MMA thread waits on this one barrier per step.  The scale ring
+              // runs about three groups ahead, so this wait rarely blocks.
+              const int slot = g % P_SF_SLOTS;
+              if (slot % P_SF_GROUP == 0 &&
+                  !pair_lane_wait(&sf_full[slot / P_SF_GROUP], (g / P_SF_SLOTS) & 1u, true, abort_flag, peer_abort, p,
+                                  ERR_TIMEOUT_PRODUCER))
+                ok = false;
+              mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+            }
           }
           __syncwarp();
+          ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == P_STAGES) {
@@ -772,15 +784,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) {
         const uint32_t idesc = idesc_mxf8_e4m3(2 * BM, 256);
         int stage = 0, slot = 0;
-        uint32_t phase = 0, sf_phase = 0, acc_phase = 0;
+        uint32_t phase = 0, acc_phase = 0;
         bool issued = false, ok = true;
         for (int u = first_unit; ok && u < total_units; u += unit_stride) {
           if (!pair_lane_wait(acc_empty, acc_phase ^ 1u, true, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) break;
           tc_fence_after();
           for (int kb = 0; kb < p.KT; ++kb) {
-            if ((slot % P_SF_GROUP == 0 &&
-                 !pair_lane_wait(&sf_full[slot / P_SF_GROUP], sf_phase, true, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) ||
-                !pair_lane_wait(&full[stage], phase, false, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) {
+            // full implies the step's scales are staged (the leader's producer waited for them)
+            if (!pair_lane_wait(&full[stage], phase, false, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) {
               ok = false;
               break;
             }
@@ -800,10 +811,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               stage = 0;
               phase ^= 1u;
             }
-            if (++slot == P_SF_SLOTS) {
-              slot = 0;
-              sf_phase ^= 1u;
-            }
+            if (++slot == P_SF_SLOTS) slot = 0;
           }
           if (!ok) break;
           tc_commit_pair_both(acc_full);
