@@ -70,6 +70,14 @@ def lib() -> ctypes.CDLL:
                                                P, i64, P, P, P, ctypes.c_int]
             L.ora_moe_permute.restype = ctypes.c_int
             L.ora_moe_permute.argtypes = [P, P, i64, ctypes.c_int, ctypes.c_int, P, P, P, P]
+            L.ora_grouped_mlp_bwd_rows.restype = ctypes.c_int
+            L.ora_grouped_mlp_bwd_rows.argtypes = [P, i64, i64, i64, ctypes.c_int, P, P, P, P, P, P, P, P, P,
+                                                   P, i64, P, P, P, P, ctypes.c_int, ctypes.c_int]
+            L.ora_grouped_mlp_bwd_dw.restype = ctypes.c_int
+            L.ora_grouped_mlp_bwd_dw.argtypes = [P, i64, i64, i64, ctypes.c_int, P, P, P, P, P, P, P,
+                                                 ctypes.c_int, P, i64, P, ctypes.c_int, ctypes.c_int]
+            L.ora_round_bf16.restype = ctypes.c_double
+            L.ora_round_bf16.argtypes = [ctypes.c_double]
             L.ora_moe_combine.restype = ctypes.c_int
             L.ora_moe_combine.argtypes = [P, P, i64, ctypes.c_int, i64, P]
             _lib = L
@@ -196,4 +204,71 @@ def moe_combine(y: np.ndarray, row_of_slot: np.ndarray) -> np.ndarray:
     rc = lib().ora_moe_combine(_ptr(yy), _ptr(rs), T, k, H, _ptr(out))
     if rc != OK:
         raise ValueError(f"oracle moe_combine rejected the arguments (status {rc})")
+    return out
+
+
+def round_bf16(v: float) -> float:
+    return float(lib().ora_round_bf16(float(v)))
+
+
+def quantize_transposed(w_bf16: np.ndarray, E: int, nthreads: int | None = None):
+    """Per-expert transpose, then row-wise MXFP8: w [E*A, B] bf16 bits -> codes [E*B, A] and
+    E8M0 bytes [E*B, A/32] (the weight quantized along its other axis, as the backward GEMMs
+    contract over it)."""
+    w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
+    EA, B = w.shape
+    A = EA // E
+    wt = np.ascontiguousarray(w.reshape(E, A, B).transpose(0, 2, 1).reshape(E * B, A))
+    return quantize_rowwise(wt, nthreads)
+
+
+def grouped_mlp_bwd_rows(x_bf16, split_sizes, gates, w1q, w1sf, w2tq, w2tsf, w1tq, w1tsf, dy_bf16, rows,
+                         nthreads=None, quant=True):
+    """Backward rows in binary64: (dx [n, H], dgate [n], dGU bf16 bits [n, 2F], h bf16 bits [n, F]).
+    quant=False turns every quantization and bf16 rounding of x, dy and the intermediates into the
+    identity (a test hook; the weights are always taken from their codes).
+
+    w1q/w1sf: W1 row-wise (forward); w2tq/w2tsf: W2 quantized along H (quantize_transposed);
+    w1tq/w1tsf: W1 quantized along 2F (quantize_transposed)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    dy = np.ascontiguousarray(dy_bf16, dtype=np.uint16)
+    R, H = x.shape
+    split = np.ascontiguousarray(split_sizes, dtype=np.int32)
+    E = split.size
+    F = w2tq.shape[0] // E
+    g = None if gates is None else np.ascontiguousarray(gates, dtype=np.float32)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.size
+    dx = np.empty((n, H), dtype=np.float64)
+    dgate = np.empty(n, dtype=np.float64)
+    dgu = np.empty((n, 2 * F), dtype=np.uint16)
+    hb = np.empty((n, F), dtype=np.uint16)
+    arrs = [np.ascontiguousarray(a, dtype=np.uint8) for a in (w1q, w1sf, w2tq, w2tsf, w1tq, w1tsf)]
+    rc = lib().ora_grouped_mlp_bwd_rows(_ptr(x), R, H, F, E, _ptr(split), _ptr(g), *[_ptr(a) for a in arrs],
+                                        _ptr(dy), _ptr(rows), n, _ptr(dx), _ptr(dgate), _ptr(dgu), _ptr(hb),
+                                        1 if quant else 0, nthreads or default_threads())
+    if rc != OK:
+        raise ValueError(f"oracle grouped_mlp_bwd_rows rejected the arguments (status {rc})")
+    return dx, dgate, dgu, hb
+
+
+def grouped_mlp_bwd_dw(x_bf16, split_sizes, gates, w1q, w1sf, w2tq, w2tsf, dy_bf16, which: int, entries,
+                       nthreads=None, quant=True):
+    """Weight-gradient entries in binary64.  which = 2: dW2 [E, H, F]; which = 1: dW1 [E, 2F, H];
+    entries: int array [n, 3] of (expert, row, column)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    dy = np.ascontiguousarray(dy_bf16, dtype=np.uint16)
+    R, H = x.shape
+    split = np.ascontiguousarray(split_sizes, dtype=np.int32)
+    E = split.size
+    F = w2tq.shape[0] // E
+    g = None if gates is None else np.ascontiguousarray(gates, dtype=np.float32)
+    ent = np.ascontiguousarray(entries, dtype=np.int64).reshape(-1, 3)
+    out = np.empty(ent.shape[0], dtype=np.float64)
+    arrs = [np.ascontiguousarray(a, dtype=np.uint8) for a in (w1q, w1sf, w2tq, w2tsf)]
+    rc = lib().ora_grouped_mlp_bwd_dw(_ptr(x), R, H, F, E, _ptr(split), _ptr(g), *[_ptr(a) for a in arrs], _ptr(dy),
+                                      which, _ptr(ent), ent.shape[0], _ptr(out), 1 if quant else 0,
+                                      nthreads or default_threads())
+    if rc != OK:
+        raise ValueError(f"oracle grouped_mlp_bwd_dw rejected the arguments (status {rc})")
     return out

@@ -378,4 +378,292 @@ int ora_moe_combine(const double* y, const int32_t* row_of_slot, int64_t T, int 
     return ORA_OK;
 }
 
+/* ------------------------------------------------------------------------------------------ */
+/* Backward of the grouped MLP                                                                  */
+/* ------------------------------------------------------------------------------------------ */
+/* Section 3 names a fused backward op for the same GroupedLinear -> ScaledSwiGLU ->
+ * GroupedLinear chain without spelling it out.  The reading taken is the usual one for MXFP8
+ * training:
+ *   - gradients pass straight through every quantization (the quantized tensor's gradient is
+ *     used as the gradient of the tensor it came from);
+ *   - every backward GEMM takes MXFP8 operands with blocks of 32 along that GEMM's contraction
+ *     axis: along H for dh = dy W2, along 2F for dx = dGU W1, along the expert's rows for the
+ *     weight gradients (32-row blocks counted from the expert's first row, the last one padded
+ *     with zeros);
+ *   - the two tensors the backward hands from one GEMM to the next, dGU = [dG | dU] and the
+ *     activation h for dW2, are bf16 tensors, so they are rounded to bf16 before they are
+ *     quantized (x and dy are bf16 inputs already).
+ * With a = dequant(Q_row(x_r)), g_j, u_j, h_j as in the forward, and
+ *   s_j = g_j / (1 + exp(-g_j))                       (silu)
+ *   s'_j = sigma_j * (1 + g_j * (1 - sigma_j)),  sigma_j = 1 / (1 + exp(-g_j))
+ * the backward of row r (expert e) is
+ *   dh_j    = sum_k dequant(Q_row(dy_r))_k * W2t[e, j, k]       (W2 quantized along H)
+ *   dG_j    = dh_j * gate_r * u_j * s'_j,   dU_j = dh_j * gate_r * s_j
+ *   dgate_r = sum_j dh_j * s_j * u_j
+ *   dx_r,k  = sum_j dequant(Q_row(bf16(dGU_r)))_j * W1t[e, k, j] (W1 quantized along 2F)
+ * and the weight gradients of expert e are
+ *   dW2[e, i, j] = sum_r dequant(Q_col(dy))_{r,i} * dequant(Q_col(bf16(h)))_{r,j}
+ *   dW1[e, j, k] = sum_r dequant(Q_col(bf16(dGU)))_{r,j} * dequant(Q_col(x))_{r,k}
+ * W2t holds, for each expert, W2[e]^T = [F, H] quantized row-wise (i.e. W2 quantized along H);
+ * W1t holds W1[e]^T = [H, 2F] quantized row-wise (W1 quantized along 2F). */
+
+/* Nearest bf16 value of a finite double, ties to even (binary32 exponent range; bf16 subnormals
+ * keep the fixed spacing 2^-133; overflow is not reached by the values this file produces). */
+double ora_round_bf16(double v) {
+    int ex, e;
+    double a = fabs(v), q;
+    if (a == 0.0) return v;
+    (void)frexp(a, &ex);
+    e = ex - 1;                     /* a in [2^e, 2^(e+1)) */
+    if (e < -126) e = -126;         /* subnormal range: spacing 2^-133 */
+    q = ldexp(rint(ldexp(a, 7 - e)), e - 7);
+    return v < 0 ? -q : q;
+}
+
+uint16_t ora_double_to_bf16_bits(double v) {
+    float f = (float)ora_round_bf16(v);   /* exact: the value has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+typedef struct {
+    const uint16_t *x, *dy; int64_t R, H, F; int E;
+    const int64_t* off; const float* gates;
+    double code_val[256], scale_val[256];
+    const uint8_t *w1q, *w1sf, *w2tq, *w2tsf, *w1tq, *w1tsf;
+    const int64_t* rows; double *dx, *dgate; uint16_t *dgu_out, *h_out;
+    /* entries of the weight gradients */
+    int which; const int64_t* ent; double* dw;
+    /* 1: quantize and round as documented; 0: every quantization and bf16 rounding of x, dy and
+     * the intermediates is the identity (a test hook that exposes the calculus alone) */
+    int quant;
+} ora_bwd_ctx;
+
+static int ora_expert_of(const ora_bwd_ctx* c, int64_t r) {
+    int e = 0;
+    while (!(r >= c->off[e] && r < c->off[e + 1])) ++e;
+    return e;
+}
+
+static double ora_wval(const ora_bwd_ctx* c, const uint8_t* q, const uint8_t* sf, int64_t row, int64_t K, int64_t k) {
+    return c->code_val[q[row * K + k]] * c->scale_val[sf[row * (K / 32) + k / 32]];
+}
+
+/* dequant(Q_row(v)) for a length-n vector (n % 32 == 0), in place. */
+static void ora_qdq_row(double* v, int64_t n) {
+    uint8_t codes[32];
+    int64_t b;
+    int i;
+    for (b = 0; b < n / 32; ++b) {
+        uint8_t sf = ora_quantize_block(v + b * 32, 32, codes);
+        for (i = 0; i < 32; ++i) v[b * 32 + i] = ora_dequant(codes[i], sf);
+    }
+}
+
+/* dequant(Q_col(v)) for the values of one column over an expert's n rows: blocks of 32 from the
+ * first row, the last block shorter (its zero padding does not change the block's amax). */
+static void ora_qdq_col(double* v, int64_t n) {
+    uint8_t codes[32];
+    int64_t b;
+    int i;
+    for (b = 0; b < n; b += 32) {
+        int len = (int)((n - b) < 32 ? (n - b) : 32);
+        uint8_t sf = ora_quantize_block(v + b, len, codes);
+        for (i = 0; i < len; ++i) v[b + i] = ora_dequant(codes[i], sf);
+    }
+}
+
+/* Forward pre-activations g_j, u_j of a row of expert e from its dequantized activation a. */
+static void ora_row_gu(const ora_bwd_ctx* c, int e, const double* a, int64_t j, double* g, double* u) {
+    const int64_t H = c->H, F = c->F;
+    const int64_t rg = (int64_t)e * 2 * F + j, ru = (int64_t)e * 2 * F + F + j;
+    double gg = 0.0, uu = 0.0;
+    int64_t k;
+    for (k = 0; k < H; ++k) {
+        gg += a[k] * ora_wval(c, c->w1q, c->w1sf, rg, H, k);
+        uu += a[k] * ora_wval(c, c->w1q, c->w1sf, ru, H, k);
+    }
+    *g = gg;
+    *u = uu;
+}
+
+static void ora_row_a(const ora_bwd_ctx* c, int64_t r, double* a) {
+    int64_t k;
+    for (k = 0; k < c->H; ++k) a[k] = ora_bf16_to_double(c->x[r * c->H + k]);
+    if (c->quant) ora_qdq_row(a, c->H);
+}
+
+static void ora_row_dyq(const ora_bwd_ctx* c, int64_t r, double* d) {
+    int64_t k;
+    for (k = 0; k < c->H; ++k) d[k] = ora_bf16_to_double(c->dy[r * c->H + k]);
+    if (c->quant) ora_qdq_row(d, c->H);
+}
+
+static double ora_bwd_round(const ora_bwd_ctx* c, double v) { return c->quant ? ora_round_bf16(v) : v; }
+
+static double ora_row_dh(const ora_bwd_ctx* c, int e, const double* dyq, int64_t j) {
+    double acc = 0.0;
+    int64_t k;
+    for (k = 0; k < c->H; ++k) acc += dyq[k] * ora_wval(c, c->w2tq, c->w2tsf, (int64_t)e * c->F + j, c->H, k);
+    return acc;
+}
+
+static void ora_bwd_rows_range(void* p, int64_t i0, int64_t i1) {
+    ora_bwd_ctx* c = (ora_bwd_ctx*)p;
+    const int64_t H = c->H, F = c->F;
+    double* a = (double*)malloc(sizeof(double) * (size_t)H);
+    double* dyq = (double*)malloc(sizeof(double) * (size_t)H);
+    double* dgu = (double*)malloc(sizeof(double) * (size_t)(2 * F));
+    int64_t i, j, k;
+    for (i = i0; i < i1; ++i) {
+        const int64_t r = c->rows[i];
+        const int e = ora_expert_of(c, r);
+        const double gate = c->gates ? (double)c->gates[r] : 1.0;
+        double dgate = 0.0;
+        ora_row_a(c, r, a);
+        ora_row_dyq(c, r, dyq);
+        for (j = 0; j < F; ++j) {
+            double g, u, dh, sig, sl, dsl;
+            ora_row_gu(c, e, a, j, &g, &u);
+            dh = ora_row_dh(c, e, dyq, j);
+            sig = 1.0 / (1.0 + exp(-g));
+            sl = g * sig;
+            dsl = sig * (1.0 + g * (1.0 - sig));
+            dgu[j] = dh * gate * u * dsl;
+            dgu[F + j] = dh * gate * sl;
+            dgate += dh * sl * u;
+            if (c->h_out) c->h_out[i * F + j] = ora_double_to_bf16_bits(gate * sl * u);
+        }
+        for (j = 0; j < 2 * F; ++j) {
+            dgu[j] = ora_bwd_round(c, dgu[j]);
+            if (c->dgu_out) c->dgu_out[i * 2 * F + j] = ora_double_to_bf16_bits(dgu[j]);
+        }
+        if (c->quant) ora_qdq_row(dgu, 2 * F);
+        for (k = 0; k < H; ++k) {
+            double acc = 0.0;
+            for (j = 0; j < 2 * F; ++j) acc += dgu[j] * ora_wval(c, c->w1tq, c->w1tsf, (int64_t)e * H + k, 2 * F, j);
+            c->dx[i * H + k] = acc;
+        }
+        c->dgate[i] = dgate;
+    }
+    free(a); free(dyq); free(dgu);
+}
+
+/* One weight-gradient entry per index: ent[3i..3i+2] = (e, row, col) of dW2 [E, H, F]
+ * (which == 2) or of dW1 [E, 2F, H] (which == 1). */
+static void ora_bwd_dw_range(void* p, int64_t i0, int64_t i1) {
+    ora_bwd_ctx* c = (ora_bwd_ctx*)p;
+    const int64_t H = c->H, F = c->F;
+    double* a = (double*)malloc(sizeof(double) * (size_t)H);
+    double* dyq = (double*)malloc(sizeof(double) * (size_t)H);
+    int64_t i, r;
+    for (i = i0; i < i1; ++i) {
+        const int e = (int)c->ent[3 * i];
+        const int64_t ri = c->ent[3 * i + 1], ci = c->ent[3 * i + 2];
+        const int64_t r0 = c->off[e], n = c->off[e + 1] - c->off[e];
+        double* va = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        double* vb = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        double acc = 0.0;
+        for (r = 0; r < n; ++r) {
+            const int64_t row = r0 + r;
+            const double gate = c->gates ? (double)c->gates[row] : 1.0;
+            double g, u, sig, sl;
+            ora_row_a(c, row, a);
+            if (c->which == 2) {   /* dW2[e, ri, ci]: dy column ri, h column ci */
+                va[r] = ora_bf16_to_double(c->dy[row * H + ri]);
+                ora_row_gu(c, e, a, ci, &g, &u);
+                sig = 1.0 / (1.0 + exp(-g));
+                vb[r] = ora_bwd_round(c, gate * (g * sig) * u);
+            } else {               /* dW1[e, ri, ci]: dGU column ri, x column ci */
+                const int64_t jj = ri < F ? ri : ri - F;
+                double dh, dsl;
+                ora_row_dyq(c, row, dyq);
+                ora_row_gu(c, e, a, jj, &g, &u);
+                dh = ora_row_dh(c, e, dyq, jj);
+                sig = 1.0 / (1.0 + exp(-g));
+                sl = g * sig;
+                dsl = sig * (1.0 + g * (1.0 - sig));
+                va[r] = ora_bwd_round(c, ri < F ? dh * gate * u * dsl : dh * gate * sl);
+                vb[r] = ora_bf16_to_double(c->x[row * H + ci]);
+            }
+        }
+        if (c->quant) {
+            ora_qdq_col(va, n);
+            ora_qdq_col(vb, n);
+        }
+        for (r = 0; r < n; ++r) acc += va[r] * vb[r];
+        c->dw[i] = acc;
+        free(va); free(vb);
+    }
+    free(a); free(dyq);
+}
+
+static int ora_bwd_setup(ora_bwd_ctx* c, const uint16_t* x, int64_t R, int64_t H, int64_t F, int E,
+                         const int32_t* split, const float* gates, const uint8_t* w1q, const uint8_t* w1sf,
+                         const uint8_t* w2tq, const uint8_t* w2tsf, const uint16_t* dy) {
+    int64_t total = 0, i;
+    int e;
+    if (!x || !split || !w1q || !w1sf || !w2tq || !w2tsf || !dy) return ORA_BAD_ARG;
+    if (R < 0 || H <= 0 || F <= 0 || E <= 0 || H % 32 || F % 32) return ORA_BAD_ARG;
+    memset(c, 0, sizeof *c);
+    c->off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(E + 1));
+    ((int64_t*)c->off)[0] = 0;
+    for (e = 0; e < E; ++e) {
+        if (split[e] < 0) { free((void*)c->off); return ORA_BAD_ARG; }
+        total += split[e];
+        ((int64_t*)c->off)[e + 1] = total;
+    }
+    if (total != R) { free((void*)c->off); return ORA_SPLIT_MISMATCH; }
+    c->x = x; c->dy = dy; c->R = R; c->H = H; c->F = F; c->E = E; c->gates = gates;
+    c->w1q = w1q; c->w1sf = w1sf; c->w2tq = w2tq; c->w2tsf = w2tsf;
+    for (i = 0; i < 256; ++i) {
+        c->code_val[i] = ora_e4m3_decode((uint8_t)i);
+        c->scale_val[i] = ldexp(1.0, (int)i - 127);
+    }
+    return ORA_OK;
+}
+
+int ora_grouped_mlp_bwd_rows(const uint16_t* x, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
+                             const float* gates, const uint8_t* w1q, const uint8_t* w1sf, const uint8_t* w2tq,
+                             const uint8_t* w2tsf, const uint8_t* w1tq, const uint8_t* w1tsf, const uint16_t* dy,
+                             const int64_t* rows, int64_t nrows, double* dx, double* dgate, uint16_t* dgu,
+                             uint16_t* h, int quant, int nthreads) {
+    ora_bwd_ctx c;
+    int64_t i;
+    int rc = ora_bwd_setup(&c, x, R, H, F, E, split, gates, w1q, w1sf, w2tq, w2tsf, dy);
+    if (rc != ORA_OK) return rc;
+    if (!w1tq || !w1tsf || !dx || !dgate || nrows < 0 || (nrows > 0 && !rows)) {
+        free((void*)c.off);
+        return ORA_BAD_ARG;
+    }
+    for (i = 0; i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= R) { free((void*)c.off); return ORA_BAD_ARG; }
+    c.w1tq = w1tq; c.w1tsf = w1tsf; c.rows = rows; c.dx = dx; c.dgate = dgate; c.dgu_out = dgu; c.h_out = h;
+    c.quant = quant != 0;
+    ora_parallel(ora_bwd_rows_range, &c, nrows, nthreads);
+    free((void*)c.off);
+    return ORA_OK;
+}
+
+int ora_grouped_mlp_bwd_dw(const uint16_t* x, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
+                           const float* gates, const uint8_t* w1q, const uint8_t* w1sf, const uint8_t* w2tq,
+                           const uint8_t* w2tsf, const uint16_t* dy, int which, const int64_t* ent, int64_t n,
+                           double* dw, int quant, int nthreads) {
+    ora_bwd_ctx c;
+    int64_t i;
+    int rc = ora_bwd_setup(&c, x, R, H, F, E, split, gates, w1q, w1sf, w2tq, w2tsf, dy);
+    if (rc != ORA_OK) return rc;
+    if ((which != 1 && which != 2) || !dw || n < 0 || (n > 0 && !ent)) { free((void*)c.off); return ORA_BAD_ARG; }
+    for (i = 0; i < n; ++i) {
+        const int64_t e = ent[3 * i], ri = ent[3 * i + 1], ci = ent[3 * i + 2];
+        const int64_t nr = which == 2 ? H : 2 * F, nc = which == 2 ? F : H;
+        if (e < 0 || e >= E || ri < 0 || ri >= nr || ci < 0 || ci >= nc) { free((void*)c.off); return ORA_BAD_ARG; }
+    }
+    c.which = which; c.ent = ent; c.dw = dw; c.quant = quant != 0;
+    ora_parallel(ora_bwd_dw_range, &c, n, nthreads);
+    free((void*)c.off);
+    return ORA_OK;
+}
+
 int ora_abi_version(void) { return 1; }
