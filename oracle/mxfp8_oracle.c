@@ -392,7 +392,9 @@ int ora_moe_combine(const double* y, const int32_t* row_of_slot, int64_t T, int 
  *     with zeros);
  *   - the two tensors the backward hands from one GEMM to the next, dGU = [dG | dU] and the
  *     activation h for dW2, are bf16 tensors, so they are rounded to bf16 before they are
- *     quantized (x and dy are bf16 inputs already).
+ *     quantized (x and dy are bf16 inputs already);
+ *   - the forward saves its pre-activations g, u for the backward as bf16, so the backward's
+ *     SwiGLU derivative starts from bf16(g), bf16(u).
  * With a = dequant(Q_row(x_r)), g_j, u_j, h_j as in the forward, and
  *   s_j = g_j / (1 + exp(-g_j))                       (silu)
  *   s'_j = sigma_j * (1 + g_j * (1 - sigma_j)),  sigma_j = 1 / (1 + exp(-g_j))
@@ -474,7 +476,10 @@ static void ora_qdq_col(double* v, int64_t n) {
     }
 }
 
-/* Forward pre-activations g_j, u_j of a row of expert e from its dequantized activation a. */
+static double ora_bwd_round(const ora_bwd_ctx* c, double v) { return c->quant ? ora_round_bf16(v) : v; }
+
+/* Saved forward pre-activations g_j, u_j of a row of expert e from its dequantized activation a
+ * (bf16-rounded as the forward saves them). */
 static void ora_row_gu(const ora_bwd_ctx* c, int e, const double* a, int64_t j, double* g, double* u) {
     const int64_t H = c->H, F = c->F;
     const int64_t rg = (int64_t)e * 2 * F + j, ru = (int64_t)e * 2 * F + F + j;
@@ -484,8 +489,8 @@ static void ora_row_gu(const ora_bwd_ctx* c, int e, const double* a, int64_t j, 
         gg += a[k] * ora_wval(c, c->w1q, c->w1sf, rg, H, k);
         uu += a[k] * ora_wval(c, c->w1q, c->w1sf, ru, H, k);
     }
-    *g = gg;
-    *u = uu;
+    *g = ora_bwd_round(c, gg);
+    *u = ora_bwd_round(c, uu);
 }
 
 static void ora_row_a(const ora_bwd_ctx* c, int64_t r, double* a) {
@@ -499,8 +504,6 @@ static void ora_row_dyq(const ora_bwd_ctx* c, int64_t r, double* d) {
     for (k = 0; k < c->H; ++k) d[k] = ora_bf16_to_double(c->dy[r * c->H + k]);
     if (c->quant) ora_qdq_row(d, c->H);
 }
-
-static double ora_bwd_round(const ora_bwd_ctx* c, double v) { return c->quant ? ora_round_bf16(v) : v; }
 
 static double ora_row_dh(const ora_bwd_ctx* c, int e, const double* dyq, int64_t j) {
     double acc = 0.0;

@@ -4,7 +4,8 @@ Page "Efficient MoE training for biological foundation models", Key technical ap
 the fused GroupedLinear -> ScaledSwiGLU -> GroupedLinear op has a corresponding fused backward.
 The pages do not spell the backward out; the oracle takes the usual MXFP8-training reading
 (straight-through gradients, each backward GEMM's operands quantized along its contraction
-axis, bf16 hand-off tensors).  The pins below check
+axis, bf16 hand-off tensors, pre-activations saved by the forward as bf16).  The pins below
+check
   - the calculus alone (quantization switched off) against torch.autograd in float64 on a
     ragged problem with an empty expert;
   - the quantization axes, with inputs built so that quantizing along the wrong axis changes
