@@ -197,6 +197,69 @@ int grouped_mlp_fwd_noalloc(const void* x_sorted, int64_t R, int64_t H, int64_t 
                             const uint8_t* w2_q, const uint8_t* w2_sf,
                             void* y, void* stream);
 
+/*
+ * Backward of the grouped MLP (page item 3: the fused forward op has a corresponding fused
+ * backward op; the pages give no further detail).  Reading implemented, as in MXFP8 training:
+ * gradients pass straight through every quantization; each backward GEMM takes MXFP8 operands
+ * with blocks of 32 along its own contraction axis; the tensors handed from one backward GEMM to
+ * the next ([dG | dU] and h) are bf16; the forward's pre-activations [G | U] are saved as bf16.
+ * For sorted row r of expert e, with s = silu(g), s' = sig(g) (1 + g (1 - sig(g))):
+ *   dh     = dy_r W2[e]                 (MXFP8: dy along H, W2 along H)
+ *   dG     = dh * gate_r * u * s',  dU = dh * gate_r * s,  dgate_r = sum_j dh_j s_j u_j
+ *   dx_r   = [dG | dU] W1[e]            (MXFP8 along 2F)
+ *   dW2[e] = dy_e^T h_e,  dW1[e] = [dG | dU]_e^T x_e    (MXFP8 along the expert's rows)
+ *
+ * grouped_mlp_saved_bytes -- bytes of the saved pre-activations of one training forward
+ *   (bf16 [G | U] in the expert-padded row space); 0 on bad arguments.
+ * grouped_mlp_fwd_train -- grouped_mlp_fwd that also writes those pre-activations to `saved`
+ *   (device, saved_bytes >= grouped_mlp_saved_bytes, 16-byte aligned, caller-owned; keep it
+ *   until the backward has run).  Same results and errors as grouped_mlp_fwd.
+ * grouped_mlp_bwd -- all arguments on the device unless noted:
+ *   x_sorted, split_sizes, gates   as given to the forward (gates may be NULL for 1).
+ *   saved        the forward's pre-activations (grouped_mlp_fwd_train).
+ *   w1t_q,w1t_sf W1 quantized along 2F: mxfp8_quantize_colwise_t(W1 [E*2F, H], SF_MMA), i.e.
+ *                codes [H, E*2F] (row k holds column k of the stacked W1) + bytes.
+ *   w2t_q,w2t_sf W2 quantized along H: mxfp8_quantize_colwise_t(W2 [E*H, F], SF_MMA): codes
+ *                [F, E*H] + bytes.
+ *   dy           bf16 [R, H] gradient of y, rows in x_sorted's order.
+ *   dx           bf16 [R, H] out.   dgates  float [R] out, or NULL to skip.
+ *   dw1          float [E, 2F, H] out (gradient of W1).   dw2  float [E, H, F] out.
+ *   workspace    grouped_mlp_bwd_workspace_size(R, H, F, E) bytes, 256-byte aligned.
+ * Requirements: H % 256 == 0, F % 256 == 0 (all backward GEMMs run on CTA pairs with 256-wide
+ * tiles; MXFP8_ERR_UNSUPPORTED otherwise), 1 <= E <= 1024.  Outputs are fully overwritten (an
+ * expert without rows gets zero weight gradients).  Split errors and timeouts are reported in
+ * the workspace error word as for the forward.
+ * grouped_mlp_bwd_timed additionally records 7 caller-created events (stage_events[0..6]) around
+ * its stages: quantizations of dy and x | dh + ScaledSwiGLU backward | quantizations of dGU and
+ * h, dgate | dx | dW2 | dW1.
+ */
+size_t grouped_mlp_saved_bytes(int64_t R, int64_t H, int64_t F, int E);
+int grouped_mlp_fwd_train(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
+                          const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
+                          const uint8_t* w2_sf, void* y, void* saved, size_t saved_bytes, void* workspace,
+                          size_t workspace_bytes, void* stream);
+size_t grouped_mlp_bwd_workspace_size(int64_t R, int64_t H, int64_t F, int E);
+int grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
+                    const float* gates, const void* saved, size_t saved_bytes, const uint8_t* w1t_q,
+                    const uint8_t* w1t_sf, const uint8_t* w2t_q, const uint8_t* w2t_sf, const void* dy, void* dx,
+                    float* dgates, float* dw1, float* dw2, void* workspace, size_t workspace_bytes, void* stream);
+int grouped_mlp_bwd_timed(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
+                          const float* gates, const void* saved, size_t saved_bytes, const uint8_t* w1t_q,
+                          const uint8_t* w1t_sf, const uint8_t* w2t_q, const uint8_t* w2t_sf, const void* dy,
+                          void* dx, float* dgates, float* dw1, float* dw2, void* workspace, size_t workspace_bytes,
+                          void* stream, void* const* stage_events);
+
+/* mxfp8_quantize_colwise_t -- column-wise MXFP8 (blocks of 32 consecutive rows, item 2) with the
+ * codes written transposed, the operand form of GEMMs that contract over x's rows.
+ *   x    (device) bf16 [M, K], row-major.
+ *   q_t  (device, out) E4M3 codes [K, M]: row k holds column k of x.
+ *   sf_t (device, out) E8M0 bytes of the [K, M] code matrix with blocks along its rows:
+ *        compact [K, M/32], or MXFP8_SF_MMA layout (mxfp8_sf_bytes(K, M, ROWWISE, SF_MMA)).
+ * Requirements: M % 128 == 0, K % 32 == 0 (K % 128 == 0 for MXFP8_SF_MMA), 16-byte aligned
+ * pointers.  Same rule and rounding as mxfp8_quantize; M == 0 or K == 0 is a no-op. */
+int mxfp8_quantize_colwise_t(const void* x, int64_t M, int64_t K, int sf_layout, uint8_t* q_t, uint8_t* sf_t,
+                             void* stream);
+
 /* Byte offsets of the pieces of a grouped_mlp_fwd workspace, for inspection by tests:
  *   [0] error word (uint32)   [1] schedule          [2] quantized activations [R_pad, H]
  *   [3] their E8M0 bytes (MXFP8_SF_MMA layout)      [4] quantized intermediate [R_pad, F]

@@ -28,7 +28,8 @@ __all__ = [
     "MXFP8Error", "ROWWISE", "COLWISE", "SF_COMPACT", "SF_MMA", "lib", "library_path",
     "mxfp8_sf_bytes", "mxfp8_quantize", "grouped_mlp_workspace_size", "grouped_mlp_workspace_layout",
     "grouped_mlp_fwd", "grouped_mlp_fwd_noalloc", "grouped_mlp_fwd_tokens", "moe_permute",
-    "moe_permute_workspace_size", "moe_combine", "mxfp8_check_device_error", "mxfp8_status_string", "mxfp8_abi_version",
+    "moe_permute_workspace_size", "moe_combine", "mxfp8_check_device_error", "mxfp8_quantize_colwise_t",
+    "grouped_mlp_saved_bytes", "grouped_mlp_fwd_train", "grouped_mlp_bwd_workspace_size", "grouped_mlp_bwd", "mxfp8_status_string", "mxfp8_abi_version",
 ]
 
 ROWWISE = 1
@@ -78,6 +79,18 @@ def lib() -> ctypes.CDLL:
             L.grouped_mlp_fwd.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P]
             L.grouped_mlp_fwd_timed.restype = i32
             L.grouped_mlp_fwd_timed.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P, P]
+            L.grouped_mlp_saved_bytes.restype = sz
+            L.grouped_mlp_saved_bytes.argtypes = [i64, i64, i64, i32]
+            L.grouped_mlp_fwd_train.restype = i32
+            L.grouped_mlp_fwd_train.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P, sz, P]
+            L.grouped_mlp_bwd_workspace_size.restype = sz
+            L.grouped_mlp_bwd_workspace_size.argtypes = [i64, i64, i64, i32]
+            L.grouped_mlp_bwd.restype = i32
+            L.grouped_mlp_bwd.argtypes = [P, i64, i64, i64, i32, P, P, P, sz, P, P, P, P, P, P, P, P, P, P, sz, P]
+            L.grouped_mlp_bwd_timed.restype = i32
+            L.grouped_mlp_bwd_timed.argtypes = L.grouped_mlp_bwd.argtypes + [P]
+            L.mxfp8_quantize_colwise_t.restype = i32
+            L.mxfp8_quantize_colwise_t.argtypes = [P, i64, i64, i32, P, P, P]
             L.grouped_mlp_fwd_noalloc.restype = i32
             L.grouped_mlp_fwd_noalloc.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P]
             L.grouped_mlp_fwd_tokens.restype = i32
@@ -153,6 +166,26 @@ def mxfp8_quantize(x, rowwise: bool = True, colwise: bool = False, sf_layout: in
     return tuple(out)
 
 
+def mxfp8_quantize_colwise_t(x, sf_layout: int = SF_MMA, out=None, stream=None):
+    """Column-wise MXFP8 of bf16 [M, K] with the codes transposed: returns (q_t uint8 [K, M],
+    sf_t) where row k of q_t holds column k of x in blocks of 32 rows (the operand form of GEMMs
+    that contract over x's rows; weights quantized for the backward)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous() and x.dim() == 2
+    M, K = x.shape
+    if out is None:
+        q_t = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+        n = mxfp8_sf_bytes(K, M, ROWWISE, sf_layout)
+        sf_t = torch.empty(n, dtype=torch.uint8, device=x.device)
+        if sf_layout == SF_COMPACT:
+            sf_t = sf_t.view(K, M // 32)
+    else:
+        q_t, sf_t = out
+    _check(lib().mxfp8_quantize_colwise_t(_ptr(x), M, K, sf_layout, _ptr(q_t), _ptr(sf_t), _stream(stream)),
+           "mxfp8_quantize_colwise_t")
+    return q_t, sf_t
+
+
 def grouped_mlp_workspace_size(R: int, H: int, F: int, E: int) -> int:
     return int(lib().grouped_mlp_workspace_size(R, H, F, E))
 
@@ -198,6 +231,72 @@ def grouped_mlp_fwd(x_sorted, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y=No
         arr = (ctypes.c_void_p * 5)(*handles)
         _check(lib().grouped_mlp_fwd_timed(*args, arr), "grouped_mlp_fwd_timed")
     return y
+
+
+def grouped_mlp_saved_bytes(R: int, H: int, F: int, E: int) -> int:
+    return int(lib().grouped_mlp_saved_bytes(R, H, F, E))
+
+
+def grouped_mlp_bwd_workspace_size(R: int, H: int, F: int, E: int) -> int:
+    return int(lib().grouped_mlp_bwd_workspace_size(R, H, F, E))
+
+
+def grouped_mlp_fwd_train(x_sorted, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y=None, saved=None,
+                          workspace=None, stream=None):
+    """grouped_mlp_fwd that also keeps the bf16 pre-activations [G | U] the backward needs.
+    Returns (y, saved); `saved` is a uint8 CUDA tensor of grouped_mlp_saved_bytes(...) bytes."""
+    import torch
+    R, H = x_sorted.shape
+    E = int(split_sizes.numel())
+    F = int(w2_q.shape[1])
+    dev = x_sorted.device
+    if y is None:
+        y = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    if saved is None:
+        saved = torch.empty(grouped_mlp_saved_bytes(R, H, F, E), dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = torch.empty(grouped_mlp_workspace_size(R, H, F, E), dtype=torch.uint8, device=dev)
+    st = lib().grouped_mlp_fwd_train(_ptr(x_sorted), R, H, F, E, _ptr(split_sizes), _ptr(gates), _ptr(w1_q),
+                                     _ptr(w1_sf), _ptr(w2_q), _ptr(w2_sf), _ptr(y), _ptr(saved), saved.numel(),
+                                     _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "grouped_mlp_fwd_train")
+    return y, saved
+
+
+def grouped_mlp_bwd(x_sorted, split_sizes, gates, saved, w1t_q, w1t_sf, w2t_q, w2t_sf, dy, dx=None, dgates=True,
+                    dw1=None, dw2=None, workspace=None, stream=None, stage_events=None):
+    """Backward of the grouped MLP.  w1t_*/w2t_* are W1 [E*2F, H] and W2 [E*H, F] quantized
+    along their other axis (mxfp8_quantize_colwise_t, tensor-core layout).  Returns
+    (dx bf16 [R, H], dgates float32 [R] or None, dW1 float32 [E, 2F, H], dW2 float32 [E, H, F],
+    workspace)."""
+    import torch
+    R, H = x_sorted.shape
+    E = int(split_sizes.numel())
+    F = int(w2t_q.shape[0])
+    dev = x_sorted.device
+    if dx is None:
+        dx = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    if dgates is True:
+        dgates = torch.empty(R, dtype=torch.float32, device=dev)
+    elif dgates is False:
+        dgates = None
+    if dw1 is None:
+        dw1 = torch.empty((E, 2 * F, H), dtype=torch.float32, device=dev)
+    if dw2 is None:
+        dw2 = torch.empty((E, H, F), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(grouped_mlp_bwd_workspace_size(R, H, F, E), dtype=torch.uint8, device=dev)
+    args = (_ptr(x_sorted), R, H, F, E, _ptr(split_sizes), _ptr(gates), _ptr(saved), saved.numel(), _ptr(w1t_q),
+            _ptr(w1t_sf), _ptr(w2t_q), _ptr(w2t_sf), _ptr(dy), _ptr(dx), _ptr(dgates), _ptr(dw1), _ptr(dw2),
+            _ptr(workspace), workspace.numel(), _stream(stream))
+    if stage_events is None:
+        _check(lib().grouped_mlp_bwd(*args), "grouped_mlp_bwd")
+    else:
+        handles = [int(ev.cuda_event) for ev in stage_events]
+        if len(handles) != 7 or not all(handles):
+            raise ValueError("stage_events: 7 CUDA events that have been recorded at least once")
+        _check(lib().grouped_mlp_bwd_timed(*args, (ctypes.c_void_p * 7)(*handles)), "grouped_mlp_bwd_timed")
+    return dx, dgates, dw1, dw2, workspace
 
 
 def grouped_mlp_fwd_noalloc(x_sorted, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y, stream=None):

@@ -108,7 +108,8 @@ static int grouped_mlp_fwd_impl(const void* x_sorted, int64_t R, int64_t H, int6
                                 const int32_t* split_sizes, const float* gates, const uint8_t* w1_q,
                                 const uint8_t* w1_sf, const uint8_t* w2_q, const uint8_t* w2_sf, void* y,
                                 void* workspace, size_t workspace_bytes, void* stream, void* const* events,
-                                const int32_t* token_of_row = nullptr, int64_t x_rows = 0) {
+                                const int32_t* token_of_row = nullptr, int64_t x_rows = 0,
+                                void* saved = nullptr, size_t saved_bytes = 0) {
   if (R < 0 || E < 1 || E > 1024 || H <= 0 || F <= 0) return MXFP8_ERR_INVALID_ARG;
   if (H % 128 != 0 || F % 128 != 0) return MXFP8_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(E) * 2 * F > INT32_MAX || static_cast<int64_t>(E) * H > INT32_MAX)
@@ -120,8 +121,11 @@ static int grouped_mlp_fwd_impl(const void* x_sorted, int64_t R, int64_t H, int6
   WsLayout L;
   if (!ws_layout(R, H, F, E, &L)) return MXFP8_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total) return MXFP8_ERR_WORKSPACE;
+  if (saved != nullptr && (!aligned16(saved) || saved_bytes < static_cast<size_t>(L.r_pad) * 2 * F * 2))
+    return MXFP8_ERR_WORKSPACE;
   return launch_grouped_mlp(x_sorted, R, H, F, E, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y, workspace, L,
-                            static_cast<cudaStream_t>(stream), events, token_of_row, x_rows);
+                            static_cast<cudaStream_t>(stream), events, token_of_row, x_rows,
+                            static_cast<uint16_t*>(saved));
 }
 
 int grouped_mlp_fwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
@@ -174,6 +178,82 @@ int moe_combine(const void* y_rows, const int32_t* row_of_slot, int64_t T, int k
   if (y_rows == nullptr || row_of_slot == nullptr || out == nullptr || !aligned16(y_rows) || !aligned16(out))
     return MXFP8_ERR_INVALID_ARG;
   const cudaError_t e = launch_combine(y_rows, row_of_slot, T, k, H, out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+}
+
+size_t grouped_mlp_saved_bytes(int64_t R, int64_t H, int64_t F, int E) {
+  WsLayout L;
+  if (!ws_layout(R, H, F, E, &L)) return 0;
+  return static_cast<size_t>(L.r_pad) * 2 * F * 2;
+}
+
+int grouped_mlp_fwd_train(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
+                          const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
+                          const uint8_t* w2_sf, void* y, void* saved, size_t saved_bytes, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (saved == nullptr) return MXFP8_ERR_INVALID_ARG;
+  return grouped_mlp_fwd_impl(x_sorted, R, H, F, E, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y, workspace,
+                              workspace_bytes, stream, nullptr, nullptr, 0, saved, saved_bytes);
+}
+
+size_t grouped_mlp_bwd_workspace_size(int64_t R, int64_t H, int64_t F, int E) {
+  BwdWsLayout L;
+  if (!bwd_ws_layout(R, H, F, E, &L)) return 0;
+  return L.total;
+}
+
+static int grouped_mlp_bwd_impl(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E,
+                                const int32_t* split_sizes, const float* gates, const void* saved,
+                                size_t saved_bytes, const uint8_t* w1t_q, const uint8_t* w1t_sf,
+                                const uint8_t* w2t_q, const uint8_t* w2t_sf, const void* dy, void* dx, float* dgates,
+                                float* dw1, float* dw2, void* workspace, size_t workspace_bytes, void* stream,
+                                void* const* events) {
+  if (R < 0 || E < 1 || E > 1024 || H <= 0 || F <= 0) return MXFP8_ERR_INVALID_ARG;
+  if (H % 256 != 0 || F % 256 != 0) return MXFP8_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(E) * 2 * F > INT32_MAX || static_cast<int64_t>(E) * H > INT32_MAX)
+    return MXFP8_ERR_UNSUPPORTED;
+  const void* ptrs[] = {x_sorted, split_sizes, saved, w1t_q, w1t_sf, w2t_q, w2t_sf, dy, dx, dw1, dw2, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return MXFP8_ERR_INVALID_ARG;
+  if ((gates != nullptr && !aligned16(gates)) || (dgates != nullptr && !aligned16(dgates)))
+    return MXFP8_ERR_INVALID_ARG;
+  BwdWsLayout L;
+  if (!bwd_ws_layout(R, H, F, E, &L)) return MXFP8_ERR_UNSUPPORTED;
+  if (saved_bytes < static_cast<size_t>(L.r_pad) * 2 * F * 2) return MXFP8_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total) return MXFP8_ERR_WORKSPACE;
+  return launch_grouped_mlp_bwd(x_sorted, R, H, F, E, split_sizes, gates, static_cast<const uint16_t*>(saved),
+                                w1t_q, w1t_sf, w2t_q, w2t_sf, dy, dx, dgates, dw1, dw2, workspace, L,
+                                static_cast<cudaStream_t>(stream), events);
+}
+
+int grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
+                    const float* gates, const void* saved, size_t saved_bytes, const uint8_t* w1t_q,
+                    const uint8_t* w1t_sf, const uint8_t* w2t_q, const uint8_t* w2t_sf, const void* dy, void* dx,
+                    float* dgates, float* dw1, float* dw2, void* workspace, size_t workspace_bytes, void* stream) {
+  return grouped_mlp_bwd_impl(x_sorted, R, H, F, E, split_sizes, gates, saved, saved_bytes, w1t_q, w1t_sf, w2t_q,
+                              w2t_sf, dy, dx, dgates, dw1, dw2, workspace, workspace_bytes, stream, nullptr);
+}
+
+int grouped_mlp_bwd_timed(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
+                          const float* gates, const void* saved, size_t saved_bytes, const uint8_t* w1t_q,
+                          const uint8_t* w1t_sf, const uint8_t* w2t_q, const uint8_t* w2t_sf, const void* dy,
+                          void* dx, float* dgates, float* dw1, float* dw2, void* workspace, size_t workspace_bytes,
+                          void* stream, void* const* stage_events) {
+  if (stage_events == nullptr) return MXFP8_ERR_INVALID_ARG;
+  return grouped_mlp_bwd_impl(x_sorted, R, H, F, E, split_sizes, gates, saved, saved_bytes, w1t_q, w1t_sf, w2t_q,
+                              w2t_sf, dy, dx, dgates, dw1, dw2, workspace, workspace_bytes, stream, stage_events);
+}
+
+int mxfp8_quantize_colwise_t(const void* x, int64_t M, int64_t K, int sf_layout, uint8_t* q_t, uint8_t* sf_t,
+                             void* stream) {
+  if (M < 0 || K < 0 || K % 32 != 0) return MXFP8_ERR_INVALID_ARG;
+  if (sf_layout != MXFP8_SF_COMPACT && sf_layout != MXFP8_SF_MMA) return MXFP8_ERR_INVALID_ARG;
+  if (M % 128 != 0 || (sf_layout == MXFP8_SF_MMA && K % 128 != 0)) return MXFP8_ERR_UNSUPPORTED;
+  if (M == 0 || K == 0) return MXFP8_OK;
+  if (x == nullptr || q_t == nullptr || sf_t == nullptr || !aligned16(x) || !aligned16(q_t))
+    return MXFP8_ERR_INVALID_ARG;
+  const cudaError_t e = launch_quantize_t(x, M, K, M, sf_layout == MXFP8_SF_MMA, q_t, sf_t, nullptr, 0, nullptr, 0,
+                                          static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
 }
 

@@ -83,7 +83,11 @@ static_assert(A_BYTES + B_BYTES_MAX + 3 * SF_ATOM <= STAGE_BYTES, "stage layout"
 static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment for the 128B swizzle");
 static_assert(SFB_COL + 8 * STAGES <= TMEM_COLS, "TMEM budget");
 
-enum GemmMode { GEMM_SWIGLU = 0, GEMM_OUT = 1 };
+// GEMM_SWIGLU  forward GroupedLinear 1 + ScaledSwiGLU + requant (optionally saving [G | U])
+// GEMM_OUT     A B^T -> bf16 rows (forward GroupedLinear 2; backward dx = dGU W1)
+// GEMM_DGRAD   backward dh = dy W2 with the ScaledSwiGLU backward in the epilogue
+// GEMM_WGRAD   weight gradient of every expert: A^T B over the expert's rows (K varies by expert)
+enum GemmMode { GEMM_SWIGLU = 0, GEMM_OUT = 1, GEMM_DGRAD = 2, GEMM_WGRAD = 3 };
 
 struct GemmParams {
   const SchedHeader* meta;
@@ -106,10 +110,28 @@ struct GemmParams {
   int64_t ldy;             // H
   uint32_t* err;
   uint64_t timeout_ns;
+  // operand addressing of the pair kernel
+  int a_kt;                // scale atoms per 128-row tile of A (K extent of A / 128)
+  int b_kt;                // same for B
+  int b_kofs;              // expert e's block of B starts at K column e * b_kofs (weights stored
+                           // transposed as one [N, E*K] matrix); 0 for the forward
+  // GEMM_SWIGLU in a training forward: [G | U] saved as bf16 [R_pad, 2F] (NULL: not saved)
+  uint16_t* gu_out;
+  // GEMM_DGRAD epilogue
+  const uint16_t* gu;      // saved [G | U]
+  uint16_t* dgu;           // [dG | dU] bf16 [R_pad, 2F]
+  uint16_t* hb;            // h bf16 [R_pad, F]
+  float* dgate_part;       // [R_pad, F / 128] partial sums of the routing-weight gradient
+  // GEMM_WGRAD
+  int wg_mt, wg_nt;        // 256-row tiles of A's rows (M / 256) and of B's rows (N / 256)
+  int64_t wg_m, wg_n;      // rows and columns of each expert's gradient block
+  float* dw;               // [E, M, N] fp32
 };
 
 struct TileInfo {
   int e, n, pad_row0, src_row0, valid;
+  // pair kernel: rows of this CTA's A tile and of the pair's two B halves, K offsets, K steps
+  int a_row, b_row0, b_row1, a_k0, b_k0, steps;
 };
 
 // Work unit u -> (expert, column tile, 128-row tile).  Units are ordered expert by expert; inside
@@ -230,6 +252,86 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     const int64_t atom = static_cast<int64_t>(t.pad_row0 / BM) * (p.ldh / 128) + t.n;
     *reinterpret_cast<uint16_t*>(p.hsf + atom * SF_ATOM + (r & 31) * 16 + (r >> 5) * 4 + 2 * half) =
         static_cast<uint16_t>(sf_pair);
+    if (p.gu_out != nullptr) {   // training forward: keep the pre-activations for the backward
+      uint16_t* grow = p.gu_out + static_cast<int64_t>(t.pad_row0 + r) * 2 * p.ldh + t.n * 128 + 64 * half;
+#pragma unroll
+      for (int c = 0; c < 64; c += 8) {
+        uint4 og, ou;
+        og.x = pack_bf16x2(__uint_as_float(v[c + 0]), __uint_as_float(v[c + 1]));
+        og.y = pack_bf16x2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+        og.z = pack_bf16x2(__uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+        og.w = pack_bf16x2(__uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+        ou.x = pack_bf16x2(__uint_as_float(v[64 + c + 0]), __uint_as_float(v[64 + c + 1]));
+        ou.y = pack_bf16x2(__uint_as_float(v[64 + c + 2]), __uint_as_float(v[64 + c + 3]));
+        ou.z = pack_bf16x2(__uint_as_float(v[64 + c + 4]), __uint_as_float(v[64 + c + 5]));
+        ou.w = pack_bf16x2(__uint_as_float(v[64 + c + 6]), __uint_as_float(v[64 + c + 7]));
+        *reinterpret_cast<uint4*>(grow + c) = og;
+        *reinterpret_cast<uint4*>(grow + p.ldh + c) = ou;
+      }
+    }
+  } else if (MODE == GEMM_DGRAD) {
+    // v = dh for 128 columns f of F.  From the saved bf16 pre-activations g, u and the gate:
+    //   s = silu(g) = g * sig(g),  s' = sig(g) * (1 + g * (1 - sig(g)))
+    //   dG = dh * gate * u * s',  dU = dh * gate * s,  h = gate * s * u,  dgate += dh * s * u
+    // dG, dU and h are stored as bf16 (zeros on padding rows, so the column-wise quantizations
+    // and the weight gradients see zero rows there).
+    const int64_t F = p.ldh;
+    const int64_t prow = t.pad_row0 + r;
+    const int f0 = t.n * 256 + 128 * half;
+    uint16_t* dg_row = p.dgu + prow * 2 * F + f0;
+    uint16_t* h_row = p.hb + prow * F + f0;
+    float part = 0.0f;
+    if (r < t.valid) {
+      const float gate = p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f;
+      const uint16_t* g_row = p.gu + prow * 2 * F + f0;
+#pragma unroll
+      for (int c = 0; c < 128; c += 8) {
+        const uint4 gw = __ldcs(reinterpret_cast<const uint4*>(g_row + c));
+        const uint4 uw = __ldcs(reinterpret_cast<const uint4*>(g_row + F + c));
+        const float g[8] = {bf16_lo(gw.x), bf16_hi(gw.x), bf16_lo(gw.y), bf16_hi(gw.y),
+                            bf16_lo(gw.z), bf16_hi(gw.z), bf16_lo(gw.w), bf16_hi(gw.w)};
+        const float u[8] = {bf16_lo(uw.x), bf16_hi(uw.x), bf16_lo(uw.y), bf16_hi(uw.y),
+                            bf16_lo(uw.z), bf16_hi(uw.z), bf16_lo(uw.w), bf16_hi(uw.w)};
+        float dg[8], du[8], hv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float dh = __uint_as_float(v[c + i]);
+          const float sig = 1.0f / (1.0f + __expf(-g[i]));
+          const float sl = g[i] * sig;
+          const float dsl = sig * (1.0f + g[i] * (1.0f - sig));
+          dg[i] = dh * gate * u[i] * dsl;
+          du[i] = dh * gate * sl;
+          hv[i] = gate * sl * u[i];
+          part += dh * sl * u[i];
+        }
+        uint4 o;
+        o = make_uint4(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]), pack_bf16x2(dg[4], dg[5]),
+                       pack_bf16x2(dg[6], dg[7]));
+        *reinterpret_cast<uint4*>(dg_row + c) = o;
+        o = make_uint4(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]), pack_bf16x2(du[4], du[5]),
+                       pack_bf16x2(du[6], du[7]));
+        *reinterpret_cast<uint4*>(dg_row + F + c) = o;
+        o = make_uint4(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]), pack_bf16x2(hv[4], hv[5]),
+                       pack_bf16x2(hv[6], hv[7]));
+        *reinterpret_cast<uint4*>(h_row + c) = o;
+      }
+    } else {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 4
+      for (int c = 0; c < 128; c += 8) {
+        *reinterpret_cast<uint4*>(dg_row + c) = z;
+        *reinterpret_cast<uint4*>(dg_row + F + c) = z;
+        *reinterpret_cast<uint4*>(h_row + c) = z;
+      }
+    }
+    p.dgate_part[prow * (F / 128) + f0 / 128] = part;
+  } else if (MODE == GEMM_WGRAD) {
+    // v = 128 fp32 gradient entries of row a_row + r, columns n*256 + 128*half ..
+    float* drow = p.dw + (static_cast<int64_t>(t.e) * p.wg_m + t.a_row + r) * p.wg_n + t.n * 256 + 128 * half;
+#pragma unroll
+    for (int c = 0; c < 128; c += 4)
+      *reinterpret_cast<float4*>(drow + c) = make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                                                         __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
   } else {
     if (r < t.valid) {
       const int ncols = BN / 2;
@@ -565,6 +667,47 @@ __device__ __forceinline__ void decode_pair_unit(int u, int rank, const GemmPara
   t.valid = min(BM, __ldg(row_off + e + 1) - r0 - BM * tt);
 }
 
+// Pair unit u -> this CTA's tile: rows of its A tile, the pair's two B halves, K offsets and K
+// steps.  Forward and dgrad modes: A rows are expert-padded activation rows (row-tile pairs of an
+// expert, decode_pair_unit), B rows are weight rows.  GEMM_WGRAD: units run expert by expert over
+// (256-row tile of A's rows, 256-row tile of B's rows) with B tiles fastest, and the K range is the
+// expert's padded rows (no steps for an empty expert).
+template <int MODE>
+__device__ __forceinline__ void decode_pair_tile(int u, int rank, const GemmParams& p, TileInfo& t) {
+  if constexpr (MODE == GEMM_WGRAD) {
+    const int32_t* pad_off = reinterpret_cast<const int32_t*>(p.meta + 1) + (p.E + 1);
+    const int per = p.wg_mt * p.wg_nt;
+    const int e = u / per;
+    const int rem = u - e * per;
+    const int mt = rem / p.wg_nt;
+    t.e = e;
+    t.n = rem - mt * p.wg_nt;
+    t.a_row = mt * 256 + 128 * rank;
+    t.b_row0 = t.n * 256;
+    t.b_row1 = t.n * 256 + 128;
+    t.a_k0 = __ldg(pad_off + e);
+    t.b_k0 = t.a_k0;
+    t.steps = (__ldg(pad_off + e + 1) - t.a_k0) / BK;
+    t.pad_row0 = t.a_row;
+    t.src_row0 = 0;
+    t.valid = BM;
+  } else {
+    decode_pair_unit(u, rank, p, t);
+    t.a_row = t.pad_row0;
+    t.b_row0 = b_box_row<MODE>(p, t, 0);
+    t.b_row1 = b_box_row<MODE>(p, t, 1);
+    t.a_k0 = 0;
+    t.b_k0 = t.e * p.b_kofs;
+    t.steps = p.KT;
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ int pair_total_units(const GemmParams& p) {
+  if constexpr (MODE == GEMM_WGRAD) return p.E * p.wg_mt * p.wg_nt;
+  return (p.meta->num_mtiles >> 1) * p.NT;
+}
+
 // Bounded wait shared by the warp (lane 0 polls).  On timeout it records `err_bit`, and raises the
 // abort flag of this CTA and of the other CTA of the pair so that every role of both drains.
 __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
@@ -646,13 +789,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  const int total_units = (p.meta->num_mtiles >> 1) * p.NT;
+  const int total_units = pair_total_units<MODE>(p);
   const int first_unit = static_cast<int>(cluster_index());
   const int unit_stride = static_cast<int>(cluster_count());
   const uint32_t peer_abort = map_to_cta(const_cast<int*>(abort_flag), rank ^ 1u);
   // K steps this pair runs in all (both CTAs run the same sequence of units)
-  const int my_units = first_unit < total_units ? (total_units - first_unit + unit_stride - 1) / unit_stride : 0;
-  const int total_steps = my_units * p.KT;
+  int total_steps = 0;
+  if constexpr (MODE == GEMM_WGRAD) {
+    for (int u = first_unit; u < total_units; u += unit_stride) {
+      TileInfo t;
+      decode_pair_tile<MODE>(u, static_cast<int>(rank), p, t);
+      total_steps += t.steps;
+    }
+  } else {
+    const int my_units = first_unit < total_units ? (total_units - first_unit + unit_stride - 1) / unit_stride : 0;
+    total_steps = my_units * p.KT;
+  }
 
   if (warp < NUM_SF_WARPS) {
     regs_dec<P_REGS_LOW>();
@@ -691,17 +843,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int u = first_unit; ok && u < total_units; u += unit_stride) {
         TileInfo t;
-        decode_pair_unit(u, static_cast<int>(rank), p, t);
-        const int b_own = b_box_row<MODE>(p, t, static_cast<int>(rank));
-        for (int kb = 0; kb < p.KT; ++kb, ++g) {
+        decode_pair_tile<MODE>(u, static_cast<int>(rank), p, t);
+        const int b_own = rank == 0 ? t.b_row0 : t.b_row1;
+        for (int kb = 0; kb < t.steps; ++kb, ++g) {
           if (!pair_wait(&empty[stage], phase ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_PRODUCER, lane)) {
             ok = false;
             break;
           }
           if (lane == 0) {
             uint8_t* sA = smem + stage * P_STAGE_BYTES;
-            tma_load_2d_pair(sA, &tmA, leader_full + stage * 8, kb * BK, t.pad_row0);
-            tma_load_2d_pair(sA + A_BYTES, &tmB, leader_full + stage * 8, kb * BK, b_own);
+            tma_load_2d_pair(sA, &tmA, leader_full + stage * 8, t.a_k0 + kb * BK, t.a_row);
+            tma_load_2d_pair(sA + A_BYTES, &tmB, leader_full + stage * 8, t.b_k0 + kb * BK, b_own);
             if (leader) {
               // The leader's arrival completes the stage only once the step's scales are in both
               // CTAs' TMEM, so the MMA thread waits on this one barrier per step.  The scale ring
@@ -744,34 +896,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == WARP_SF_PRODUCER) {
       // ---------------- scale-atom producer (both CTAs; lane 0 issues) ----------------
       uint32_t issued_mask = 0, issued_parity = 0;
-      TileInfo t{};
-      int64_t a_atom0 = 0, b_atom0 = 0, b_atom1 = 0;
-      for (int g = 0; g < total_steps; ++g) {
-        const int kb = g % p.KT;
-        const int slot = g % P_SF_SLOTS;
-        const int grp = slot / P_SF_GROUP;
-        const uint32_t lap = (g / P_SF_SLOTS) & 1u;
-        if (kb == 0) {
-          decode_pair_unit(first_unit + (g / p.KT) * unit_stride, static_cast<int>(rank), p, t);
-          a_atom0 = static_cast<int64_t>(t.pad_row0 / BM) * p.KT;
-          b_atom0 = static_cast<int64_t>(b_box_row<MODE>(p, t, 0) / 128) * p.KT;
-          b_atom1 = static_cast<int64_t>(b_box_row<MODE>(p, t, 1) / 128) * p.KT;
+      int g = 0;
+      bool ok = true;
+      for (int u = first_unit; ok && u < total_units; u += unit_stride) {
+        TileInfo t;
+        decode_pair_tile<MODE>(u, static_cast<int>(rank), p, t);
+        const int64_t a_atom0 = static_cast<int64_t>(t.a_row / 128) * p.a_kt + t.a_k0 / BK;
+        const int64_t b_atom0 = static_cast<int64_t>(t.b_row0 / 128) * p.b_kt + t.b_k0 / BK;
+        const int64_t b_atom1 = static_cast<int64_t>(t.b_row1 / 128) * p.b_kt + t.b_k0 / BK;
+        for (int kb = 0; kb < t.steps; ++kb, ++g) {
+          const int slot = g % P_SF_SLOTS;
+          const int grp = slot / P_SF_GROUP;
+          const uint32_t lap = (g / P_SF_SLOTS) & 1u;
+          if (slot % P_SF_GROUP == 0) {
+            // the previous lap's MMAs are done with the group; post the bytes of its (up to 4) steps
+            if (!pair_wait(&sf_empty[grp], lap ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_SF, lane)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0)
+              mbar_arrive_expect_tx(&sf_land[grp], min(P_SF_GROUP, total_steps - g) * P_SF_SLOT_BYTES);
+            issued_mask |= 1u << grp;
+            issued_parity = (issued_parity & ~(1u << grp)) | (lap << grp);
+          }
+          if (lane == 0) {
+            uint8_t* dst = sf_ring + slot * P_SF_SLOT_BYTES;
+            bulk_load(dst, p.a_sf + (a_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
+            bulk_load(dst + SF_ATOM, p.b_sf + (b_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
+            bulk_load(dst + 2 * SF_ATOM, p.b_sf + (b_atom1 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
+          }
+          __syncwarp();
         }
-        if (slot % P_SF_GROUP == 0) {
-          // the previous lap's MMAs are done with the group; post the bytes of its (up to 4) steps
-          if (!pair_wait(&sf_empty[grp], lap ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_SF, lane)) break;
-          if (lane == 0)
-            mbar_arrive_expect_tx(&sf_land[grp], min(P_SF_GROUP, total_steps - g) * P_SF_SLOT_BYTES);
-          issued_mask |= 1u << grp;
-          issued_parity = (issued_parity & ~(1u << grp)) | (lap << grp);
-        }
-        if (lane == 0) {
-          uint8_t* dst = sf_ring + slot * P_SF_SLOT_BYTES;
-          bulk_load(dst, p.a_sf + (a_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
-          bulk_load(dst + SF_ATOM, p.b_sf + (b_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
-          bulk_load(dst + 2 * SF_ATOM, p.b_sf + (b_atom1 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
-        }
-        __syncwarp();
       }
       if (lane == 0)
         for (int j = 0; j < P_SF_GROUPS; ++j)
@@ -787,9 +942,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t phase = 0, acc_phase = 0;
         bool issued = false, ok = true;
         for (int u = first_unit; ok && u < total_units; u += unit_stride) {
+          int steps = p.KT;
+          if constexpr (MODE == GEMM_WGRAD) {
+            TileInfo t;
+            decode_pair_tile<MODE>(u, 0, p, t);
+            steps = t.steps;
+            if (steps == 0) continue;   // empty expert: the epilogue writes zeros without the accumulator
+          }
           if (!pair_lane_wait(acc_empty, acc_phase ^ 1u, true, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) break;
           tc_fence_after();
-          for (int kb = 0; kb < p.KT; ++kb) {
+          for (int kb = 0; kb < steps; ++kb) {
             // full implies the step's scales are staged (the leader's producer waited for them)
             if (!pair_lane_wait(&full[stage], phase, false, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) {
               ok = false;
@@ -835,7 +997,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     for (int u = first_unit; u < total_units; u += unit_stride) {
       TileInfo t;
-      decode_pair_unit(u, static_cast<int>(rank), p, t);
+      decode_pair_tile<MODE>(u, static_cast<int>(rank), p, t);
+      if (MODE == GEMM_WGRAD && t.steps == 0) {   // expert without rows: its gradient block is zero
+        float* drow = p.dw + (static_cast<int64_t>(t.e) * p.wg_m + t.a_row + r) * p.wg_n + t.n * 256 + 128 * half;
+        for (int c = 0; c < 128; c += 4) *reinterpret_cast<float4*>(drow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        continue;
+      }
       bool got = true;
       if (warp == FIRST_EPI_WARP && lane == 0)
         got = pair_lane_wait(acc_full, acc_phase, false, abort_flag, peer_abort, p, ERR_TIMEOUT_EPILOGUE);
@@ -953,7 +1120,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
 
 struct DeviceInfo {
   int sms = 0;
-  int pair_clusters[2] = {0, 0};   // co-resident CTA pairs of each pair-kernel instance (0: none)
+  int pair_clusters[4] = {0, 0, 0, 0};   // co-resident CTA pairs of each pair-kernel mode (0: none)
   bool attr_set = false;
 };
 
@@ -1013,9 +1180,12 @@ bool device_setup(DeviceInfo** out) {
     // MXFP8MOE_SINGLE_CTA=1 selects the single-CTA kernels (also used where no CTA pair fits)
     const char* single = getenv("MXFP8MOE_SINGLE_CTA");
     if (single == nullptr || single[0] != '1') {
-      d.pair_clusters[0] = max_pair_clusters<GEMM_SWIGLU>();
-      d.pair_clusters[1] = max_pair_clusters<GEMM_OUT>();
+      d.pair_clusters[GEMM_SWIGLU] = max_pair_clusters<GEMM_SWIGLU>();
+      d.pair_clusters[GEMM_OUT] = max_pair_clusters<GEMM_OUT>();
     }
+    // the backward runs on CTA pairs only
+    d.pair_clusters[GEMM_DGRAD] = max_pair_clusters<GEMM_DGRAD>();
+    d.pair_clusters[GEMM_WGRAD] = max_pair_clusters<GEMM_WGRAD>();
     d.attr_set = true;
   }
   *out = &d;
@@ -1032,7 +1202,7 @@ cudaError_t launch_schedule(const int32_t* split, int E, int64_t R, SchedHeader*
 int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
                        const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
                        const uint8_t* w2_sf, void* y, void* workspace, const WsLayout& L, cudaStream_t stream,
-                       void* const* events, const int32_t* token_of_row, int64_t x_rows) {
+                       void* const* events, const int32_t* token_of_row, int64_t x_rows, uint16_t* gu_out) {
   DeviceInfo* dev = nullptr;
   if (!device_setup(&dev)) return MXFP8_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1077,6 +1247,9 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p1.ldh = F;
   p1.err = &meta->error;
   p1.timeout_ns = kWaitTimeoutNs;
+  p1.a_kt = p1.KT;
+  p1.b_kt = p1.KT;
+  p1.gu_out = gu_out;
   // persistent: one CTA per SM (shared memory, registers and TMEM each allow only one)
   if (dev->pair_clusters[0] > 0) {
     const int c1 = static_cast<int>(
@@ -1104,6 +1277,8 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p2.ldy = H;
   p2.err = &meta->error;
   p2.timeout_ns = kWaitTimeoutNs;
+  p2.a_kt = p2.KT;
+  p2.b_kt = p2.KT;
   if (p2.BN == 256 && dev->pair_clusters[1] > 0) {
     const int c2 = static_cast<int>(
         std::min<int64_t>(dev->pair_clusters[1], std::max<int64_t>(1, static_cast<int64_t>(max_mtiles / 2) * p2.NT)));
@@ -1114,6 +1289,184 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
     if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
   }
   if (!mark(4)) return MXFP8_ERR_CUDA;
+  return MXFP8_OK;
+}
+
+namespace {
+
+// dgates[r] = sum of the partial sums of sorted row r (over the 128-column slices of F), read
+// from the row's place in the expert-padded row space.
+__global__ void __launch_bounds__(256) k_dgate_reduce(const SchedHeader* meta, int E, int64_t R, int nparts,
+                                                     const float* part, float* dgates) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r >= R || meta->num_mtiles == 0) return;
+  const int32_t* row_off = reinterpret_cast<const int32_t*>(meta + 1);
+  const int32_t* pad_off = row_off + (E + 1);
+  int lo = 0, hi = E;   // largest e with row_off[e] <= r, skipping empty experts
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (row_off[mid] <= r) lo = mid; else hi = mid;
+  }
+  const int64_t prow = pad_off[lo] + (r - row_off[lo]);
+  float acc = 0.0f;
+  for (int i = 0; i < nparts; ++i) acc += part[prow * nparts + i];
+  dgates[r] = acc;
+}
+
+template <int MODE>
+int run_pair(const DeviceInfo* dev, int units, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+             cudaStream_t stream) {
+  if (dev->pair_clusters[MODE] <= 0) return MXFP8_ERR_UNSUPPORTED;
+  const int c = std::min(dev->pair_clusters[MODE], std::max(1, units));
+  return launch_pair<MODE>(c, a, b, p, stream) == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+}
+
+}  // namespace
+
+bool bwd_ws_layout(int64_t R, int64_t H, int64_t F, int E, BwdWsLayout* out) {
+  WsLayout f;
+  if (!ws_layout(R, H, F, E, &f)) return false;
+  const size_t rp = static_cast<size_t>(f.r_pad);
+  auto al = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+  BwdWsLayout L{};
+  L.r_pad = f.r_pad;
+  L.meta = 0;
+  L.dyq = f.xq;                                   // after the schedule, as in the forward workspace
+  L.dysf = al(L.dyq + rp * H);
+  L.dyT = al(L.dysf + rp * H / 32);
+  L.dyTsf = al(L.dyT + rp * H);
+  L.xT = al(L.dyTsf + rp * H / 32);
+  L.xTsf = al(L.xT + rp * H);
+  L.dgu = al(L.xTsf + rp * H / 32);
+  L.dguq = al(L.dgu + rp * 2 * F * 2);
+  L.dgusf = al(L.dguq + rp * 2 * F);
+  L.dguT = al(L.dgusf + rp * 2 * F / 32);
+  L.dguTsf = al(L.dguT + rp * 2 * F);
+  L.hb = al(L.dguTsf + rp * 2 * F / 32);
+  L.hT = al(L.hb + rp * F * 2);
+  L.hTsf = al(L.hT + rp * F);
+  L.part = al(L.hTsf + rp * F / 32);
+  L.total = al(L.part + rp * (F / 128) * sizeof(float));
+  *out = L;
+  return true;
+}
+
+int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
+                           const float* gates, const uint16_t* saved_gu, const uint8_t* w1t_q, const uint8_t* w1t_sf,
+                           const uint8_t* w2t_q, const uint8_t* w2t_sf, const void* dy, void* dx, float* dgates,
+                           float* dw1, float* dw2, void* workspace, const BwdWsLayout& L, cudaStream_t stream,
+                           void* const* events) {
+  DeviceInfo* dev = nullptr;
+  if (!device_setup(&dev)) return MXFP8_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SchedHeader* meta = reinterpret_cast<SchedHeader*>(ws + L.meta);
+  const int64_t rp = L.r_pad;
+  auto mark = [&](int i) {
+    return events == nullptr || events[i] == nullptr ||
+           cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess;
+  };
+  CUtensorMap mDy, mW2t, mDgu, mW1t, mDyT, mHT, mDguT, mXT;
+  if (!make_map(&mDy, ws + L.dyq, rp, H) || !make_map(&mW2t, w2t_q, F, static_cast<uint64_t>(E) * H) ||
+      !make_map(&mDgu, ws + L.dguq, rp, 2 * F) || !make_map(&mW1t, w1t_q, H, static_cast<uint64_t>(E) * 2 * F) ||
+      !make_map(&mDyT, ws + L.dyT, H, rp) || !make_map(&mHT, ws + L.hT, F, rp) ||
+      !make_map(&mDguT, ws + L.dguT, 2 * F, rp) || !make_map(&mXT, ws + L.xT, H, rp))
+    return MXFP8_ERR_CUDA;
+
+  // 0: schedule and the quantizations of dy and x
+  if (!mark(0)) return MXFP8_ERR_CUDA;
+  if (launch_schedule(split, E, R, meta, stream) != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (launch_quantize_gather(dy, R, H, meta, E, rp, nullptr, 0, ws + L.dyq, ws + L.dysf, stream) != cudaSuccess)
+    return MXFP8_ERR_CUDA;
+  if (launch_quantize_t(dy, R, H, rp, true, ws + L.dyT, ws + L.dyTsf, meta, E, nullptr, 0, stream) != cudaSuccess ||
+      launch_quantize_t(x_sorted, R, H, rp, true, ws + L.xT, ws + L.xTsf, meta, E, nullptr, 0, stream) != cudaSuccess)
+    return MXFP8_ERR_CUDA;
+  if (!mark(1)) return MXFP8_ERR_CUDA;
+
+  const int pairs = static_cast<int>(rp / 256);
+  GemmParams base{};
+  base.meta = meta;
+  base.E = E;
+  base.F = static_cast<int>(F);
+  base.err = &meta->error;
+  base.timeout_ns = kWaitTimeoutNs;
+  int st;
+
+  // 1: dh = dy W2 (W2 quantized along H) with the ScaledSwiGLU backward -> dGU, h, dgate parts
+  GemmParams pd = base;
+  pd.a_sf = ws + L.dysf;
+  pd.b_sf = w2t_sf;
+  pd.KT = static_cast<int>(H / BK);
+  pd.NT = static_cast<int>(F / 256);
+  pd.BN = 256;
+  pd.b_rows_per_expert = 0;
+  pd.b_kofs = static_cast<int>(H);
+  pd.a_kt = static_cast<int>(H / BK);
+  pd.b_kt = static_cast<int>(static_cast<int64_t>(E) * H / BK);
+  pd.n_fastest = 0;
+  pd.gates = gates;
+  pd.ldh = F;
+  pd.gu = saved_gu;
+  pd.dgu = reinterpret_cast<uint16_t*>(ws + L.dgu);
+  pd.hb = reinterpret_cast<uint16_t*>(ws + L.hb);
+  pd.dgate_part = reinterpret_cast<float*>(ws + L.part);
+  if ((st = run_pair<GEMM_DGRAD>(dev, pairs * pd.NT, mDy, mW2t, pd, stream)) != MXFP8_OK) return st;
+  if (!mark(2)) return MXFP8_ERR_CUDA;
+
+  // 2: quantizations of dGU (row-wise for dx, column-wise for dW1) and of h (column-wise for dW2)
+  if (launch_quantize(ws + L.dgu, rp, 2 * F, MXFP8_ROWWISE, MXFP8_SF_MMA, ws + L.dguq, ws + L.dgusf, nullptr,
+                      nullptr, stream) != cudaSuccess ||
+      launch_quantize_t(ws + L.dgu, rp, 2 * F, rp, true, ws + L.dguT, ws + L.dguTsf, nullptr, E, nullptr, 0,
+                        stream) != cudaSuccess ||
+      launch_quantize_t(ws + L.hb, rp, F, rp, true, ws + L.hT, ws + L.hTsf, nullptr, E, nullptr, 0, stream) !=
+          cudaSuccess)
+    return MXFP8_ERR_CUDA;
+  if (dgates != nullptr) {
+    k_dgate_reduce<<<static_cast<unsigned>((R + 255) / 256 > 0 ? (R + 255) / 256 : 1), 256, 0, stream>>>(
+        meta, E, R, static_cast<int>(F / 128), reinterpret_cast<const float*>(ws + L.part), dgates);
+    if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
+  }
+  if (!mark(3)) return MXFP8_ERR_CUDA;
+
+  // 3: dx = dGU W1 (W1 quantized along 2F)
+  GemmParams px = base;
+  px.a_sf = ws + L.dgusf;
+  px.b_sf = w1t_sf;
+  px.KT = static_cast<int>(2 * F / BK);
+  px.NT = static_cast<int>(H / 256);
+  px.BN = 256;
+  px.b_rows_per_expert = 0;
+  px.b_kofs = static_cast<int>(2 * F);
+  px.a_kt = px.KT;
+  px.b_kt = static_cast<int>(static_cast<int64_t>(E) * 2 * F / BK);
+  px.n_fastest = 1;
+  px.y = static_cast<uint16_t*>(dx);
+  px.ldy = H;
+  if ((st = run_pair<GEMM_OUT>(dev, pairs * px.NT, mDgu, mW1t, px, stream)) != MXFP8_OK) return st;
+  if (!mark(4)) return MXFP8_ERR_CUDA;
+
+  // 4: weight gradients over each expert's rows
+  GemmParams pw = base;
+  pw.a_kt = static_cast<int>(rp / BK);
+  pw.b_kt = pw.a_kt;
+  pw.KT = 0;
+  pw.a_sf = ws + L.dyTsf;
+  pw.b_sf = ws + L.hTsf;
+  pw.wg_mt = static_cast<int>(H / 256);
+  pw.wg_nt = static_cast<int>(F / 256);
+  pw.wg_m = H;
+  pw.wg_n = F;
+  pw.dw = dw2;
+  if ((st = run_pair<GEMM_WGRAD>(dev, E * pw.wg_mt * pw.wg_nt, mDyT, mHT, pw, stream)) != MXFP8_OK) return st;
+  if (!mark(5)) return MXFP8_ERR_CUDA;
+  pw.a_sf = ws + L.dguTsf;
+  pw.b_sf = ws + L.xTsf;
+  pw.wg_mt = static_cast<int>(2 * F / 256);
+  pw.wg_nt = static_cast<int>(H / 256);
+  pw.wg_m = 2 * F;
+  pw.wg_n = H;
+  pw.dw = dw1;
+  if ((st = run_pair<GEMM_WGRAD>(dev, E * pw.wg_mt * pw.wg_nt, mDguT, mXT, pw, stream)) != MXFP8_OK) return st;
+  if (!mark(6)) return MXFP8_ERR_CUDA;
   return MXFP8_OK;
 }
 

@@ -22,8 +22,8 @@ constexpr uint32_t ERR_TIMEOUT_MASK = 0x1F00u;
 
 // Device schedule written by the schedule kernel at the start of the workspace.  Arrays of E+1
 // int32 follow the header: row_off (prefix sums of split_sizes), pad_off (prefix sums of
-// 128 * ceil(split/128): each expert's first row in the padded row space), mt_off (prefix sums
-// of ceil(split/128): each expert's first 128-row tile).
+// 256 * ceil(split/256): each expert's first row in the padded row space), mt_off (prefix sums
+// of 2 * ceil(split/256): each expert's first 128-row tile).
 struct SchedHeader {
   uint32_t error;
   int32_t num_mtiles;   // total 128-row tiles over all experts (0 on a split error)
@@ -39,6 +39,22 @@ struct WsLayout {
 };
 bool ws_layout(int64_t R, int64_t H, int64_t F, int E, WsLayout* out);
 
+// Backward workspace: schedule, then (all in the expert-padded row space of r_pad rows)
+//   dyq/dysf    dy row-wise (blocks along H), tensor-core scale layout        [r_pad, H]
+//   dyT/dyTsf   dy column-wise, codes transposed (blocks along rows)          [H, r_pad]
+//   xT/xTsf     x column-wise, transposed                                    [H, r_pad]
+//   dgu         [dG | dU] bf16                                               [r_pad, 2F]
+//   dguq/dgusf  dGU row-wise                                                 [r_pad, 2F]
+//   dguT/dguTsf dGU column-wise, transposed                                  [2F, r_pad]
+//   hb          h bf16                                                       [r_pad, F]
+//   hT/hTsf     h column-wise, transposed                                    [F, r_pad]
+//   part        partial sums of the routing-weight gradient (float)          [r_pad, F/128]
+struct BwdWsLayout {
+  size_t meta, dyq, dysf, dyT, dyTsf, xT, xTsf, dgu, dguq, dgusf, dguT, dguTsf, hb, hT, hTsf, part, total;
+  int64_t r_pad;
+};
+bool bwd_ws_layout(int64_t R, int64_t H, int64_t F, int E, BwdWsLayout* out);
+
 // Quantize launchers (quantize.cu).  Return a cudaError_t from the launch.
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int dirs, int sf_layout, uint8_t* q_row,
                             uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, cudaStream_t stream);
@@ -48,6 +64,13 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int dirs, int s
 cudaError_t launch_quantize_gather(const void* x, int64_t R, int64_t H, const SchedHeader* meta, int E,
                                    int64_t r_pad, const int32_t* token_of_row, int64_t x_rows, uint8_t* xq,
                                    uint8_t* xsf, cudaStream_t stream);
+// Column-wise MXFP8 with transposed codes: x [M, K] -> qT [K, m_out] (m_out % 128 == 0), scale
+// bytes in the tensor-core layout of [K, m_out] (mma) or compact [K, m_out/32].  With meta, the
+// m_out rows are the expert-padded row space gathered from the sorted rows of x (through
+// token_of_row when given; then x has x_rows rows).
+cudaError_t launch_quantize_t(const void* x, int64_t M, int64_t K, int64_t m_out, bool mma, uint8_t* qT,
+                              uint8_t* sfT, const SchedHeader* meta, int E, const int32_t* token_of_row,
+                              int64_t x_rows, cudaStream_t stream);
 
 // Dispatch and combine around the grouped MLP (moe_routing.cu).
 size_t permute_workspace_bytes(int64_t n, int E);
@@ -66,6 +89,16 @@ cudaError_t launch_schedule(const int32_t* split, int E, int64_t R, SchedHeader*
 int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
                        const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q,
                        const uint8_t* w2_sf, void* y, void* workspace, const WsLayout& L, cudaStream_t stream,
-                       void* const* events, const int32_t* token_of_row = nullptr, int64_t x_rows = 0);
+                       void* const* events, const int32_t* token_of_row = nullptr, int64_t x_rows = 0,
+                       uint16_t* gu_out = nullptr);
+// gu_out (may be NULL): training forward, [G | U] saved as bf16 [r_pad, 2F] for the backward.
+
+// Backward of the grouped MLP (all GEMMs on CTA pairs; needs H % 256 == 0 and F % 256 == 0).
+// `events` (may be null): 7 events recorded on `stream` around its stages.
+int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
+                           const float* gates, const uint16_t* saved_gu, const uint8_t* w1t_q, const uint8_t* w1t_sf,
+                           const uint8_t* w2t_q, const uint8_t* w2t_sf, const void* dy, void* dx, float* dgates,
+                           float* dw1, float* dw2, void* workspace, const BwdWsLayout& L, cudaStream_t stream,
+                           void* const* events);
 
 }  // namespace mx

@@ -209,6 +209,102 @@ __global__ void __launch_bounds__(QT_THREADS, (ROW && COL) || GATHER ? 3 : 4) k_
   }
 }
 
+// Column-wise MXFP8 with the codes written transposed, for GEMMs that contract over the rows of
+// a matrix (the weight gradients, and the backward GEMMs that contract weights over their other
+// axis).  Source [M, K] bf16 -> qT [K, m_out]: row c of qT holds column c of the source, each run
+// of 32 consecutive source rows is one block.  Scale bytes go to sfT: the tensor-core layout of
+// the [K, m_out] code matrix, or compact [K, m_out / 32].  GATHER: source rows are the
+// expert-padded row space (as in k_quantize), padding rows are zeros.
+//
+// One CTA of 256 threads owns 128 source rows x 64 source columns: the tile is read with 128-bit
+// loads into shared memory (16 KB), then thread t takes column t % 64 and 32-row block t / 64,
+// reads its 32 values down the column (a warp reads 32 adjacent columns of one row: no bank
+// conflicts), and writes its 32 codes as two 16-byte stores.
+constexpr int QTT_ROWS = 128;
+constexpr int QTT_COLS = 64;
+
+struct QuantTArgs {
+  const uint16_t* x;
+  int64_t M, K;        // source rows (rows past M read as zeros) / columns
+  int64_t m_out;       // columns of qT (rows of the source space, a multiple of 128 in MMA layout)
+  uint8_t* qT;
+  uint8_t* sfT;
+  bool mma;
+  const SchedHeader* meta;  // gather mode only
+  int E;
+  const int32_t* tok;
+};
+
+template <bool GATHER>
+__global__ void __launch_bounds__(256) k_quantize_t(const QuantTArgs a) {
+  __shared__ __align__(16) uint16_t tile[QTT_ROWS][QTT_COLS + 8];
+  const int tid = threadIdx.x;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * QTT_ROWS;
+  const int64_t col0 = static_cast<int64_t>(blockIdx.y) * QTT_COLS;
+  // source row of every tile row (-1: zero row)
+  int64_t first_src = row0;
+  int64_t nsrc = a.M - row0;
+  if constexpr (GATHER) {
+    const int32_t pad_rows = a.meta->pad_rows;
+    if (row0 >= pad_rows) {
+      nsrc = 0;
+    } else {
+      const int32_t* row_off = reinterpret_cast<const int32_t*>(a.meta + 1);
+      const int32_t* pad_off = row_off + (a.E + 1);
+      int lo = 0, hi = a.E;   // largest e with pad_off[e] <= row0 (experts span whole 256-row pairs)
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pad_off[mid] <= row0) lo = mid; else hi = mid;
+      }
+      first_src = row_off[lo] + (row0 - pad_off[lo]);
+      nsrc = (row_off[lo + 1] - row_off[lo]) - (row0 - pad_off[lo]);
+    }
+  }
+  nsrc = nsrc < 0 ? 0 : (nsrc > QTT_ROWS ? QTT_ROWS : nsrc);
+  // load: 128 rows x 8 chunks of 16 bytes; thread t takes chunk t % 8 of rows t / 8 + 32 j
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int rr = tid / 8 + 32 * j;
+    const int ch = tid % 8;
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (rr < nsrc) {
+      int64_t src = first_src + rr;
+      if (GATHER && a.tok != nullptr) {
+        src = __ldg(a.tok + src);
+        if (src < 0 || src >= a.M) {
+          atomicOr(const_cast<uint32_t*>(&a.meta->error), ERR_TOKEN_RANGE);
+          src = -1;
+        }
+      }
+      if (src >= 0 && col0 + ch * 8 < a.K) w = __ldcs(reinterpret_cast<const uint4*>(a.x + src * a.K + col0 + ch * 8));
+    }
+    *reinterpret_cast<uint4*>(&tile[rr][ch * 8]) = w;
+  }
+  __syncthreads();
+  const int c = tid % QTT_COLS;
+  const int rb = tid / QTT_COLS;   // 32-row block inside the tile
+  const int64_t col = col0 + c;
+  if (col >= a.K) return;
+  float v[32];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = __uint_as_float(static_cast<uint32_t>(tile[rb * 32 + i][c]) << 16);
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  const uint32_t sfb = e8m0_from_amax(amax);
+  const float inv = e8m0_inverse_scale(sfb);
+  const uint2 q0 = quant8(v + 0, inv), q1 = quant8(v + 8, inv), q2 = quant8(v + 16, inv), q3 = quant8(v + 24, inv);
+  uint8_t* dst = a.qT + col * a.m_out + row0 + rb * 32;
+  reinterpret_cast<uint4*>(dst)[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
+  reinterpret_cast<uint4*>(dst)[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
+  const int64_t blk = (row0 >> 5) + rb;
+  if (a.mma)
+    a.sfT[sf_mma_offset(col, blk, a.m_out / 128)] = static_cast<uint8_t>(sfb);
+  else
+    a.sfT[col * (a.m_out >> 5) + blk] = static_cast<uint8_t>(sfb);
+}
+
 template <bool ROW, bool COL, bool MMA>
 cudaError_t launch_dirs(const QuantArgs& a, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>((a.M + QT_ROWS - 1) / QT_ROWS),
@@ -253,6 +349,29 @@ cudaError_t launch_quantize_gather(const void* x, int64_t R, int64_t H, const Sc
   const dim3 grid(static_cast<unsigned>((r_pad + QT_ROWS - 1) / QT_ROWS),
                   static_cast<unsigned>((H + QT_COLS - 1) / QT_COLS));
   k_quantize<true, false, true, true><<<grid, QT_THREADS, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_t(const void* x, int64_t M, int64_t K, int64_t m_out, bool mma, uint8_t* qT,
+                              uint8_t* sfT, const SchedHeader* meta, int E, const int32_t* token_of_row,
+                              int64_t x_rows, cudaStream_t stream) {
+  QuantTArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.M = meta ? (token_of_row ? x_rows : M) : M;
+  a.K = K;
+  a.m_out = m_out;
+  a.qT = qT;
+  a.sfT = sfT;
+  a.mma = mma;
+  a.meta = meta;
+  a.E = E;
+  a.tok = token_of_row;
+  const dim3 grid(static_cast<unsigned>((m_out + QTT_ROWS - 1) / QTT_ROWS),
+                  static_cast<unsigned>((K + QTT_COLS - 1) / QTT_COLS));
+  if (meta)
+    k_quantize_t<true><<<grid, 256, 0, stream>>>(a);
+  else
+    k_quantize_t<false><<<grid, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
