@@ -334,6 +334,88 @@ def run_native(args, world, rank, local):
                 "kernel_ms": kern_ms,
                 "grouped_linear2": {"achieved": g2_tflops, "frac": g2_tflops / fp8_peak}}
 
+    def measure_backward():
+        # ---- backward (training): fwd_train saves [G | U]; the backward runs on a resident dy ----
+        bwd = None
+        if H % 256 == 0 and F % 256 == 0:
+            w1b, w2b = bf(w.w1), bf(w.w2)
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w1t = mx.mxfp8_quantize_colwise_t(w1b)
+            w2t = mx.mxfp8_quantize_colwise_t(w2b)
+            t0.record()
+            mx.mxfp8_quantize_colwise_t(w1b, out=w1t)
+            mx.mxfp8_quantize_colwise_t(w2b, out=w2t)
+            t1.record()
+            torch.cuda.synchronize()
+            wt_ms = t0.elapsed_time(t1)
+            del w1b, w2b
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(1)
+            dy = torch.randn((R, H), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+            saved = torch.empty(mx.grouped_mlp_saved_bytes(R, H, F, E), dtype=torch.uint8, device=dev)
+            bws = torch.empty(mx.grouped_mlp_bwd_workspace_size(R, H, F, E), dtype=torch.uint8, device=dev)
+            dx = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+            dgt = torch.empty(R, dtype=torch.float32, device=dev)
+            dw1 = torch.empty((E, 2 * F, H), dtype=torch.float32, device=dev)
+            dw2 = torch.empty((E, H, F), dtype=torch.float32, device=dev)
+
+            def fwd_train():
+                mx.grouped_mlp_fwd_train(x, split, gates, w1q, w1s, w2q, w2s, y=y, saved=saved, workspace=ws)
+
+            def bwd_step(evs=None):
+                mx.grouped_mlp_bwd(x, split, gates, saved, w1t[0], w1t[1], w2t[0], w2t[1], dy, dx=dx,
+                                   dgates=dgt if gates is not None else False, dw1=dw1, dw2=dw2, workspace=bws,
+                                   stage_events=evs)
+
+            fwd_train()
+            for _ in range(max(3, args.warmup)):
+                bwd_step()
+            torch.cuda.synchronize()
+            for wsx in (ws, bws):
+                st, bits = mx.mxfp8_check_device_error(wsx)
+                if st != 0:
+                    raise RuntimeError(f"device error word {bits:#x} in the backward")
+            nb = max(3, args.steps)
+            bev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(nb)]
+            for evs in bev:
+                for ev in evs:
+                    ev.record()
+            torch.cuda.synchronize()
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record()
+            for _ in range(nb):
+                fwd_train()
+            f1.record()
+            torch.cuda.synchronize()
+            ftrain_ms = f0.elapsed_time(f1) / nb
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record()
+            for i in range(nb):
+                bwd_step(bev[i])
+            b1.record()
+            torch.cuda.synchronize()
+            bwd_ms = b0.elapsed_time(b1) / nb
+            names = ["quantize_dy_x", "dgrad2_swiglu_bwd", "quantize_dgu_h_dgate", "dgrad1", "wgrad2", "wgrad1"]
+            stage = {n: sum(e[j].elapsed_time(e[j + 1]) for e in bev) / nb for j, n in enumerate(names)}
+            bflops = 12.0 * R * H * F
+            fp8_peak_b = peaks["bf16_tflops"] * FP8_OVER_BF16
+            gemm_tf = {"dgrad2_swiglu_bwd": 2.0 * R * H * F, "dgrad1": 4.0 * R * H * F, "wgrad2": 2.0 * R * H * F,
+                       "wgrad1": 4.0 * R * H * F}
+            bwd = {"ms": bwd_ms, "tflops": bflops / (bwd_ms * 1e-3) / 1e12, "flops_per_step": bflops,
+                   "stage_ms": stage,
+                   "gemm_frac_of_peak": {k: v / (stage[k] * 1e-3) / 1e12 / fp8_peak_b for k, v in gemm_tf.items()},
+                   "fwd_train_ms": ftrain_ms,
+                   "train_step_tflops": 18.0 * R * H * F / ((bwd_ms + ftrain_ms) * 1e-3) / 1e12,
+                   "weight_quantize_transposed_ms": wt_ms,
+                   "note": "flops = 12 R H F (dh, dx, dW2, dW1); dy resident, no L2 flush (operands above L2)"}
+            del dy, saved, bws, dx, dgt, dw1, dw2, w1t, w2t
+
+        return bwd
+
+    if args.only == "bwd":
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, "backward": measure_backward()}), flush=True)
+        return
     if args.only == "fwd":
         if rank == 0:
             print(json.dumps({"workload": args.workload, "ms_per_step": step_ms, "value": value,
@@ -408,6 +490,8 @@ def run_native(args, world, rank, local):
                  "l2": "no flush: per-launch inputs above L2 except the permute's 128 KB of ids"}
         del xt, out
 
+    bwd = measure_backward()
+
     # ---- end to end through the public API with host buffers ----
     # Every step copies its inputs from pinned host memory and its output back.  Steps are
     # pipelined over three streams with double-buffered device x / y: the host->device copy of
@@ -481,7 +565,8 @@ def run_native(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
-            "config": workload_config(w), "roofline": roofline, "quantize": quant, "moe_layer": layer, "e2e": e2e,
+            "config": workload_config(w), "roofline": roofline, "quantize": quant, "moe_layer": layer, "backward": bwd,
+            "e2e": e2e,
             "cpu_baseline": cpu, "clocks": clocks, "gpu_launches": 4 * args.steps,
             "weight_quantize_ms": weight_quant_ms, "peaks": {"source": peak_src, **peaks},
         }
@@ -500,8 +585,9 @@ def main():
                     help="length of the timed oracle call behind cpu_baseline")
     ap.add_argument("--workload", choices=["mixtral", "llama", "fine", "tiny"], default=WORKLOAD,
                     help="workload of the timed step (the headline line uses mixtral)")
-    ap.add_argument("--only", choices=["all", "fwd"], default="all",
-                    help="fwd: time the forward only and print a short line (profiling runs)")
+    ap.add_argument("--only", choices=["all", "fwd", "bwd"], default="all",
+                    help="fwd / bwd: time the forward (or forward + backward) only and print a short line "
+                         "(profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -124,6 +124,7 @@ struct GemmParams {
   float* dgate_part;       // [R_pad, F / 128] partial sums of the routing-weight gradient
   // GEMM_WGRAD
   int wg_mt, wg_nt;        // 256-row tiles of A's rows (M / 256) and of B's rows (N / 256)
+  int wg_m_fastest;        // 1: A tiles run fastest inside an expert (keeps the smaller A block in L2)
   int64_t wg_m, wg_n;      // rows and columns of each expert's gradient block
   float* dw;               // [E, M, N] fp32
 };
@@ -214,6 +215,14 @@ __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Saved pre-activations [G | U] ([r_pad, 2F] bf16) are stored in blocks of 32 rows x 8 columns
+// (512 contiguous bytes, row-major inside): the epilogue thread of padded row p reads and writes
+// 8 columns with one 16-byte access, and the 32 lanes of a warp (32 consecutive rows) cover one
+// block, so every such warp access is one contiguous 512-byte transfer.
+__device__ __forceinline__ int64_t gu_offset(int64_t prow, int64_t j, int64_t two_f) {
+  return ((prow >> 5) * (two_f >> 3) + (j >> 3)) * 256 + (prow & 31) * 8 + (j & 7);
+}
+
 // Epilogue math of one tile for the thread holding tile row r and column half `half`, from the
 // accumulator values v already read out of TMEM.
 //   GEMM_SWIGLU: v[0..63] gate columns 64*half.., v[64..127] the matching up columns;
@@ -253,7 +262,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     *reinterpret_cast<uint16_t*>(p.hsf + atom * SF_ATOM + (r & 31) * 16 + (r >> 5) * 4 + 2 * half) =
         static_cast<uint16_t>(sf_pair);
     if (p.gu_out != nullptr) {   // training forward: keep the pre-activations for the backward
-      uint16_t* grow = p.gu_out + static_cast<int64_t>(t.pad_row0 + r) * 2 * p.ldh + t.n * 128 + 64 * half;
+      const int64_t prow = t.pad_row0 + r, j0 = t.n * 128 + 64 * half;
 #pragma unroll
       for (int c = 0; c < 64; c += 8) {
         uint4 og, ou;
@@ -265,8 +274,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
         ou.y = pack_bf16x2(__uint_as_float(v[64 + c + 2]), __uint_as_float(v[64 + c + 3]));
         ou.z = pack_bf16x2(__uint_as_float(v[64 + c + 4]), __uint_as_float(v[64 + c + 5]));
         ou.w = pack_bf16x2(__uint_as_float(v[64 + c + 6]), __uint_as_float(v[64 + c + 7]));
-        *reinterpret_cast<uint4*>(grow + c) = og;
-        *reinterpret_cast<uint4*>(grow + p.ldh + c) = ou;
+        *reinterpret_cast<uint4*>(p.gu_out + gu_offset(prow, j0 + c, 2 * p.ldh)) = og;
+        *reinterpret_cast<uint4*>(p.gu_out + gu_offset(prow, p.ldh + j0 + c, 2 * p.ldh)) = ou;
       }
     }
   } else if (MODE == GEMM_DGRAD) {
@@ -283,11 +292,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     float part = 0.0f;
     if (r < t.valid) {
       const float gate = p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f;
-      const uint16_t* g_row = p.gu + prow * 2 * F + f0;
+      // blocked layout (gu_offset), prefetched into L2 at the tile's start
 #pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-        const uint4 gw = __ldcs(reinterpret_cast<const uint4*>(g_row + c));
-        const uint4 uw = __ldcs(reinterpret_cast<const uint4*>(g_row + F + c));
+      for (int c0 = 0; c0 < 128; c0 += 16) {
+        // the four 16-byte loads of 16 columns go out together
+        uint4 gw2[2], uw2[2];
+        gw2[0] = __ldg(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, f0 + c0, 2 * F)));
+        gw2[1] = __ldg(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, f0 + c0 + 8, 2 * F)));
+        uw2[0] = __ldg(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + f0 + c0, 2 * F)));
+        uw2[1] = __ldg(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + f0 + c0 + 8, 2 * F)));
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+        const int c = c0 + 8 * hh;
+        const uint4 gw = gw2[hh], uw = uw2[hh];
         const float g[8] = {bf16_lo(gw.x), bf16_hi(gw.x), bf16_lo(gw.y), bf16_hi(gw.y),
                             bf16_lo(gw.z), bf16_hi(gw.z), bf16_lo(gw.w), bf16_hi(gw.w)};
         const float u[8] = {bf16_lo(uw.x), bf16_hi(uw.x), bf16_lo(uw.y), bf16_hi(uw.y),
@@ -296,7 +313,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float dh = __uint_as_float(v[c + i]);
-          const float sig = 1.0f / (1.0f + __expf(-g[i]));
+          const float sig = __fdividef(1.0f, 1.0f + __expf(-g[i]));
           const float sl = g[i] * sig;
           const float dsl = sig * (1.0f + g[i] * (1.0f - sig));
           dg[i] = dh * gate * u[i] * dsl;
@@ -314,6 +331,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
         o = make_uint4(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]), pack_bf16x2(hv[4], hv[5]),
                        pack_bf16x2(hv[6], hv[7]));
         *reinterpret_cast<uint4*>(h_row + c) = o;
+        }
       }
     } else {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -679,9 +697,15 @@ __device__ __forceinline__ void decode_pair_tile(int u, int rank, const GemmPara
     const int per = p.wg_mt * p.wg_nt;
     const int e = u / per;
     const int rem = u - e * per;
-    const int mt = rem / p.wg_nt;
+    int mt;
+    if (p.wg_m_fastest) {
+      t.n = rem / p.wg_mt;
+      mt = rem - t.n * p.wg_mt;
+    } else {
+      mt = rem / p.wg_nt;
+      t.n = rem - mt * p.wg_nt;
+    }
     t.e = e;
-    t.n = rem - mt * p.wg_nt;
     t.a_row = mt * 256 + 128 * rank;
     t.b_row0 = t.n * 256;
     t.b_row1 = t.n * 256 + 128;
@@ -845,6 +869,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         TileInfo t;
         decode_pair_tile<MODE>(u, static_cast<int>(rank), p, t);
         const int b_own = rank == 0 ? t.b_row0 : t.b_row1;
+        if constexpr (MODE == GEMM_DGRAD) {
+          // the epilogue of this tile reads the saved g and u of its 128 rows x 256 columns of F:
+          // have L2 fetch them while the tile's MMAs run (in the blocked layout each 32-row block's
+          // 256 columns of G, and of U, are 16 KB in one piece)
+          if (lane < 8) {
+            const int64_t prow = t.pad_row0 + 32 * (lane & 3);
+            const int64_t j = (lane < 4 ? 0 : p.ldh) + t.n * 256;
+            prefetch_l2(p.gu + gu_offset(prow, j, 2 * p.ldh), 16384);
+          }
+        }
         for (int kb = 0; kb < t.steps; ++kb, ++g) {
           if (!pair_wait(&empty[stage], phase ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_PRODUCER, lane)) {
             ok = false;
@@ -1455,6 +1489,7 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   pw.wg_nt = static_cast<int>(F / 256);
   pw.wg_m = H;
   pw.wg_n = F;
+  pw.wg_m_fastest = 1;   // dy^T (H rows) is the smaller operand: keep it in L2, stream h^T once
   pw.dw = dw2;
   if ((st = run_pair<GEMM_WGRAD>(dev, E * pw.wg_mt * pw.wg_nt, mDyT, mHT, pw, stream)) != MXFP8_OK) return st;
   if (!mark(5)) return MXFP8_ERR_CUDA;
@@ -1464,6 +1499,7 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   pw.wg_nt = static_cast<int>(H / 256);
   pw.wg_m = 2 * F;
   pw.wg_n = H;
+  pw.wg_m_fastest = 0;   // x^T (H rows) is the smaller operand: keep it in L2, stream dGU^T once
   pw.dw = dw1;
   if ((st = run_pair<GEMM_WGRAD>(dev, E * pw.wg_mt * pw.wg_nt, mDguT, mXT, pw, stream)) != MXFP8_OK) return st;
   if (!mark(6)) return MXFP8_ERR_CUDA;

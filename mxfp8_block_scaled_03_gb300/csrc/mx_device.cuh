@@ -294,6 +294,11 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
     if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
 }
+// Ask L2 to fetch [p, p + bytes) ahead of its use (16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
 // Tile copy into this CTA's shared memory whose completion is counted on an mbarrier that may sit
 // in either CTA of the pair (`bar_cluster` is a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int32_t x,
