@@ -297,10 +297,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
       for (int c0 = 0; c0 < 128; c0 += 16) {
         // the four 16-byte loads of 16 columns go out together
         uint4 gw2[2], uw2[2];
-        gw2[0] = __ldg(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, f0 + c0, 2 * F)));
-        gw2[1] = __ldg(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, f0 + c0 + 8, 2 * F)));
-        uw2[0] = __ldg(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + f0 + c0, 2 * F)));
-        uw2[1] = __ldg(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + f0 + c0 + 8, 2 * F)));
+        gw2[0] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, f0 + c0, 2 * F)));
+        gw2[1] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, f0 + c0 + 8, 2 * F)));
+        uw2[0] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + f0 + c0, 2 * F)));
+        uw2[1] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + f0 + c0 + 8, 2 * F)));
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
         const int c = c0 + 8 * hh;
@@ -324,13 +324,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
         uint4 o;
         o = make_uint4(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]), pack_bf16x2(dg[4], dg[5]),
                        pack_bf16x2(dg[6], dg[7]));
-        *reinterpret_cast<uint4*>(dg_row + c) = o;
+        __stcs(reinterpret_cast<uint4*>(dg_row + c), o);
         o = make_uint4(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]), pack_bf16x2(du[4], du[5]),
                        pack_bf16x2(du[6], du[7]));
-        *reinterpret_cast<uint4*>(dg_row + F + c) = o;
+        __stcs(reinterpret_cast<uint4*>(dg_row + F + c), o);
         o = make_uint4(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]), pack_bf16x2(hv[4], hv[5]),
                        pack_bf16x2(hv[6], hv[7]));
-        *reinterpret_cast<uint4*>(h_row + c) = o;
+        __stcs(reinterpret_cast<uint4*>(h_row + c), o);
         }
       }
     } else {
@@ -861,6 +861,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_PRODUCER) {
       // ---------------- tile producer (both CTAs; lane 0 issues) ----------------
       const uint32_t leader_full = map_to_cta(full, 0);
+      const uint64_t a_policy = l2_policy_evict_last();
       uint32_t issued_mask = 0, issued_parity = 0;
       int stage = 0, g = 0;
       uint32_t phase = 0;
@@ -886,7 +887,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (lane == 0) {
             uint8_t* sA = smem + stage * P_STAGE_BYTES;
-            tma_load_2d_pair(sA, &tmA, leader_full + stage * 8, t.a_k0 + kb * BK, t.a_row);
+            if constexpr (MODE == GEMM_DGRAD)   // dy tiles are reused by every column tile: keep them in L2
+              tma_load_2d_pair_hint(sA, &tmA, leader_full + stage * 8, t.a_k0 + kb * BK, t.a_row, a_policy);
+            else
+              tma_load_2d_pair(sA, &tmA, leader_full + stage * 8, t.a_k0 + kb * BK, t.a_row);
             tma_load_2d_pair(sA + A_BYTES, &tmB, leader_full + stage * 8, t.b_k0 + kb * BK, b_own);
             if (leader) {
               // The leader's arrival completes the stage only once the step's scales are in both
