@@ -249,6 +249,27 @@ int grouped_mlp_bwd_timed(const void* x_sorted, int64_t R, int64_t H, int64_t F,
                           void* dx, float* dgates, float* dw1, float* dw2, void* workspace, size_t workspace_bytes,
                           void* stream, void* const* stage_events);
 
+/* The MoE layer in training (f1 around the backward): grouped_mlp_fwd_tokens_train is
+ * grouped_mlp_fwd_tokens that also saves the pre-activations (as grouped_mlp_fwd_train);
+ * grouped_mlp_bwd_tokens is grouped_mlp_bwd reading x and the output gradient as token rows:
+ * sorted row r reads row token_of_row[r] of x_tokens [T, H] and of d_out_tokens [T, H].  That
+ * gather is the gradient of moe_combine; the caller finishes the layer's backward with
+ * moe_combine(dx_rows, row_of_slot) (the gradient of the token gather) and picks
+ * dgates_sorted[row_of_slot[t, j]] for the routing weight of (t, j).  Other arguments, outputs
+ * and errors as grouped_mlp_fwd_train / grouped_mlp_bwd (dx_rows and dgates_sorted in sorted-row
+ * order); token ids outside [0, T) read zero rows and set MXFP8_ERR_INVALID_ARG in the workspace
+ * error word. */
+int grouped_mlp_fwd_tokens_train(const void* x_tokens, int64_t T, const int32_t* token_of_row, int64_t R,
+                                 int64_t H, int64_t F, int E, const int32_t* split_sizes, const float* gates_sorted,
+                                 const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q, const uint8_t* w2_sf,
+                                 void* y_rows, void* saved, size_t saved_bytes, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+int grouped_mlp_bwd_tokens(const void* x_tokens, int64_t T, const int32_t* token_of_row, int64_t R, int64_t H,
+                           int64_t F, int E, const int32_t* split_sizes, const float* gates_sorted, const void* saved,
+                           size_t saved_bytes, const uint8_t* w1t_q, const uint8_t* w1t_sf, const uint8_t* w2t_q,
+                           const uint8_t* w2t_sf, const void* d_out_tokens, void* dx_rows, float* dgates_sorted,
+                           float* dw1, float* dw2, void* workspace, size_t workspace_bytes, void* stream);
+
 /* mxfp8_quantize_colwise_t -- column-wise MXFP8 (blocks of 32 consecutive rows, item 2) with the
  * codes written transposed, the operand form of GEMMs that contract over x's rows.
  *   x    (device) bf16 [M, K], row-major.

@@ -29,7 +29,8 @@ __all__ = [
     "mxfp8_sf_bytes", "mxfp8_quantize", "grouped_mlp_workspace_size", "grouped_mlp_workspace_layout",
     "grouped_mlp_fwd", "grouped_mlp_fwd_noalloc", "grouped_mlp_fwd_tokens", "moe_permute",
     "moe_permute_workspace_size", "moe_combine", "mxfp8_check_device_error", "mxfp8_quantize_colwise_t",
-    "grouped_mlp_saved_bytes", "grouped_mlp_fwd_train", "grouped_mlp_bwd_workspace_size", "grouped_mlp_bwd", "mxfp8_status_string", "mxfp8_abi_version",
+    "grouped_mlp_saved_bytes", "grouped_mlp_fwd_train", "grouped_mlp_bwd_workspace_size", "grouped_mlp_bwd",
+    "grouped_mlp_fwd_tokens_train", "grouped_mlp_bwd_tokens", "mxfp8_status_string", "mxfp8_abi_version",
 ]
 
 ROWWISE = 1
@@ -89,6 +90,12 @@ def lib() -> ctypes.CDLL:
             L.grouped_mlp_bwd.argtypes = [P, i64, i64, i64, i32, P, P, P, sz, P, P, P, P, P, P, P, P, P, P, sz, P]
             L.grouped_mlp_bwd_timed.restype = i32
             L.grouped_mlp_bwd_timed.argtypes = L.grouped_mlp_bwd.argtypes + [P]
+            L.grouped_mlp_fwd_tokens_train.restype = i32
+            L.grouped_mlp_fwd_tokens_train.argtypes = [P, i64, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P,
+                                                       sz, P]
+            L.grouped_mlp_bwd_tokens.restype = i32
+            L.grouped_mlp_bwd_tokens.argtypes = [P, i64, P, i64, i64, i64, i32, P, P, P, sz, P, P, P, P, P, P, P, P,
+                                                 P, P, sz, P]
             L.mxfp8_quantize_colwise_t.restype = i32
             L.mxfp8_quantize_colwise_t.argtypes = [P, i64, i64, i32, P, P, P]
             L.grouped_mlp_fwd_noalloc.restype = i32
@@ -297,6 +304,53 @@ def grouped_mlp_bwd(x_sorted, split_sizes, gates, saved, w1t_q, w1t_sf, w2t_q, w
             raise ValueError("stage_events: 7 CUDA events that have been recorded at least once")
         _check(lib().grouped_mlp_bwd_timed(*args, (ctypes.c_void_p * 7)(*handles)), "grouped_mlp_bwd_timed")
     return dx, dgates, dw1, dw2, workspace
+
+
+def grouped_mlp_fwd_tokens_train(x_tokens, token_of_row, split_sizes, gates_sorted, w1_q, w1_sf, w2_q, w2_sf,
+                                 y=None, saved=None, workspace=None, stream=None):
+    """grouped_mlp_fwd_tokens that also saves the pre-activations.  Returns (y_rows, saved)."""
+    import torch
+    T, H = x_tokens.shape
+    R = int(token_of_row.numel())
+    E = int(split_sizes.numel())
+    F = int(w2_q.shape[1])
+    dev = x_tokens.device
+    if y is None:
+        y = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    if saved is None:
+        saved = torch.empty(grouped_mlp_saved_bytes(R, H, F, E), dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = torch.empty(grouped_mlp_workspace_size(R, H, F, E), dtype=torch.uint8, device=dev)
+    st = lib().grouped_mlp_fwd_tokens_train(_ptr(x_tokens), T, _ptr(token_of_row), R, H, F, E, _ptr(split_sizes),
+                                            _ptr(gates_sorted), _ptr(w1_q), _ptr(w1_sf), _ptr(w2_q), _ptr(w2_sf),
+                                            _ptr(y), _ptr(saved), saved.numel(), _ptr(workspace), workspace.numel(),
+                                            _stream(stream))
+    _check(st, "grouped_mlp_fwd_tokens_train")
+    return y, saved
+
+
+def grouped_mlp_bwd_tokens(x_tokens, token_of_row, split_sizes, gates_sorted, saved, w1t_q, w1t_sf, w2t_q, w2t_sf,
+                           d_out_tokens, workspace=None, stream=None):
+    """grouped_mlp_bwd reading x and the output gradient as token rows through token_of_row.
+    Returns (dx_rows bf16 [R, H], dgates_sorted float32 [R] or None, dW1, dW2, workspace)."""
+    import torch
+    T, H = x_tokens.shape
+    R = int(token_of_row.numel())
+    E = int(split_sizes.numel())
+    F = int(w2t_q.shape[0])
+    dev = x_tokens.device
+    dx = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    dg = torch.empty(R, dtype=torch.float32, device=dev) if gates_sorted is not None else None
+    dw1 = torch.empty((E, 2 * F, H), dtype=torch.float32, device=dev)
+    dw2 = torch.empty((E, H, F), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(grouped_mlp_bwd_workspace_size(R, H, F, E), dtype=torch.uint8, device=dev)
+    st = lib().grouped_mlp_bwd_tokens(_ptr(x_tokens), T, _ptr(token_of_row), R, H, F, E, _ptr(split_sizes),
+                                      _ptr(gates_sorted), _ptr(saved), saved.numel(), _ptr(w1t_q), _ptr(w1t_sf),
+                                      _ptr(w2t_q), _ptr(w2t_sf), _ptr(d_out_tokens), _ptr(dx), _ptr(dg), _ptr(dw1),
+                                      _ptr(dw2), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "grouped_mlp_bwd_tokens")
+    return dx, dg, dw1, dw2, workspace
 
 
 def grouped_mlp_fwd_noalloc(x_sorted, split_sizes, gates, w1_q, w1_sf, w2_q, w2_sf, y, stream=None):

@@ -207,8 +207,9 @@ static int grouped_mlp_bwd_impl(const void* x_sorted, int64_t R, int64_t H, int6
                                 size_t saved_bytes, const uint8_t* w1t_q, const uint8_t* w1t_sf,
                                 const uint8_t* w2t_q, const uint8_t* w2t_sf, const void* dy, void* dx, float* dgates,
                                 float* dw1, float* dw2, void* workspace, size_t workspace_bytes, void* stream,
-                                void* const* events) {
-  if (R < 0 || E < 1 || E > 1024 || H <= 0 || F <= 0) return MXFP8_ERR_INVALID_ARG;
+                                void* const* events, const int32_t* token_of_row = nullptr, int64_t x_rows = 0) {
+  if (R < 0 || E < 1 || E > 1024 || H <= 0 || F <= 0 || x_rows < 0) return MXFP8_ERR_INVALID_ARG;
+  if (token_of_row != nullptr && !aligned16(token_of_row)) return MXFP8_ERR_INVALID_ARG;
   if (H % 256 != 0 || F % 256 != 0) return MXFP8_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(E) * 2 * F > INT32_MAX || static_cast<int64_t>(E) * H > INT32_MAX)
     return MXFP8_ERR_UNSUPPORTED;
@@ -223,7 +224,7 @@ static int grouped_mlp_bwd_impl(const void* x_sorted, int64_t R, int64_t H, int6
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total) return MXFP8_ERR_WORKSPACE;
   return launch_grouped_mlp_bwd(x_sorted, R, H, F, E, split_sizes, gates, static_cast<const uint16_t*>(saved),
                                 w1t_q, w1t_sf, w2t_q, w2t_sf, dy, dx, dgates, dw1, dw2, workspace, L,
-                                static_cast<cudaStream_t>(stream), events);
+                                static_cast<cudaStream_t>(stream), events, token_of_row, x_rows);
 }
 
 int grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
@@ -242,6 +243,27 @@ int grouped_mlp_bwd_timed(const void* x_sorted, int64_t R, int64_t H, int64_t F,
   if (stage_events == nullptr) return MXFP8_ERR_INVALID_ARG;
   return grouped_mlp_bwd_impl(x_sorted, R, H, F, E, split_sizes, gates, saved, saved_bytes, w1t_q, w1t_sf, w2t_q,
                               w2t_sf, dy, dx, dgates, dw1, dw2, workspace, workspace_bytes, stream, stage_events);
+}
+
+int grouped_mlp_fwd_tokens_train(const void* x_tokens, int64_t T, const int32_t* token_of_row, int64_t R,
+                                 int64_t H, int64_t F, int E, const int32_t* split_sizes, const float* gates_sorted,
+                                 const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q, const uint8_t* w2_sf,
+                                 void* y_rows, void* saved, size_t saved_bytes, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (T < 0 || token_of_row == nullptr || !aligned16(token_of_row) || saved == nullptr) return MXFP8_ERR_INVALID_ARG;
+  return grouped_mlp_fwd_impl(x_tokens, R, H, F, E, split_sizes, gates_sorted, w1_q, w1_sf, w2_q, w2_sf, y_rows,
+                              workspace, workspace_bytes, stream, nullptr, token_of_row, T, saved, saved_bytes);
+}
+
+int grouped_mlp_bwd_tokens(const void* x_tokens, int64_t T, const int32_t* token_of_row, int64_t R, int64_t H,
+                           int64_t F, int E, const int32_t* split_sizes, const float* gates_sorted, const void* saved,
+                           size_t saved_bytes, const uint8_t* w1t_q, const uint8_t* w1t_sf, const uint8_t* w2t_q,
+                           const uint8_t* w2t_sf, const void* d_out_tokens, void* dx_rows, float* dgates_sorted,
+                           float* dw1, float* dw2, void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || token_of_row == nullptr) return MXFP8_ERR_INVALID_ARG;
+  return grouped_mlp_bwd_impl(x_tokens, R, H, F, E, split_sizes, gates_sorted, saved, saved_bytes, w1t_q, w1t_sf,
+                              w2t_q, w2t_sf, d_out_tokens, dx_rows, dgates_sorted, dw1, dw2, workspace,
+                              workspace_bytes, stream, nullptr, token_of_row, T);
 }
 
 int mxfp8_quantize_colwise_t(const void* x, int64_t M, int64_t K, int sf_layout, uint8_t* q_t, uint8_t* sf_t,

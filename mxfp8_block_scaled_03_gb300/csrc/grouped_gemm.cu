@@ -1393,7 +1393,7 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
                            const float* gates, const uint16_t* saved_gu, const uint8_t* w1t_q, const uint8_t* w1t_sf,
                            const uint8_t* w2t_q, const uint8_t* w2t_sf, const void* dy, void* dx, float* dgates,
                            float* dw1, float* dw2, void* workspace, const BwdWsLayout& L, cudaStream_t stream,
-                           void* const* events) {
+                           void* const* events, const int32_t* token_of_row, int64_t x_rows) {
   DeviceInfo* dev = nullptr;
   if (!device_setup(&dev)) return MXFP8_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1413,10 +1413,15 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   // 0: schedule and the quantizations of dy and x
   if (!mark(0)) return MXFP8_ERR_CUDA;
   if (launch_schedule(split, E, R, meta, stream) != cudaSuccess) return MXFP8_ERR_CUDA;
-  if (launch_quantize_gather(dy, R, H, meta, E, rp, nullptr, 0, ws + L.dyq, ws + L.dysf, stream) != cudaSuccess)
+  // with token_of_row, x and dy are token rows ([x_rows, H]): sorted row r reads token
+  // token_of_row[r] (the gradient of the combine is this same gather of the output gradient)
+  if (launch_quantize_gather(dy, R, H, meta, E, rp, token_of_row, x_rows, ws + L.dyq, ws + L.dysf, stream) !=
+      cudaSuccess)
     return MXFP8_ERR_CUDA;
-  if (launch_quantize_t(dy, R, H, rp, true, ws + L.dyT, ws + L.dyTsf, meta, E, nullptr, 0, stream) != cudaSuccess ||
-      launch_quantize_t(x_sorted, R, H, rp, true, ws + L.xT, ws + L.xTsf, meta, E, nullptr, 0, stream) != cudaSuccess)
+  if (launch_quantize_t(dy, R, H, rp, true, ws + L.dyT, ws + L.dyTsf, meta, E, token_of_row, x_rows, stream) !=
+          cudaSuccess ||
+      launch_quantize_t(x_sorted, R, H, rp, true, ws + L.xT, ws + L.xTsf, meta, E, token_of_row, x_rows, stream) !=
+          cudaSuccess)
     return MXFP8_ERR_CUDA;
   if (!mark(1)) return MXFP8_ERR_CUDA;
 

@@ -99,6 +99,6 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
                            const float* gates, const uint16_t* saved_gu, const uint8_t* w1t_q, const uint8_t* w1t_sf,
                            const uint8_t* w2t_q, const uint8_t* w2t_sf, const void* dy, void* dx, float* dgates,
                            float* dw1, float* dw2, void* workspace, const BwdWsLayout& L, cudaStream_t stream,
-                           void* const* events);
+                           void* const* events, const int32_t* token_of_row = nullptr, int64_t x_rows = 0);
 
 }  // namespace mx

@@ -182,3 +182,44 @@ def test_gather_reports_bad_token(mx):
     mx.grouped_mlp_fwd_tokens(x, G.to_dev(np.arange(64, dtype=np.int32)), G.to_dev(w.split_sizes), None,
                               *_weights(mx, w), workspace=ws)
     assert mx.mxfp8_check_device_error(ws) == (0, 0)
+
+
+def test_tiny_layer_backward_through_tokens(mx, oracle):
+    """The MoE layer in training on the device: permute -> token forward (pre-activations saved)
+    -> combine; backward from a token-space output gradient: the token backward (the combine's
+    gradient gathers d_out rows by token) -> moe_combine of dx rows (the gather's gradient).
+    Checked against the oracle's backward on the sorted rows, combined by the oracle."""
+    import torch
+    w = W.moe_workload("tiny")
+    x = G.to_dev_bf16(w.x_tokens)
+    split, ros, tor, gs, _ = mx.moe_permute(G.to_dev(w.topk_experts), G.to_dev(w.topk_gates), w.E)
+    w1, w2 = G.to_dev_bf16(w.w1), G.to_dev_bf16(w.w2)
+    w1q, w1s, _, _ = mx.mxfp8_quantize(w1, sf_layout=mx.SF_MMA)
+    w2q, w2s, _, _ = mx.mxfp8_quantize(w2, sf_layout=mx.SF_MMA)
+    w1tq, w1ts = mx.mxfp8_quantize_colwise_t(w1)
+    w2tq, w2ts = mx.mxfp8_quantize_colwise_t(w2)
+    y_rows, saved = mx.grouped_mlp_fwd_tokens_train(x, tor, split, gs, w1q, w1s, w2q, w2s)
+    rng = np.random.default_rng(31)
+    d_out = W.bf16_bits(rng.standard_normal((w.T, w.H)).astype(np.float32))
+    dx_rows, dg, dw1, dw2, ws = mx.grouped_mlp_bwd_tokens(x, tor, split, gs, saved, w1tq, w1ts, w2tq, w2ts,
+                                                          G.to_dev_bf16(d_out))
+    assert mx.mxfp8_check_device_error(ws) == (0, 0)
+    dx_tok = mx.moe_combine(dx_rows, ros)
+    ros_h = _np(ros)
+    # oracle: the same rows through the pre-sorted backward, the output gradient gathered by token
+    dy_rows = d_out[w.token_of_row]
+    o1q, o1s = oracle.quantize_rowwise(w.w1)
+    o2tq, o2ts = oracle.quantize_transposed(w.w2, w.E)
+    o1tq, o1ts = oracle.quantize_transposed(w.w1, w.E)
+    rdx, rdg, _, _ = oracle.grouped_mlp_bwd_rows(w.x_sorted, w.split_sizes, w.gates, o1q, o1s, o2tq, o2ts, o1tq,
+                                                 o1ts, dy_rows, np.arange(w.R))
+    rdx_tok = oracle.moe_combine(rdx, ros_h)
+    got = W.bf16_to_f32(_np(dx_tok.view(torch.int16)).view(np.uint16)).astype(np.float64)
+    rel, mxe = G.y_errors(got, rdx_tok)
+    assert rel <= G.Y_REL_TOL and mxe <= G.Y_MAX_TOL, f"dx tokens rel {rel:.3e} max {mxe:.3e}"
+    rel, mxe = G.y_errors(_np(dg).astype(np.float64)[ros_h], rdg[ros_h])
+    assert rel <= G.Y_REL_TOL and mxe <= G.Y_MAX_TOL, f"d gates rel {rel:.3e} max {mxe:.3e}"
+    ent = np.array([[0, 0, 0], [1, 100, 300], [2, 255, 511], [3, 17, 5]])
+    ref = oracle.grouped_mlp_bwd_dw(w.x_sorted, w.split_sizes, w.gates, o1q, o1s, o2tq, o2ts, dy_rows, 2, ent)
+    got = _np(dw2)[ent[:, 0], ent[:, 1], ent[:, 2]]
+    assert np.allclose(got, ref, rtol=1e-2, atol=1e-3 * np.abs(ref).max())
