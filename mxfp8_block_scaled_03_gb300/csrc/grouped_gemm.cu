@@ -301,6 +301,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
         gw2[1] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, f0 + c0 + 8, 2 * F)));
         uw2[0] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + f0 + c0, 2 * F)));
         uw2[1] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + f0 + c0 + 8, 2 * F)));
+        uint4 odg[2], odu[2], oh[2];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
         const int c = c0 + 8 * hh;
@@ -321,25 +322,24 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
           hv[i] = gate * sl * u[i];
           part += dh * sl * u[i];
         }
-        uint4 o;
-        o = make_uint4(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]), pack_bf16x2(dg[4], dg[5]),
-                       pack_bf16x2(dg[6], dg[7]));
-        __stcs(reinterpret_cast<uint4*>(dg_row + c), o);
-        o = make_uint4(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]), pack_bf16x2(du[4], du[5]),
-                       pack_bf16x2(du[6], du[7]));
-        __stcs(reinterpret_cast<uint4*>(dg_row + F + c), o);
-        o = make_uint4(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]), pack_bf16x2(hv[4], hv[5]),
-                       pack_bf16x2(hv[6], hv[7]));
-        __stcs(reinterpret_cast<uint4*>(h_row + c), o);
+        odg[hh] = make_uint4(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]), pack_bf16x2(dg[4], dg[5]),
+                             pack_bf16x2(dg[6], dg[7]));
+        odu[hh] = make_uint4(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]), pack_bf16x2(du[4], du[5]),
+                             pack_bf16x2(du[6], du[7]));
+        oh[hh] = make_uint4(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]), pack_bf16x2(hv[4], hv[5]),
+                            pack_bf16x2(hv[6], hv[7]));
         }
+        st_global_32B_cs(dg_row + c0, odg[0], odg[1]);
+        st_global_32B_cs(dg_row + F + c0, odu[0], odu[1]);
+        st_global_32B_cs(h_row + c0, oh[0], oh[1]);
       }
     } else {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 4
-      for (int c = 0; c < 128; c += 8) {
-        *reinterpret_cast<uint4*>(dg_row + c) = z;
-        *reinterpret_cast<uint4*>(dg_row + F + c) = z;
-        *reinterpret_cast<uint4*>(h_row + c) = z;
+      for (int c = 0; c < 128; c += 16) {
+        st_global_32B_cs(dg_row + c, z, z);
+        st_global_32B_cs(dg_row + F + c, z, z);
+        st_global_32B_cs(h_row + c, z, z);
       }
     }
     p.dgate_part[prow * (F / 128) + f0 / 128] = part;
@@ -347,22 +347,26 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     // v = 128 fp32 gradient entries of row a_row + r, columns n*256 + 128*half ..
     float* drow = p.dw + (static_cast<int64_t>(t.e) * p.wg_m + t.a_row + r) * p.wg_n + t.n * 256 + 128 * half;
 #pragma unroll
-    for (int c = 0; c < 128; c += 4)
-      *reinterpret_cast<float4*>(drow + c) = make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                                                         __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+    for (int c = 0; c < 128; c += 8)
+      st_global_32B_cs(drow + c, make_uint4(v[c], v[c + 1], v[c + 2], v[c + 3]),
+                       make_uint4(v[c + 4], v[c + 5], v[c + 6], v[c + 7]));
   } else {
     if (r < t.valid) {
       const int ncols = BN / 2;
       uint16_t* yrow = p.y + static_cast<int64_t>(t.src_row0 + r) * p.ldy + t.n * BN + ncols * half;
 #pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-        if (c < ncols) {
-          uint4 o;
-          o.x = pack_bf16x2(__uint_as_float(v[c + 0]), __uint_as_float(v[c + 1]));
-          o.y = pack_bf16x2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-          o.z = pack_bf16x2(__uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
-          o.w = pack_bf16x2(__uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
-          *reinterpret_cast<uint4*>(yrow + c) = o;
+      for (int c = 0; c < 128; c += 16) {
+        if (c < ncols) {   // 16 columns = one 32-byte store
+          uint4 o[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int cc = c + 8 * k;
+            o[k].x = pack_bf16x2(__uint_as_float(v[cc + 0]), __uint_as_float(v[cc + 1]));
+            o[k].y = pack_bf16x2(__uint_as_float(v[cc + 2]), __uint_as_float(v[cc + 3]));
+            o[k].z = pack_bf16x2(__uint_as_float(v[cc + 4]), __uint_as_float(v[cc + 5]));
+            o[k].w = pack_bf16x2(__uint_as_float(v[cc + 6]), __uint_as_float(v[cc + 7]));
+          }
+          st_global_32B(yrow + c, o[0], o[1]);
         }
       }
     }
@@ -1038,7 +1042,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       decode_pair_tile<MODE>(u, static_cast<int>(rank), p, t);
       if (MODE == GEMM_WGRAD && t.steps == 0) {   // expert without rows: its gradient block is zero
         float* drow = p.dw + (static_cast<int64_t>(t.e) * p.wg_m + t.a_row + r) * p.wg_n + t.n * 256 + 128 * half;
-        for (int c = 0; c < 128; c += 4) *reinterpret_cast<float4*>(drow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < 128; c += 8) st_global_32B_cs(drow + c, make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u));
         continue;
       }
       bool got = true;

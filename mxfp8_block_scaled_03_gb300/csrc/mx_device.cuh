@@ -234,6 +234,19 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// 32-byte global stores (one full sector per lane); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_32B(void* p, uint4 a, uint4 b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+// Same, marked streaming (evict first): for outputs no later kernel of the call reads soon.
+__device__ __forceinline__ void st_global_32B_cs(void* p, uint4 a, uint4 b) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
 // ------------------------------------------------------------------------------------------
 // Thread-block clusters and the CTA pair (cta_group::2)
 // ------------------------------------------------------------------------------------------
