@@ -1414,16 +1414,13 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
       !make_map(&mDguT, ws + L.dguT, 2 * F, rp) || !make_map(&mXT, ws + L.xT, H, rp))
     return MXFP8_ERR_CUDA;
 
-  // 0: schedule and the quantizations of dy and x
+  // 0: schedule and the quantizations of dy (row-wise and column-wise in one pass) and x
   if (!mark(0)) return MXFP8_ERR_CUDA;
   if (launch_schedule(split, E, R, meta, stream) != cudaSuccess) return MXFP8_ERR_CUDA;
   // with token_of_row, x and dy are token rows ([x_rows, H]): sorted row r reads token
   // token_of_row[r] (the gradient of the combine is this same gather of the output gradient)
-  if (launch_quantize_gather(dy, R, H, meta, E, rp, token_of_row, x_rows, ws + L.dyq, ws + L.dysf, stream) !=
-      cudaSuccess)
-    return MXFP8_ERR_CUDA;
-  if (launch_quantize_t(dy, R, H, rp, true, ws + L.dyT, ws + L.dyTsf, meta, E, token_of_row, x_rows, stream) !=
-          cudaSuccess ||
+  if (launch_quantize_t(dy, R, H, rp, true, ws + L.dyT, ws + L.dyTsf, meta, E, token_of_row, x_rows, stream,
+                        ws + L.dyq, ws + L.dysf) != cudaSuccess ||
       launch_quantize_t(x_sorted, R, H, rp, true, ws + L.xT, ws + L.xTsf, meta, E, token_of_row, x_rows, stream) !=
           cudaSuccess)
     return MXFP8_ERR_CUDA;
@@ -1459,11 +1456,10 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   if ((st = run_pair<GEMM_DGRAD>(dev, pairs * pd.NT, mDy, mW2t, pd, stream)) != MXFP8_OK) return st;
   if (!mark(2)) return MXFP8_ERR_CUDA;
 
-  // 2: quantizations of dGU (row-wise for dx, column-wise for dW1) and of h (column-wise for dW2)
-  if (launch_quantize(ws + L.dgu, rp, 2 * F, MXFP8_ROWWISE, MXFP8_SF_MMA, ws + L.dguq, ws + L.dgusf, nullptr,
-                      nullptr, stream) != cudaSuccess ||
-      launch_quantize_t(ws + L.dgu, rp, 2 * F, rp, true, ws + L.dguT, ws + L.dguTsf, nullptr, E, nullptr, 0,
-                        stream) != cudaSuccess ||
+  // 2: quantizations of dGU (row-wise for dx and column-wise for dW1, one pass) and of h (column-wise
+  //    for dW2)
+  if (launch_quantize_t(ws + L.dgu, rp, 2 * F, rp, true, ws + L.dguT, ws + L.dguTsf, nullptr, E, nullptr, 0,
+                        stream, ws + L.dguq, ws + L.dgusf) != cudaSuccess ||
       launch_quantize_t(ws + L.hb, rp, F, rp, true, ws + L.hT, ws + L.hTsf, nullptr, E, nullptr, 0, stream) !=
           cudaSuccess)
     return MXFP8_ERR_CUDA;

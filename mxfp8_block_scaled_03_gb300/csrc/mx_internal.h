@@ -68,9 +68,12 @@ cudaError_t launch_quantize_gather(const void* x, int64_t R, int64_t H, const Sc
 // bytes in the tensor-core layout of [K, m_out] (mma) or compact [K, m_out/32].  With meta, the
 // m_out rows are the expert-padded row space gathered from the sorted rows of x (through
 // token_of_row when given; then x has x_rows rows).
+// q_row / sf_row (optional, K % 128 == 0): also the row-wise MXFP8 of the same rows, scale bytes
+// in the tensor-core layout, from the same read of x.
 cudaError_t launch_quantize_t(const void* x, int64_t M, int64_t K, int64_t m_out, bool mma, uint8_t* qT,
                               uint8_t* sfT, const SchedHeader* meta, int E, const int32_t* token_of_row,
-                              int64_t x_rows, cudaStream_t stream);
+                              int64_t x_rows, cudaStream_t stream, uint8_t* q_row = nullptr,
+                              uint8_t* sf_row = nullptr);
 
 // Dispatch and combine around the grouped MLP (moe_routing.cu).
 size_t permute_workspace_bytes(int64_t n, int E);

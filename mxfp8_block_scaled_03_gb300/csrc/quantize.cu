@@ -219,7 +219,9 @@ __global__ void __launch_bounds__(QT_THREADS, (ROW && COL) || GATHER ? 3 : 4) k_
 // One CTA of 256 threads owns 128 source rows x 64 source columns: the tile is read with 128-bit
 // loads into shared memory (16 KB), then thread t takes column t % 64 and 32-row block t / 64,
 // reads its 32 values down the column (a warp reads 32 adjacent columns of one row: no bank
-// conflicts), and writes its 32 codes as two 16-byte stores.
+// conflicts), and writes its 32 codes as two 16-byte stores.  ROW: the same tile also yields the
+// row-wise MXFP8 of those rows (thread t: row t / 2, 32-column block t % 2; tensor-core scale
+// layout), so a tensor needed in both directions is read from memory once.
 constexpr int QTT_ROWS = 128;
 constexpr int QTT_COLS = 64;
 
@@ -230,12 +232,14 @@ struct QuantTArgs {
   uint8_t* qT;
   uint8_t* sfT;
   bool mma;
+  uint8_t* q_row;           // ROW: codes [m_out, K] (row-major, rows of the tile's row space)
+  uint8_t* sf_row;          // ROW: scale bytes, tensor-core layout of [m_out, K]
   const SchedHeader* meta;  // gather mode only
   int E;
   const int32_t* tok;
 };
 
-template <bool GATHER>
+template <bool GATHER, bool ROW>
 __global__ void __launch_bounds__(256) k_quantize_t(const QuantTArgs a) {
   __shared__ __align__(16) uint16_t tile[QTT_ROWS][QTT_COLS + 8];
   const int tid = threadIdx.x;
@@ -281,6 +285,32 @@ __global__ void __launch_bounds__(256) k_quantize_t(const QuantTArgs a) {
     *reinterpret_cast<uint4*>(&tile[rr][ch * 8]) = w;
   }
   __syncthreads();
+  if constexpr (ROW) {
+    const int rr = tid >> 1, cb = tid & 1;
+    float v[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 w = *reinterpret_cast<const uint4*>(&tile[rr][cb * 32 + 8 * j]);
+      const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                          bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[8 * j + i] = f[i];
+        amax = fmaxf(amax, fabsf(f[i]));
+      }
+    }
+    const int64_t rcol = col0 + cb * 32;
+    if (rcol < a.K) {
+      const uint32_t sfb = e8m0_from_amax(amax);
+      const float inv = e8m0_inverse_scale(sfb);
+      const uint2 q0 = quant8(v + 0, inv), q1 = quant8(v + 8, inv), q2 = quant8(v + 16, inv), q3 = quant8(v + 24, inv);
+      uint8_t* dst = a.q_row + (row0 + rr) * a.K + rcol;
+      reinterpret_cast<uint4*>(dst)[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
+      reinterpret_cast<uint4*>(dst)[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
+      a.sf_row[sf_mma_offset(row0 + rr, rcol >> 5, a.K / 128)] = static_cast<uint8_t>(sfb);
+    }
+  }
   const int c = tid % QTT_COLS;
   const int rb = tid / QTT_COLS;   // 32-row block inside the tile
   const int64_t col = col0 + c;
@@ -354,7 +384,7 @@ cudaError_t launch_quantize_gather(const void* x, int64_t R, int64_t H, const Sc
 
 cudaError_t launch_quantize_t(const void* x, int64_t M, int64_t K, int64_t m_out, bool mma, uint8_t* qT,
                               uint8_t* sfT, const SchedHeader* meta, int E, const int32_t* token_of_row,
-                              int64_t x_rows, cudaStream_t stream) {
+                              int64_t x_rows, cudaStream_t stream, uint8_t* q_row, uint8_t* sf_row) {
   QuantTArgs a{};
   a.x = static_cast<const uint16_t*>(x);
   a.M = meta ? (token_of_row ? x_rows : M) : M;
@@ -368,10 +398,20 @@ cudaError_t launch_quantize_t(const void* x, int64_t M, int64_t K, int64_t m_out
   a.tok = token_of_row;
   const dim3 grid(static_cast<unsigned>((m_out + QTT_ROWS - 1) / QTT_ROWS),
                   static_cast<unsigned>((K + QTT_COLS - 1) / QTT_COLS));
-  if (meta)
-    k_quantize_t<true><<<grid, 256, 0, stream>>>(a);
-  else
-    k_quantize_t<false><<<grid, 256, 0, stream>>>(a);
+  a.q_row = q_row;
+  a.sf_row = sf_row;
+  const bool row = q_row != nullptr;
+  if (meta) {
+    if (row)
+      k_quantize_t<true, true><<<grid, 256, 0, stream>>>(a);
+    else
+      k_quantize_t<true, false><<<grid, 256, 0, stream>>>(a);
+  } else {
+    if (row)
+      k_quantize_t<false, true><<<grid, 256, 0, stream>>>(a);
+    else
+      k_quantize_t<false, false><<<grid, 256, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
