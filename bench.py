@@ -323,7 +323,7 @@ def run_native(args, world, rank, local):
     g1_flops = 4.0 * R * H * F
     g1_tflops = g1_flops / (kern_ms["grouped_linear1_swiglu_requant"] * 1e-3) / 1e12
     g2_tflops = 2.0 * R * H * F / (kern_ms["grouped_linear2"] * 1e-3) / 1e12
-    roofline = {"kernel": "k_grouped_gemm<GEMM_SWIGLU> (GroupedLinear 1 + ScaledSwiGLU + requant)",
+    roofline = {"kernel": "k_grouped_gemm_pair<GEMM_SWIGLU> (GroupedLinear 1 + ScaledSwiGLU + requant)",
                 "bound": "tensor", "achieved": g1_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": g1_tflops / fp8_peak,
                 "peak_source": f"{peak_src} bf16_tflops {peaks['bf16_tflops']:.1f} x {FP8_OVER_BF16:.0f} "
