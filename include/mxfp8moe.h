@@ -225,7 +225,7 @@ int grouped_mlp_fwd_noalloc(const void* x_sorted, int64_t R, int64_t H, int64_t 
  *   dx           bf16 [R, H] out.   dgates  float [R] out, or NULL to skip.
  *   dw1          float [E, 2F, H] out (gradient of W1).   dw2  float [E, H, F] out.
  *   workspace    grouped_mlp_bwd_workspace_size(R, H, F, E) bytes, 256-byte aligned.
- * Requirements: H % 256 == 0, F % 256 == 0 (all backward GEMMs run on CTA pairs with 256-wide
+ * Requirements: H % 256 == 0, F % 128 == 0 (all backward GEMMs run on CTA pairs with 256-wide
  * tiles; MXFP8_ERR_UNSUPPORTED otherwise), 1 <= E <= 1024.  Outputs are fully overwritten (an
  * expert without rows gets zero weight gradients).  Split errors and timeouts are reported in
  * the workspace error word as for the forward.

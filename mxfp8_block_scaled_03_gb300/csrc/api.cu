@@ -210,7 +210,7 @@ static int grouped_mlp_bwd_impl(const void* x_sorted, int64_t R, int64_t H, int6
                                 void* const* events, const int32_t* token_of_row = nullptr, int64_t x_rows = 0) {
   if (R < 0 || E < 1 || E > 1024 || H <= 0 || F <= 0 || x_rows < 0) return MXFP8_ERR_INVALID_ARG;
   if (token_of_row != nullptr && !aligned16(token_of_row)) return MXFP8_ERR_INVALID_ARG;
-  if (H % 256 != 0 || F % 256 != 0) return MXFP8_ERR_UNSUPPORTED;
+  if (H % 256 != 0 || F % 128 != 0) return MXFP8_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(E) * 2 * F > INT32_MAX || static_cast<int64_t>(E) * H > INT32_MAX)
     return MXFP8_ERR_UNSUPPORTED;
   const void* ptrs[] = {x_sorted, split_sizes, saved, w1t_q, w1t_sf, w2t_q, w2t_sf, dy, dx, dw1, dw2, workspace};

@@ -1,24 +1,32 @@
-// grouped_gemm.cu -- the fused MXFP8 grouped expert MLP forward on sm_103a.
+// grouped_gemm.cu -- the fused MXFP8 grouped expert MLP on sm_103a: forward and backward GEMMs.
 //
 // Operation (page "Efficient MoE training for biological foundation models", Key technical
 // approaches): GroupedLinear over per-expert row counts split_sizes (item 1), MXFP8 operands
 // with one E8M0 scale per 32 values along K (item 2), and the fused
 // GroupedLinear -> ScaledSwiGLU -> GroupedLinear forward in which the SwiGLU activation and the
 // routing-weight multiply run inside the first GEMM and the intermediate is requantized to MXFP8
-// there, so it never exists in 16-bit memory (item 3).
+// there, so it never exists in 16-bit memory (item 3), with its corresponding backward.
 //
-// Device pipeline of one call (one stream, no host synchronization):
-//   1. k_schedule    split_sizes -> prefix sums, expert-padded row offsets, 128-row tile counts,
-//                    sum check (error word on mismatch).
+// Forward pipeline of one call (one stream, no host synchronization):
+//   1. k_schedule    split_sizes -> prefix sums, expert-padded row offsets (every expert padded to
+//                    a multiple of 256 rows), tile counts, sum check (error word on mismatch).
 //   2. k_quantize    x_sorted -> x_q (E4M3) + scale bytes in the tensor-core layout, rows moved
-//                    into an expert-padded row space so every 128-row tile belongs to one expert.
-//   3. k_grouped_gemm<GEMM_SWIGLU>  per tile (expert e, 128 rows, 128 columns of F):
+//                    into the expert-padded row space so every 256-row tile pair is one expert's.
+//   3. k_grouped_gemm_pair<GEMM_SWIGLU>  per pair tile (expert e, 256 rows, 128 columns of F):
 //                    [G | U] = x_q W1[e, {gate, up} rows]^T accumulated in TMEM, then
-//                    h = gate * silu(G) * U, requantized to h_q + scale bytes.
-//   4. k_grouped_gemm<GEMM_OUT>     per tile (expert e, 128 rows, BN columns of H):
+//                    h = gate * silu(G) * U, requantized to h_q + scale bytes (and, in a training
+//                    forward, [G | U] saved as bf16).
+//   4. k_grouped_gemm_pair<GEMM_OUT>     per pair tile (expert e, 256 rows, 256 columns of H):
 //                    y = h_q W2[e]^T -> bf16, stored only for the expert's real rows.
+// Backward (launch_grouped_mlp_bwd): GEMM_DGRAD (dh = dy W2 with the ScaledSwiGLU backward in the
+// epilogue), GEMM_OUT (dx = dGU W1), GEMM_WGRAD (dW2, dW1 over each expert's rows).
 //
-// GEMM kernel structure (persistent, one 512-thread CTA per SM, 4-stage shared-memory ring):
+// Main kernel (k_grouped_gemm_pair, persistent clusters of two CTAs on two SMs, 512 threads each):
+// one tcgen05.mma.cta_group::2 computes a 256 x 256 tile, each CTA loading its own 128 rows of A
+// and half of B (32 KB per K step), 6-stage data ring, 16-slot scale ring running ahead of it;
+// roles and synchronization are described above the kernel.  k_grouped_gemm is the single-CTA
+// kernel (M=128, 4 stages of 48 KB): GroupedLinear 2 uses it when H % 256 != 0, and both forward
+// GEMMs use it where no CTA pair can be co-scheduled.  Its structure:
 //   TMA producer  A tile (128 rows x 128 K bytes), B tile (BN rows x 128) and the 512-byte scale
 //                 atoms of both, all completing on one mbarrier per stage.
 //   scale warps   four warps copy the stage's scale atoms into TMEM with tcgen05.st (one TMEM lane
@@ -125,6 +133,9 @@ struct GemmParams {
   // GEMM_WGRAD
   int wg_mt, wg_nt;        // 256-row tiles of A's rows (M / 256) and of B's rows (N / 256)
   int wg_m_fastest;        // 1: A tiles run fastest inside an expert (keeps the smaller A block in L2)
+  int b_rows;              // rows of B when its last 256-row tile may be half past the end (GEMM_DGRAD,
+                           // GEMM_WGRAD with N % 256 == 128): that half reads zeros and is not stored;
+                           // 0 when every tile is whole
   int64_t wg_m, wg_n;      // rows and columns of each expert's gradient block
   float* dw;               // [E, M, N] fp32
 };
@@ -287,6 +298,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     const int64_t F = p.ldh;
     const int64_t prow = t.pad_row0 + r;
     const int f0 = t.n * 256 + 128 * half;
+    if (f0 >= F) return;   // the half of the last column tile that lies past F
     uint16_t* dg_row = p.dgu + prow * 2 * F + f0;
     uint16_t* h_row = p.hb + prow * F + f0;
     float part = 0.0f;
@@ -345,6 +357,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     p.dgate_part[prow * (F / 128) + f0 / 128] = part;
   } else if (MODE == GEMM_WGRAD) {
     // v = 128 fp32 gradient entries of row a_row + r, columns n*256 + 128*half ..
+    if (t.n * 256 + 128 * half >= p.wg_n) return;   // half of the last column tile past N
     float* drow = p.dw + (static_cast<int64_t>(t.e) * p.wg_m + t.a_row + r) * p.wg_n + t.n * 256 + 128 * half;
 #pragma unroll
     for (int c = 0; c < 128; c += 8)
@@ -881,7 +894,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (lane < 8) {
             const int64_t prow = t.pad_row0 + 32 * (lane & 3);
             const int64_t j = (lane < 4 ? 0 : p.ldh) + t.n * 256;
-            prefetch_l2(p.gu + gu_offset(prow, j, 2 * p.ldh), 16384);
+            prefetch_l2(p.gu + gu_offset(prow, j, 2 * p.ldh), t.n * 256 + 256 <= p.ldh ? 16384 : 8192);
           }
         }
         for (int kb = 0; kb < t.steps; ++kb, ++g) {
@@ -945,7 +958,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         decode_pair_tile<MODE>(u, static_cast<int>(rank), p, t);
         const int64_t a_atom0 = static_cast<int64_t>(t.a_row / 128) * p.a_kt + t.a_k0 / BK;
         const int64_t b_atom0 = static_cast<int64_t>(t.b_row0 / 128) * p.b_kt + t.b_k0 / BK;
-        const int64_t b_atom1 = static_cast<int64_t>(t.b_row1 / 128) * p.b_kt + t.b_k0 / BK;
+        // past the end of B (half of a last tile), any valid atom will do: those B rows are zeros
+        const int b_row1 = (p.b_rows > 0 && t.b_row1 >= p.b_rows) ? t.b_row0 : t.b_row1;
+        const int64_t b_atom1 = static_cast<int64_t>(b_row1 / 128) * p.b_kt + t.b_k0 / BK;
         for (int kb = 0; kb < t.steps; ++kb, ++g) {
           const int slot = g % P_SF_SLOTS;
           const int grp = slot / P_SF_GROUP;
@@ -1041,6 +1056,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       TileInfo t;
       decode_pair_tile<MODE>(u, static_cast<int>(rank), p, t);
       if (MODE == GEMM_WGRAD && t.steps == 0) {   // expert without rows: its gradient block is zero
+        if (t.n * 256 + 128 * half >= p.wg_n) continue;
         float* drow = p.dw + (static_cast<int64_t>(t.e) * p.wg_m + t.a_row + r) * p.wg_n + t.n * 256 + 128 * half;
         for (int c = 0; c < 128; c += 8) st_global_32B_cs(drow + c, make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u));
         continue;
@@ -1440,7 +1456,8 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   pd.a_sf = ws + L.dysf;
   pd.b_sf = w2t_sf;
   pd.KT = static_cast<int>(H / BK);
-  pd.NT = static_cast<int>(F / 256);
+  pd.NT = static_cast<int>((F + 255) / 256);
+  pd.b_rows = static_cast<int>(F);
   pd.BN = 256;
   pd.b_rows_per_expert = 0;
   pd.b_kofs = static_cast<int>(H);
@@ -1495,7 +1512,8 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   pw.a_sf = ws + L.dyTsf;
   pw.b_sf = ws + L.hTsf;
   pw.wg_mt = static_cast<int>(H / 256);
-  pw.wg_nt = static_cast<int>(F / 256);
+  pw.wg_nt = static_cast<int>((F + 255) / 256);
+  pw.b_rows = static_cast<int>(F);
   pw.wg_m = H;
   pw.wg_n = F;
   pw.wg_m_fastest = 1;   // dy^T (H rows) is the smaller operand: keep it in L2, stream h^T once
@@ -1506,6 +1524,7 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   pw.b_sf = ws + L.xTsf;
   pw.wg_mt = static_cast<int>(2 * F / 256);
   pw.wg_nt = static_cast<int>(H / 256);
+  pw.b_rows = 0;
   pw.wg_m = 2 * F;
   pw.wg_n = H;
   pw.wg_m_fastest = 0;   // x^T (H rows) is the smaller operand: keep it in L2, stream dGU^T once

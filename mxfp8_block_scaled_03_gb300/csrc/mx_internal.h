@@ -96,7 +96,7 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
                        uint16_t* gu_out = nullptr);
 // gu_out (may be NULL): training forward, [G | U] saved as bf16 [r_pad, 2F] for the backward.
 
-// Backward of the grouped MLP (all GEMMs on CTA pairs; needs H % 256 == 0 and F % 256 == 0).
+// Backward of the grouped MLP (all GEMMs on CTA pairs; needs H % 256 == 0 and F % 128 == 0).
 // `events` (may be null): 7 events recorded on `stream` around its stages.
 int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
                            const float* gates, const uint16_t* saved_gu, const uint8_t* w1t_q, const uint8_t* w1t_sf,

@@ -118,6 +118,12 @@ def test_ragged_backward_with_empty_experts(mx, oracle):
     _assert_bwd_parity(mx, oracle, w, np.arange(w.R), 800, seed=3)
 
 
+def test_backward_half_last_column_tile(mx, oracle):
+    """F % 256 == 128: the last 256-wide column tile of dh and dW2 is half past the end."""
+    w = W.custom_moe([100, 0, 200, 3], H=256, F=384, seed=25)
+    _assert_bwd_parity(mx, oracle, w, np.arange(w.R), 800, seed=9)
+
+
 def test_backward_without_gates(mx, oracle):
     w = W.custom_moe([130, 126], H=512, F=256, seed=22, with_gates=False)
     _assert_bwd_parity(mx, oracle, w, np.arange(w.R), 600, seed=5)
@@ -130,6 +136,15 @@ def test_backward_deterministic(mx):
     b = _gpu_bwd(mx, w, dyb)
     for u, v in zip(a[:4], b[:4]):
         assert np.array_equal(u, v)
+
+
+def test_fine_grained_backward_sampled(mx, oracle):
+    """Full fine-grained workload (64 experts, 3 of them empty, top-8, F = 1408 = 5.5 x 256):
+    sampled rows and weight-gradient entries against the oracle, zero gradients of the empty
+    experts."""
+    w = W.moe_workload("fine")
+    rows = W.sample_rows(w.split_sizes, seed=1, first=0, last=1, rand=0, tile=1 << 30)
+    _assert_bwd_parity(mx, oracle, w, rows, 40, seed=11)
 
 
 def test_backward_rejects_unsupported_shapes(mx):
