@@ -216,14 +216,16 @@ __global__ void __launch_bounds__(QT_THREADS, (ROW && COL) || GATHER ? 3 : 4) k_
 // the [K, m_out] code matrix, or compact [K, m_out / 32].  GATHER: source rows are the
 // expert-padded row space (as in k_quantize), padding rows are zeros.
 //
-// One CTA of 256 threads owns 128 source rows x 64 source columns: the tile is read with 128-bit
-// loads into shared memory (16 KB), then thread t takes column t % 64 and 32-row block t / 64,
-// reads its 32 values down the column (a warp reads 32 adjacent columns of one row: no bank
-// conflicts), and writes its 32 codes as two 16-byte stores.  ROW: the same tile also yields the
-// row-wise MXFP8 of those rows (thread t: row t / 2, 32-column block t % 2; tensor-core scale
-// layout), so a tensor needed in both directions is read from memory once.
+// One CTA of 256 threads owns 128 source rows x 128 source columns: the tile is read with
+// 128-bit loads into shared memory (34 KB with padding), then thread t takes the column pair
+// 2 (t % 64), 2 (t % 64) + 1 and the 32-row block t / 64: it reads 32 packed bf16 pairs down the
+// columns (a warp reads 32 consecutive words of one row: no bank conflicts), takes both columns'
+// amax on the packed pairs, and writes each column's 32 codes as two 16-byte stores.  ROW: the
+// same tile also yields the row-wise MXFP8 of those rows (thread t: row t / 2, 32-column blocks
+// 2 (t % 2) and 2 (t % 2) + 1; tensor-core scale layout), so a tensor needed in both directions is
+// read from memory once.
 constexpr int QTT_ROWS = 128;
-constexpr int QTT_COLS = 64;
+constexpr int QTT_COLS = 128;
 
 struct QuantTArgs {
   const uint16_t* x;
@@ -245,7 +247,7 @@ __global__ void __launch_bounds__(256) k_quantize_t(const QuantTArgs a) {
   const int tid = threadIdx.x;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * QTT_ROWS;
   const int64_t col0 = static_cast<int64_t>(blockIdx.y) * QTT_COLS;
-  // source row of every tile row (-1: zero row)
+  // source rows of the tile: first_src .. first_src + nsrc - 1 (the rest read as zeros)
   int64_t first_src = row0;
   int64_t nsrc = a.M - row0;
   if constexpr (GATHER) {
@@ -265,11 +267,11 @@ __global__ void __launch_bounds__(256) k_quantize_t(const QuantTArgs a) {
     }
   }
   nsrc = nsrc < 0 ? 0 : (nsrc > QTT_ROWS ? QTT_ROWS : nsrc);
-  // load: 128 rows x 8 chunks of 16 bytes; thread t takes chunk t % 8 of rows t / 8 + 32 j
+  // load: 128 rows x 16 chunks of 16 bytes; thread t takes chunk t % 16 of rows t / 16 + 16 j
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int rr = tid / 8 + 32 * j;
-    const int ch = tid % 8;
+  for (int j = 0; j < 8; ++j) {
+    const int rr = tid / 16 + 16 * j;
+    const int ch = tid % 16;
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
     if (rr < nsrc) {
       int64_t src = first_src + rr;
@@ -286,53 +288,62 @@ __global__ void __launch_bounds__(256) k_quantize_t(const QuantTArgs a) {
   }
   __syncthreads();
   if constexpr (ROW) {
-    const int rr = tid >> 1, cb = tid & 1;
-    float v[32];
-    float amax = 0.0f;
+    const int rr = tid >> 1;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 w = *reinterpret_cast<const uint4*>(&tile[rr][cb * 32 + 8 * j]);
-      const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                          bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+    for (int b2 = 0; b2 < 2; ++b2) {
+      const int cb = 2 * (tid & 1) + b2;   // 32-column block inside the tile
+      const int64_t rcol = col0 + cb * 32;
+      uint4 w[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[8 * j + i] = f[i];
-        amax = fmaxf(amax, fabsf(f[i]));
+      for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint4*>(&tile[rr][cb * 32 + 8 * j]);
+      uint32_t m2 = absmax_bf16x2(absmax_bf16x2(w[0].x, w[0].y), absmax_bf16x2(w[0].z, w[0].w));
+#pragma unroll
+      for (int j = 1; j < 4; ++j)
+        m2 = absmax_bf16x2(m2, absmax_bf16x2(absmax_bf16x2(w[j].x, w[j].y), absmax_bf16x2(w[j].z, w[j].w)));
+      if (rcol < a.K) {
+        const uint32_t sfb = e8m0_from_amax(max_halves(m2));
+        const float inv = e8m0_inverse_scale(sfb);
+        uint8_t* dst = a.q_row + (row0 + rr) * a.K + rcol;
+        const uint2 q0 = quant8_bf16(w[0], inv), q1 = quant8_bf16(w[1], inv), q2 = quant8_bf16(w[2], inv),
+                    q3 = quant8_bf16(w[3], inv);
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
+        a.sf_row[sf_mma_offset(row0 + rr, rcol >> 5, a.K / 128)] = static_cast<uint8_t>(sfb);
       }
     }
-    const int64_t rcol = col0 + cb * 32;
-    if (rcol < a.K) {
-      const uint32_t sfb = e8m0_from_amax(amax);
-      const float inv = e8m0_inverse_scale(sfb);
-      const uint2 q0 = quant8(v + 0, inv), q1 = quant8(v + 8, inv), q2 = quant8(v + 16, inv), q3 = quant8(v + 24, inv);
-      uint8_t* dst = a.q_row + (row0 + rr) * a.K + rcol;
-      reinterpret_cast<uint4*>(dst)[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
-      reinterpret_cast<uint4*>(dst)[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
-      a.sf_row[sf_mma_offset(row0 + rr, rcol >> 5, a.K / 128)] = static_cast<uint8_t>(sfb);
-    }
   }
-  const int c = tid % QTT_COLS;
-  const int rb = tid / QTT_COLS;   // 32-row block inside the tile
-  const int64_t col = col0 + c;
+  const int cp = tid % (QTT_COLS / 2);   // column pair
+  const int rb = tid / (QTT_COLS / 2);   // 32-row block inside the tile
+  const int64_t col = col0 + 2 * cp;
   if (col >= a.K) return;
-  float v[32];
-  float amax = 0.0f;
+  uint32_t pk[32];                        // packed bf16 pairs (column col in the low half)
+  uint32_t m2 = 0;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    v[i] = __uint_as_float(static_cast<uint32_t>(tile[rb * 32 + i][c]) << 16);
-    amax = fmaxf(amax, fabsf(v[i]));
+    pk[i] = *reinterpret_cast<const uint32_t*>(&tile[rb * 32 + i][2 * cp]);
+    m2 = absmax_bf16x2(m2, pk[i]);
   }
-  const uint32_t sfb = e8m0_from_amax(amax);
-  const float inv = e8m0_inverse_scale(sfb);
-  const uint2 q0 = quant8(v + 0, inv), q1 = quant8(v + 8, inv), q2 = quant8(v + 16, inv), q3 = quant8(v + 24, inv);
-  uint8_t* dst = a.qT + col * a.m_out + row0 + rb * 32;
-  reinterpret_cast<uint4*>(dst)[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
-  reinterpret_cast<uint4*>(dst)[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
   const int64_t blk = (row0 >> 5) + rb;
-  if (a.mma)
-    a.sfT[sf_mma_offset(col, blk, a.m_out / 128)] = static_cast<uint8_t>(sfb);
-  else
-    a.sfT[col * (a.m_out >> 5) + blk] = static_cast<uint8_t>(sfb);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t sfb = e8m0_from_amax(h == 0 ? bf16_lo(m2) : bf16_hi(m2));
+    const float inv = e8m0_inverse_scale(sfb);
+    uint32_t q[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t a0 = pk[4 * k], a1 = pk[4 * k + 1], a2 = pk[4 * k + 2], a3 = pk[4 * k + 3];
+      const float v0 = h ? bf16_hi(a0) : bf16_lo(a0), v1 = h ? bf16_hi(a1) : bf16_lo(a1);
+      const float v2 = h ? bf16_hi(a2) : bf16_lo(a2), v3 = h ? bf16_hi(a3) : bf16_lo(a3);
+      q[k] = e4m3x2(v0 * inv, v1 * inv) | (e4m3x2(v2 * inv, v3 * inv) << 16);
+    }
+    uint8_t* dst = a.qT + (col + h) * a.m_out + row0 + rb * 32;
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    if (a.mma)
+      a.sfT[sf_mma_offset(col + h, blk, a.m_out / 128)] = static_cast<uint8_t>(sfb);
+    else
+      a.sfT[(col + h) * (a.m_out >> 5) + blk] = static_cast<uint8_t>(sfb);
+  }
 }
 
 template <bool ROW, bool COL, bool MMA>
