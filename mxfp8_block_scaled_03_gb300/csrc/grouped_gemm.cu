@@ -630,8 +630,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // CTA rank r of the pair holds row tile 2q + r of the expert (its 128 rows of A) and half of the
 // 256-row B tile (GroupedLinear 1: r = 0 the gate rows, r = 1 the up rows; GroupedLinear 2: W2 rows
 // 256n + 128r ..), so each SM loads 32 KB per K step for the same MMA work that costs the
-// single-CTA kernel 48 KB, and the same shared memory holds 6 stages instead of 4.  Each CTA's
-// TMEM receives its own 128 rows x 256 columns of the accumulator.
+// single-CTA kernel 48 KB.  Each CTA's TMEM receives its own 128 rows x 256 columns of the
+// accumulator.
+//
+// A stage of the data ring holds two K steps (K = 256: 8 MMAs per barrier wait; a tile with an odd
+// number of steps ends on a half stage).  The MMA thread shares its warp scheduler with two
+// epilogue warps; while those run their math, every instruction of the issuing loop waits longer,
+// and with one wait per 4 MMAs the tensor pipe ran dry in those stretches (K = 128 stages: about
+// 10% slower GroupedLinear 1).
 //
 // Synchronization is arranged so that the data ring has one hop per direction:
 //   full[s]      (leader)  both CTAs' tile copies complete on the leader's barrier (.cta_group::2
@@ -650,8 +656,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // Warp roles as in the single-CTA kernel, plus warp 6: scale-atom producer.  The MMA warp of the
 // second CTA only takes part in the TMEM allocation.
 // ---------------------------------------------------------------------------------------------
-constexpr int P_STAGES = 6;
-constexpr int P_STAGE_BYTES = 2 * 128 * BK;                   // own A tile + own half of the B tile
+constexpr int P_STAGES = 3;
+constexpr int P_SUB = 2;                                      // K steps per stage
+constexpr int P_STEP_BYTES = 2 * 128 * BK;                    // own A tile + own half of the B tile
+constexpr int P_STAGE_BYTES = P_SUB * P_STEP_BYTES;
 constexpr int P_SF_SLOTS = 16;
 constexpr int P_SF_GROUP = 4;                                 // slots freed by one MMA commit
 constexpr int P_SF_GROUPS = P_SF_SLOTS / P_SF_GROUP;
@@ -666,7 +674,7 @@ constexpr int WARP_SF_PRODUCER = 6;
 constexpr uint32_t P_REGS_LOW = 64;
 constexpr uint32_t P_REGS_HIGH = 192;
 static_assert(2 * 128 * P_REGS_LOW + 256 * P_REGS_HIGH == NUM_THREADS * 128, "register split must equal the launch pool");
-static_assert(P_STAGE_BYTES % 1024 == 0, "pair stages keep 1024-byte alignment");
+static_assert(P_STEP_BYTES % 1024 == 0, "pair stages keep 1024-byte alignment");
 static_assert(P_SFA_COL + 4 * P_SF_SLOTS <= P_SFB_COL && P_SFB_COL + 8 * P_SF_SLOTS <= TMEM_COLS, "pair TMEM budget");
 static_assert(P_SMEM_BYTES <= 232448, "pair shared memory budget");
 
@@ -897,28 +905,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             prefetch_l2(p.gu + gu_offset(prow, j, 2 * p.ldh), t.n * 256 + 256 <= p.ldh ? 16384 : 8192);
           }
         }
-        for (int kb = 0; kb < t.steps; ++kb, ++g) {
+        for (int kb = 0, nsub = 0; kb < t.steps; kb += nsub, g += nsub) {
+          nsub = min(P_SUB, t.steps - kb);
           if (!pair_wait(&empty[stage], phase ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_PRODUCER, lane)) {
             ok = false;
             break;
           }
           if (lane == 0) {
-            uint8_t* sA = smem + stage * P_STAGE_BYTES;
-            if constexpr (MODE == GEMM_DGRAD)   // dy tiles are reused by every column tile: keep them in L2
-              tma_load_2d_pair_hint(sA, &tmA, leader_full + stage * 8, t.a_k0 + kb * BK, t.a_row, a_policy);
-            else
-              tma_load_2d_pair(sA, &tmA, leader_full + stage * 8, t.a_k0 + kb * BK, t.a_row);
-            tma_load_2d_pair(sA + A_BYTES, &tmB, leader_full + stage * 8, t.b_k0 + kb * BK, b_own);
+            for (int j = 0; j < nsub; ++j) {
+              uint8_t* sA = smem + stage * P_STAGE_BYTES + j * P_STEP_BYTES;
+              const int k0 = (kb + j) * BK;
+              if constexpr (MODE == GEMM_DGRAD)   // dy tiles are reused by every column tile: keep them in L2
+                tma_load_2d_pair_hint(sA, &tmA, leader_full + stage * 8, t.a_k0 + k0, t.a_row, a_policy);
+              else
+                tma_load_2d_pair(sA, &tmA, leader_full + stage * 8, t.a_k0 + k0, t.a_row);
+              tma_load_2d_pair(sA + A_BYTES, &tmB, leader_full + stage * 8, t.b_k0 + k0, b_own);
+            }
             if (leader) {
-              // The leader's arrival completes the stage only once the step's scales are in both
-              // CTAs' TMEM, so the MMA thread waits on this one barrier per step.  The scale ring
+              // The leader's arrival completes the stage only once its steps' scales are in both
+              // CTAs' TMEM, so the MMA thread waits on this one barrier per stage.  The scale ring
               // runs about three groups ahead, so this wait rarely blocks.
-              const int slot = g % P_SF_SLOTS;
-              if (slot % P_SF_GROUP == 0 &&
-                  !pair_lane_wait(&sf_full[slot / P_SF_GROUP], (g / P_SF_SLOTS) & 1u, true, abort_flag, peer_abort, p,
-                                  ERR_TIMEOUT_PRODUCER))
-                ok = false;
-              mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+              for (int j = 0; j < nsub; ++j) {
+                const int slot = (g + j) % P_SF_SLOTS;
+                if (slot % P_SF_GROUP == 0 &&
+                    !pair_lane_wait(&sf_full[slot / P_SF_GROUP], ((g + j) / P_SF_SLOTS) & 1u, true, abort_flag,
+                                    peer_abort, p, ERR_TIMEOUT_PRODUCER))
+                  ok = false;
+              }
+              mbar_arrive_expect_tx(&full[stage], 2 * nsub * P_STEP_BYTES);
             }
           }
           __syncwarp();
@@ -1008,29 +1022,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (!pair_lane_wait(acc_empty, acc_phase ^ 1u, true, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) break;
           tc_fence_after();
-          for (int kb = 0; kb < steps; ++kb) {
-            // full implies the step's scales are staged (the leader's producer waited for them)
+          for (int kb = 0; kb < steps; kb += P_SUB) {
+            // full implies the stage's scales are staged (the leader's producer waited for them)
             if (!pair_lane_wait(&full[stage], phase, false, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(smem + stage * P_STAGE_BYTES), b0 = a0 + A_BYTES;
-            const uint32_t t_sfa = tmem + P_SFA_COL + 4 * slot;
-            const uint32_t t_sfb = tmem + P_SFB_COL + 8 * slot;
+            const uint32_t st0 = smem_u32(smem + stage * P_STAGE_BYTES);
+            const int slot0 = slot;
 #pragma unroll
-            for (int k = 0; k < BK / 32; ++k) {
-              tc_mma_mxf8_pair(tmem + ACC_COL, sdesc_kmajor_sw128(a0 + 32 * k), sdesc_kmajor_sw128(b0 + 32 * k),
-                               idesc_with_sf_id(idesc, k), t_sfa, t_sfb, (kb | k) != 0 ? 1u : 0u);
+            for (int j = 0; j < P_SUB; ++j) {
+              if (j > 0 && kb + j >= steps) break;   // half stage at the end of an odd tile
+              const uint32_t a0 = st0 + j * P_STEP_BYTES, b0 = a0 + A_BYTES;
+              const uint32_t t_sfa = tmem + P_SFA_COL + 4 * slot;
+              const uint32_t t_sfb = tmem + P_SFB_COL + 8 * slot;
+#pragma unroll
+              for (int k = 0; k < BK / 32; ++k) {
+                tc_mma_mxf8_pair(tmem + ACC_COL, sdesc_kmajor_sw128(a0 + 32 * k), sdesc_kmajor_sw128(b0 + 32 * k),
+                                 idesc_with_sf_id(idesc, k), t_sfa, t_sfb, ((kb + j) | k) != 0 ? 1u : 0u);
+              }
+              if (++slot == P_SF_SLOTS) slot = 0;
             }
             tc_commit_pair_both(&empty[stage]);
-            if (slot % P_SF_GROUP == P_SF_GROUP - 1) tc_commit_pair_both(&sf_empty[slot / P_SF_GROUP]);
+            // a group's slots are free once the MMAs of its last step completed
+            for (int s2 = slot0; s2 != slot; s2 = (s2 + 1) % P_SF_SLOTS)
+              if (s2 % P_SF_GROUP == P_SF_GROUP - 1) tc_commit_pair_both(&sf_empty[s2 / P_SF_GROUP]);
             issued = true;
             if (++stage == P_STAGES) {
               stage = 0;
               phase ^= 1u;
             }
-            if (++slot == P_SF_SLOTS) slot = 0;
           }
           if (!ok) break;
           tc_commit_pair_both(acc_full);
