@@ -248,24 +248,35 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     const float gate = real ? (p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f) : 0.0f;
     uint8_t* hrow = p.hq + static_cast<int64_t>(t.pad_row0 + r) * p.ldh + t.n * 128 + 64 * half;
     uint32_t sf_pair = 0;
+    const uint64_t one2 = f2_pack(1.0f, 1.0f);
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
-      float h[32];
+      // column pairs in f32x2 arithmetic: hs = silu(G) * U; h = gate * hs.  The gate is one
+      // factor per row, so it moves out of the block maximum and into the quantization
+      // multiplier: max|fl(gate hs)| = fl(|gate| max|hs|) (rounding is monotonic) and
+      // fl(hs fl(gate 2^-s)) = fl(gate hs) 2^-s (power-of-two scaling is exact): the same codes and
+      // scale byte as rounding h itself.
+      uint64_t hs[16];
       float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float g = __uint_as_float(v[32 * b + i]);
-        const float up = __uint_as_float(v[64 + 32 * b + i]);
-        const float s = __fdividef(g, 1.0f + __expf(-g));
-        h[i] = gate * s * up;
-        amax = fmaxf(amax, fabsf(h[i]));
+      for (int i = 0; i < 16; ++i) {
+        const uint64_t g = f2_pack(__uint_as_float(v[32 * b + 2 * i]), __uint_as_float(v[32 * b + 2 * i + 1]));
+        const uint64_t up =
+            f2_pack(__uint_as_float(v[64 + 32 * b + 2 * i]), __uint_as_float(v[64 + 32 * b + 2 * i + 1]));
+        const uint64_t d = f2_add(f2_pack(__expf(-f2_lo(g)), __expf(-f2_hi(g))), one2);   // 1 + e^-g
+        const uint64_t sig = f2_pack(__fdividef(1.0f, f2_lo(d)), __fdividef(1.0f, f2_hi(d)));
+        hs[i] = f2_mul(f2_mul(g, sig), up);
+        amax = fmaxf(amax, fmaxf(fabsf(f2_lo(hs[i])), fabsf(f2_hi(hs[i]))));
       }
-      const uint32_t sfb = e8m0_from_amax(amax);
-      const float inv = e8m0_inverse_scale(sfb);
-      const uint2 t0 = quant8(h + 0, inv), t1 = quant8(h + 8, inv), t2 = quant8(h + 16, inv),
-                  t3 = quant8(h + 24, inv);
-      reinterpret_cast<uint4*>(hrow + 32 * b)[0] = make_uint4(t0.x, t0.y, t1.x, t1.y);
-      reinterpret_cast<uint4*>(hrow + 32 * b)[1] = make_uint4(t2.x, t2.y, t3.x, t3.y);
+      const uint32_t sfb = e8m0_from_amax(fabsf(gate) * amax);
+      const float gi = gate * e8m0_inverse_scale(sfb);
+      const uint64_t gi2 = f2_pack(gi, gi);
+      uint32_t q[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        q[k] = e4m3x2_f2(f2_mul(hs[2 * k], gi2)) | (e4m3x2_f2(f2_mul(hs[2 * k + 1], gi2)) << 16);
+      reinterpret_cast<uint4*>(hrow + 32 * b)[0] = make_uint4(q[0], q[1], q[2], q[3]);
+      reinterpret_cast<uint4*>(hrow + 32 * b)[1] = make_uint4(q[4], q[5], q[6], q[7]);
       sf_pair |= sfb << (8 * b);
     }
     // scale bytes of blocks (2*half, 2*half+1) of column tile n for padded row pad_row0 + r
