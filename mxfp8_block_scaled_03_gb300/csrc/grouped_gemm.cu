@@ -275,8 +275,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
 #pragma unroll
       for (int k = 0; k < 8; ++k)
         q[k] = e4m3x2_f2(f2_mul(hs[2 * k], gi2)) | (e4m3x2_f2(f2_mul(hs[2 * k + 1], gi2)) << 16);
-      reinterpret_cast<uint4*>(hrow + 32 * b)[0] = make_uint4(q[0], q[1], q[2], q[3]);
-      reinterpret_cast<uint4*>(hrow + 32 * b)[1] = make_uint4(q[4], q[5], q[6], q[7]);
+      // one full 32-byte sector per store (two 16-byte stores cost GroupedLinear 1 about 3%)
+      st_global_32B(hrow + 32 * b, make_uint4(q[0], q[1], q[2], q[3]), make_uint4(q[4], q[5], q[6], q[7]));
       sf_pair |= sfb << (8 * b);
     }
     // scale bytes of blocks (2*half, 2*half+1) of column tile n for padded row pad_row0 + r
