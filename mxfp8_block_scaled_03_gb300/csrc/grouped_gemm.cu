@@ -315,6 +315,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     float part = 0.0f;
     if (r < t.valid) {
       const float gate = p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f;
+      const uint64_t gate2 = f2_pack(gate, gate), one2 = f2_pack(1.0f, 1.0f), mone2 = f2_pack(-1.0f, -1.0f);
+      uint64_t part2 = f2_pack(0.0f, 0.0f);
       // blocked layout (gu_offset), prefetched into L2 at the tile's start
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 16) {
@@ -327,35 +329,38 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
         uint4 odg[2], odu[2], oh[2];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-        const int c = c0 + 8 * hh;
-        const uint4 gw = gw2[hh], uw = uw2[hh];
-        const float g[8] = {bf16_lo(gw.x), bf16_hi(gw.x), bf16_lo(gw.y), bf16_hi(gw.y),
-                            bf16_lo(gw.z), bf16_hi(gw.z), bf16_lo(gw.w), bf16_hi(gw.w)};
-        const float u[8] = {bf16_lo(uw.x), bf16_hi(uw.x), bf16_lo(uw.y), bf16_hi(uw.y),
-                            bf16_lo(uw.z), bf16_hi(uw.z), bf16_lo(uw.w), bf16_hi(uw.w)};
-        float dg[8], du[8], hv[8];
+          const int c = c0 + 8 * hh;
+          const uint32_t gw[4] = {gw2[hh].x, gw2[hh].y, gw2[hh].z, gw2[hh].w};
+          const uint32_t uw[4] = {uw2[hh].x, uw2[hh].y, uw2[hh].z, uw2[hh].w};
+          uint32_t pdg[4], pdu[4], ph[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float dh = __uint_as_float(v[c + i]);
-          const float sig = __fdividef(1.0f, 1.0f + __expf(-g[i]));
-          const float sl = g[i] * sig;
-          const float dsl = sig * (1.0f + g[i] * (1.0f - sig));
-          dg[i] = dh * gate * u[i] * dsl;
-          du[i] = dh * gate * sl;
-          hv[i] = gate * sl * u[i];
-          part += dh * sl * u[i];
-        }
-        odg[hh] = make_uint4(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]), pack_bf16x2(dg[4], dg[5]),
-                             pack_bf16x2(dg[6], dg[7]));
-        odu[hh] = make_uint4(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]), pack_bf16x2(du[4], du[5]),
-                             pack_bf16x2(du[6], du[7]));
-        oh[hh] = make_uint4(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]), pack_bf16x2(hv[4], hv[5]),
-                            pack_bf16x2(hv[6], hv[7]));
+          for (int i = 0; i < 4; ++i) {   // column pairs (c + 2i, c + 2i + 1) in f32x2 arithmetic
+            const uint64_t g = f2_pack(bf16_lo(gw[i]), bf16_hi(gw[i]));
+            const uint64_t u = f2_pack(bf16_lo(uw[i]), bf16_hi(uw[i]));
+            const uint64_t dh = f2_pack(__uint_as_float(v[c + 2 * i]), __uint_as_float(v[c + 2 * i + 1]));
+            const uint64_t d = f2_add(f2_pack(__expf(-f2_lo(g)), __expf(-f2_hi(g))), one2);   // 1 + e^-g
+            const uint64_t sig = f2_pack(__fdividef(1.0f, f2_lo(d)), __fdividef(1.0f, f2_hi(d)));
+            const uint64_t sl = f2_mul(g, sig);                                    // silu(g)
+            const uint64_t su = f2_mul(sl, u);                                     // silu(g) u
+            const uint64_t dsl = f2_mul(sig, f2_fma(g, f2_fma(sig, mone2, one2), one2));   // silu'(g)
+            const uint64_t dhg = f2_mul(dh, gate2);
+            part2 = f2_fma(dh, su, part2);
+            const uint64_t dgv = f2_mul(f2_mul(dhg, u), dsl);
+            const uint64_t duv = f2_mul(dhg, sl);
+            const uint64_t hv = f2_mul(gate2, su);
+            pdg[i] = pack_bf16x2(f2_lo(dgv), f2_hi(dgv));
+            pdu[i] = pack_bf16x2(f2_lo(duv), f2_hi(duv));
+            ph[i] = pack_bf16x2(f2_lo(hv), f2_hi(hv));
+          }
+          odg[hh] = make_uint4(pdg[0], pdg[1], pdg[2], pdg[3]);
+          odu[hh] = make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]);
+          oh[hh] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
         }
         st_global_32B_cs(dg_row + c0, odg[0], odg[1]);
         st_global_32B_cs(dg_row + F + c0, odu[0], odu[1]);
         st_global_32B_cs(h_row + c0, oh[0], oh[1]);
       }
+      part = f2_lo(part2) + f2_hi(part2);
     } else {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 4
