@@ -242,7 +242,7 @@ struct QuantTArgs {
 };
 
 template <bool GATHER, bool ROW>
-__global__ void __launch_bounds__(256) k_quantize_t(const QuantTArgs a) {
+__global__ void __launch_bounds__(256, 5) k_quantize_t(const QuantTArgs a) {   // 5 blocks per SM: 48 registers
   __shared__ __align__(16) uint16_t tile[QTT_ROWS][QTT_COLS + 8];
   const int tid = threadIdx.x;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * QTT_ROWS;
