@@ -121,6 +121,8 @@ struct GemmParams {
   // operand addressing of the pair kernel
   int a_kt;                // scale atoms per 128-row tile of A (K extent of A / 128)
   int b_kt;                // same for B
+  int a_sf_tiles;          // 128-row tiles of A's scale array (pair kernel: extent of its scale map)
+  int b_sf_tiles;          // same for B
   int b_kofs;              // expert e's block of B starts at K column e * b_kofs (weights stored
                            // transposed as one [N, E*K] matrix); 0 for the forward
   // GEMM_SWIGLU in a training forward: [G | U] saved as bf16 [R_pad, 2F] (NULL: not saved)
@@ -659,38 +661,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //   full[s]      (leader)  both CTAs' tile copies complete on the leader's barrier (.cta_group::2
 //                          copies); the leader's producer posts the byte count of both halves
 //   empty[s]     (both)    the leader's MMA commit, multicast to both CTAs
-// The block scales travel on a separate, deeper ring (16 slots, K step g in slot g mod 16) that
-// runs ahead of the data, synchronized per group of 4 slots.  The MMA thread never waits on it:
-// the leader's producer waits for a group's scales before its arrival completes the group's first
-// stage (every wait in the MMA thread costs the tensor pipe 30-80 ns; its queue is shallow).
-//   sf_land[i]   (each)    this CTA's scale atoms of group i landed in shared memory
-//   sf_full[i]   (leader)  both CTAs' scale warps wrote group i into their TMEM (8 warp arrivals)
-//   sf_empty[i]  (both)    the MMAs that read group i completed (leader's commit, multicast)
+// The block scales of a K step (this CTA's A atom and both B atoms, 3 x 512 bytes) travel in the
+// same stage as its tiles, by TMA onto the same barrier.  The MMA thread copies them into TMEM with
+// tcgen05.cp just before the step's MMAs: copies and MMAs issued by one thread run in order, so no
+// other warp and no other barrier takes part.  A TMEM scale slot belongs to one sub-buffer of the
+// ring and is rewritten only after the stage's empty barrier, i.e. after the MMAs that read it.
+// (A version with a separate 16-slot scale ring filled by four tcgen05.st warps and one more
+// producer was 17% slower on GroupedLinear 1: its barriers sat on the path of every stage.)
 // and the accumulator hand-off:
 //   acc_full     (both)    the tile's MMAs completed (leader's commit, multicast)
 //   acc_empty    (leader)  both CTAs' epilogues read their accumulator out (16 warp arrivals)
-// Warp roles as in the single-CTA kernel, plus warp 6: scale-atom producer.  The MMA warp of the
-// second CTA only takes part in the TMEM allocation.
+// Warp roles: warp 4 producer (both CTAs), warp 5 MMA issuer (leader CTA; the MMA warp of the
+// second CTA only takes part in the TMEM allocation), warps 8-15 epilogue; the other role warps idle.
 // ---------------------------------------------------------------------------------------------
 constexpr int P_STAGES = 3;
 constexpr int P_SUB = 2;                                      // K steps per stage
 constexpr int P_STEP_BYTES = 2 * 128 * BK;                    // own A tile + own half of the B tile
-constexpr int P_STAGE_BYTES = P_SUB * P_STEP_BYTES;
-constexpr int P_SF_SLOTS = 16;
-constexpr int P_SF_GROUP = 4;                                 // slots freed by one MMA commit
-constexpr int P_SF_GROUPS = P_SF_SLOTS / P_SF_GROUP;
-constexpr int P_SF_SLOT_BYTES = 3 * SF_ATOM;                  // A atom + both B atoms
+constexpr int P_SF_BYTES = 3 * SF_ATOM;                       // own A atom + both B atoms of the step
+constexpr int P_SUBBUF_BYTES = P_STEP_BYTES + 2048;           // tiles, scale atoms, pad to 1 KB
+constexpr int P_STAGE_BYTES = P_SUB * P_SUBBUF_BYTES;
+constexpr int P_SF_SLOTS = P_STAGES * P_SUB;                  // one TMEM scale slot per sub-buffer
 constexpr int P_DATA_BYTES = P_STAGES * P_STAGE_BYTES;
-constexpr int P_BAR_OFFSET = P_DATA_BYTES + P_SF_SLOTS * P_SF_SLOT_BYTES;
-constexpr int P_NUM_BARS = 2 * P_STAGES + 3 * P_SF_GROUPS + 3;
+constexpr int P_BAR_OFFSET = P_DATA_BYTES;
+constexpr int P_NUM_BARS = 2 * P_STAGES + 3;
 constexpr int P_SMEM_BYTES = P_BAR_OFFSET + P_NUM_BARS * 8 + 8 + 1024;
 constexpr uint32_t P_SFA_COL = 256;                           // 4 columns per slot
-constexpr uint32_t P_SFB_COL = 320;                           // 8 columns per slot
-constexpr int WARP_SF_PRODUCER = 6;
+constexpr uint32_t P_SFB_COL = P_SFA_COL + 4 * P_SF_SLOTS;    // 8 columns per slot
 constexpr uint32_t P_REGS_LOW = 64;
 constexpr uint32_t P_REGS_HIGH = 192;
 static_assert(2 * 128 * P_REGS_LOW + 256 * P_REGS_HIGH == NUM_THREADS * 128, "register split must equal the launch pool");
-static_assert(P_STEP_BYTES % 1024 == 0, "pair stages keep 1024-byte alignment");
+static_assert(P_STEP_BYTES % 1024 == 0 && P_SUBBUF_BYTES % 1024 == 0, "pair stages keep 1024-byte alignment");
+static_assert(P_STEP_BYTES + P_SF_BYTES <= P_SUBBUF_BYTES, "scale atoms fit behind the tiles");
 static_assert(P_SFA_COL + 4 * P_SF_SLOTS <= P_SFB_COL && P_SFB_COL + 8 * P_SF_SLOTS <= TMEM_COLS, "pair TMEM budget");
 static_assert(P_SMEM_BYTES <= 232448, "pair shared memory budget");
 
@@ -807,16 +808,13 @@ __device__ __forceinline__ bool pair_lane_wait(uint64_t* bar, uint32_t parity, b
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sf_ring = smem + P_DATA_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_BAR_OFFSET);
   uint64_t* empty = full + P_STAGES;
-  uint64_t* sf_land = empty + P_STAGES;
-  uint64_t* sf_full = sf_land + P_SF_GROUPS;
-  uint64_t* sf_empty = sf_full + P_SF_GROUPS;
-  uint64_t* acc_full = sf_empty + P_SF_GROUPS;
+  uint64_t* acc_full = empty + P_STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drained = acc_empty + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drained + 1);
@@ -831,11 +829,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < P_STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-    }
-    for (int j = 0; j < P_SF_GROUPS; ++j) {
-      mbar_init(&sf_land[j], 1);
-      mbar_init(&sf_full[j], 2 * NUM_SF_WARPS);
-      mbar_init(&sf_empty[j], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * NUM_EPI_WARPS);
@@ -858,59 +851,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int first_unit = static_cast<int>(cluster_index());
   const int unit_stride = static_cast<int>(cluster_count());
   const uint32_t peer_abort = map_to_cta(const_cast<int*>(abort_flag), rank ^ 1u);
-  // K steps this pair runs in all (both CTAs run the same sequence of units)
-  int total_steps = 0;
-  if constexpr (MODE == GEMM_WGRAD) {
-    for (int u = first_unit; u < total_units; u += unit_stride) {
-      TileInfo t;
-      decode_pair_tile<MODE>(u, static_cast<int>(rank), p, t);
-      total_steps += t.steps;
-    }
-  } else {
-    const int my_units = first_unit < total_units ? (total_units - first_unit + unit_stride - 1) / unit_stride : 0;
-    total_steps = my_units * p.KT;
-  }
-
-  if (warp < NUM_SF_WARPS) {
-    regs_dec<P_REGS_LOW>();
-    // ---------------- scale staging: own shared-memory slots -> own TMEM slots ----------------
-    const uint32_t t_lanes = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t leader_sf_full = map_to_cta(sf_full, 0);
-    for (int g = 0; g < total_steps; ++g) {
-      const int slot = g % P_SF_SLOTS;
-      const int grp = slot / P_SF_GROUP;
-      if (slot % P_SF_GROUP == 0) {   // one thread waits for the group's atoms, the others learn it here
-        bool got = true;
-        if (threadIdx.x == 0)
-          got = pair_lane_wait(&sf_land[grp], (g / P_SF_SLOTS) & 1u, false, abort_flag, peer_abort, p, ERR_TIMEOUT_SF);
-        if (!group_and(BAR_SF, NUM_SF_WARPS * 32, got)) break;
-      }
-      const uint8_t* src = sf_ring + slot * P_SF_SLOT_BYTES;
-      tmem_st_32x32b_x4(t_lanes + P_SFA_COL + 4 * slot, *reinterpret_cast<const uint4*>(src + lane * 16));
-      tmem_st_32x32b_x4(t_lanes + P_SFB_COL + 8 * slot, *reinterpret_cast<const uint4*>(src + SF_ATOM + lane * 16));
-      tmem_st_32x32b_x4(t_lanes + P_SFB_COL + 8 * slot + 4,
-                        *reinterpret_cast<const uint4*>(src + 2 * SF_ATOM + lane * 16));
-      if (slot % P_SF_GROUP == P_SF_GROUP - 1 || g == total_steps - 1) {
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(leader_sf_full + grp * 8);
-      }
-    }
-  } else if (warp < FIRST_EPI_WARP) {
+  if (warp < FIRST_EPI_WARP) {
     regs_dec<P_REGS_LOW>();
     if (warp == WARP_PRODUCER) {
       // ---------------- tile producer (both CTAs; lane 0 issues) ----------------
       const uint32_t leader_full = map_to_cta(full, 0);
       const uint64_t a_policy = l2_policy_evict_last();
       uint32_t issued_mask = 0, issued_parity = 0;
-      int stage = 0, g = 0;
+      int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int u = first_unit; ok && u < total_units; u += unit_stride) {
         TileInfo t;
         decode_pair_tile<MODE>(u, static_cast<int>(rank), p, t);
         const int b_own = rank == 0 ? t.b_row0 : t.b_row1;
+        // scale atoms (512 bytes: 128 rows x 4 blocks) of the tile's first K step; step kb adds kb.
+        // Past the end of B (half of a last tile) any valid atom will do: those B rows are zeros.
+        const int a_atom0 = (t.a_row / 128) * p.a_kt + t.a_k0 / BK;
+        const int b_atom0 = (t.b_row0 / 128) * p.b_kt + t.b_k0 / BK;
+        const int b_row1 = (p.b_rows > 0 && t.b_row1 >= p.b_rows) ? t.b_row0 : t.b_row1;
+        const int b_atom1 = (b_row1 / 128) * p.b_kt + t.b_k0 / BK;
         if constexpr (MODE == GEMM_DGRAD) {
           // the epilogue of this tile reads the saved g and u of its 128 rows x 256 columns of F:
           // have L2 fetch them while the tile's MMAs run (in the blocked layout each 32-row block's
@@ -921,35 +881,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             prefetch_l2(p.gu + gu_offset(prow, j, 2 * p.ldh), t.n * 256 + 256 <= p.ldh ? 16384 : 8192);
           }
         }
-        for (int kb = 0, nsub = 0; kb < t.steps; kb += nsub, g += nsub) {
+        for (int kb = 0, nsub = 0; kb < t.steps; kb += nsub) {
           nsub = min(P_SUB, t.steps - kb);
           if (!pair_wait(&empty[stage], phase ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_PRODUCER, lane)) {
             ok = false;
             break;
           }
           if (lane == 0) {
+            const uint32_t bar = leader_full + stage * 8;
             for (int j = 0; j < nsub; ++j) {
-              uint8_t* sA = smem + stage * P_STAGE_BYTES + j * P_STEP_BYTES;
+              uint8_t* sA = smem + stage * P_STAGE_BYTES + j * P_SUBBUF_BYTES;
               const int k0 = (kb + j) * BK;
               if constexpr (MODE == GEMM_DGRAD)   // dy tiles are reused by every column tile: keep them in L2
-                tma_load_2d_pair_hint(sA, &tmA, leader_full + stage * 8, t.a_k0 + k0, t.a_row, a_policy);
+                tma_load_2d_pair_hint(sA, &tmA, bar, t.a_k0 + k0, t.a_row, a_policy);
               else
-                tma_load_2d_pair(sA, &tmA, leader_full + stage * 8, t.a_k0 + k0, t.a_row);
-              tma_load_2d_pair(sA + A_BYTES, &tmB, leader_full + stage * 8, t.b_k0 + k0, b_own);
+                tma_load_2d_pair(sA, &tmA, bar, t.a_k0 + k0, t.a_row);
+              tma_load_2d_pair(sA + A_BYTES, &tmB, bar, t.b_k0 + k0, b_own);
+              uint8_t* sS = sA + P_STEP_BYTES;   // scale atoms: 2 rows of 256 bytes each in the maps
+              tma_load_2d_pair(sS, &tmSA, bar, 0, 2 * (a_atom0 + kb + j));
+              tma_load_2d_pair(sS + SF_ATOM, &tmSB, bar, 0, 2 * (b_atom0 + kb + j));
+              tma_load_2d_pair(sS + 2 * SF_ATOM, &tmSB, bar, 0, 2 * (b_atom1 + kb + j));
             }
-            if (leader) {
-              // The leader's arrival completes the stage only once its steps' scales are in both
-              // CTAs' TMEM, so the MMA thread waits on this one barrier per stage.  The scale ring
-              // runs about three groups ahead, so this wait rarely blocks.
-              for (int j = 0; j < nsub; ++j) {
-                const int slot = (g + j) % P_SF_SLOTS;
-                if (slot % P_SF_GROUP == 0 &&
-                    !pair_lane_wait(&sf_full[slot / P_SF_GROUP], ((g + j) / P_SF_SLOTS) & 1u, true, abort_flag,
-                                    peer_abort, p, ERR_TIMEOUT_PRODUCER))
-                  ok = false;
-              }
-              mbar_arrive_expect_tx(&full[stage], 2 * nsub * P_STEP_BYTES);
-            }
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * nsub * (P_STEP_BYTES + P_SF_BYTES));
           }
           __syncwarp();
           ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
@@ -978,54 +931,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       __syncwarp();
-    } else if (warp == WARP_SF_PRODUCER) {
-      // ---------------- scale-atom producer (both CTAs; lane 0 issues) ----------------
-      uint32_t issued_mask = 0, issued_parity = 0;
-      int g = 0;
-      bool ok = true;
-      for (int u = first_unit; ok && u < total_units; u += unit_stride) {
-        TileInfo t;
-        decode_pair_tile<MODE>(u, static_cast<int>(rank), p, t);
-        const int64_t a_atom0 = static_cast<int64_t>(t.a_row / 128) * p.a_kt + t.a_k0 / BK;
-        const int64_t b_atom0 = static_cast<int64_t>(t.b_row0 / 128) * p.b_kt + t.b_k0 / BK;
-        // past the end of B (half of a last tile), any valid atom will do: those B rows are zeros
-        const int b_row1 = (p.b_rows > 0 && t.b_row1 >= p.b_rows) ? t.b_row0 : t.b_row1;
-        const int64_t b_atom1 = static_cast<int64_t>(b_row1 / 128) * p.b_kt + t.b_k0 / BK;
-        for (int kb = 0; kb < t.steps; ++kb, ++g) {
-          const int slot = g % P_SF_SLOTS;
-          const int grp = slot / P_SF_GROUP;
-          const uint32_t lap = (g / P_SF_SLOTS) & 1u;
-          if (slot % P_SF_GROUP == 0) {
-            // the previous lap's MMAs are done with the group; post the bytes of its (up to 4) steps
-            if (!pair_wait(&sf_empty[grp], lap ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_SF, lane)) {
-              ok = false;
-              break;
-            }
-            if (lane == 0)
-              mbar_arrive_expect_tx(&sf_land[grp], min(P_SF_GROUP, total_steps - g) * P_SF_SLOT_BYTES);
-            issued_mask |= 1u << grp;
-            issued_parity = (issued_parity & ~(1u << grp)) | (lap << grp);
-          }
-          if (lane == 0) {
-            uint8_t* dst = sf_ring + slot * P_SF_SLOT_BYTES;
-            bulk_load(dst, p.a_sf + (a_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
-            bulk_load(dst + SF_ATOM, p.b_sf + (b_atom0 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
-            bulk_load(dst + 2 * SF_ATOM, p.b_sf + (b_atom1 + kb) * SF_ATOM, SF_ATOM, &sf_land[grp]);
-          }
-          __syncwarp();
-        }
-      }
-      if (lane == 0)
-        for (int j = 0; j < P_SF_GROUPS; ++j)
-          if ((issued_mask >> j) & 1u)
-            if (!mbar_wait_bounded(&sf_land[j], (issued_parity >> j) & 1u, nullptr, p.timeout_ns))
-              atomicOr(p.err, ERR_TIMEOUT_DRAIN);
-      __syncwarp();
     } else if (warp == WARP_MMA && leader) {
       // ---------------- pair MMA issuer (leader CTA; the loop runs in lane 0 alone) ----------------
       if (lane == 0) {
         const uint32_t idesc = idesc_mxf8_e4m3(2 * BM, 256);
-        int stage = 0, slot = 0;
+        int stage = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool issued = false, ok = true;
         for (int u = first_unit; ok && u < total_units; u += unit_stride) {
@@ -1046,24 +956,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t st0 = smem_u32(smem + stage * P_STAGE_BYTES);
-            const int slot0 = slot;
 #pragma unroll
             for (int j = 0; j < P_SUB; ++j) {
               if (j > 0 && kb + j >= steps) break;   // half stage at the end of an odd tile
-              const uint32_t a0 = st0 + j * P_STEP_BYTES, b0 = a0 + A_BYTES;
+              const uint32_t a0 = st0 + j * P_SUBBUF_BYTES, b0 = a0 + A_BYTES, sf0 = a0 + P_STEP_BYTES;
+              const int slot = stage * P_SUB + j;
               const uint32_t t_sfa = tmem + P_SFA_COL + 4 * slot;
               const uint32_t t_sfb = tmem + P_SFB_COL + 8 * slot;
+              // scales of the step into TMEM (both CTAs, each from its own shared memory); the MMAs
+              // below are issued after them by this thread and see them in order
+              tc_copy_sf_pair(t_sfa, sdesc_sf_atom(sf0));
+              tc_copy_sf_pair(t_sfb, sdesc_sf_atom(sf0 + SF_ATOM));
+              tc_copy_sf_pair(t_sfb + 4, sdesc_sf_atom(sf0 + 2 * SF_ATOM));
 #pragma unroll
               for (int k = 0; k < BK / 32; ++k) {
                 tc_mma_mxf8_pair(tmem + ACC_COL, sdesc_kmajor_sw128(a0 + 32 * k), sdesc_kmajor_sw128(b0 + 32 * k),
                                  idesc_with_sf_id(idesc, k), t_sfa, t_sfb, ((kb + j) | k) != 0 ? 1u : 0u);
               }
-              if (++slot == P_SF_SLOTS) slot = 0;
             }
             tc_commit_pair_both(&empty[stage]);
-            // a group's slots are free once the MMAs of its last step completed
-            for (int s2 = slot0; s2 != slot; s2 = (s2 + 1) % P_SF_SLOTS)
-              if (s2 % P_SF_GROUP == P_SF_GROUP - 1) tc_commit_pair_both(&sf_empty[s2 / P_SF_GROUP]);
             issued = true;
             if (++stage == P_STAGES) {
               stage = 0;
@@ -1214,6 +1125,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A tensor-core scale array (512-byte atoms) as a 2-D byte matrix of 256-byte rows, boxes of two rows:
+// box (0, 2a) is atom a.
+bool make_sf_map(CUtensorMap* m, const void* base, uint64_t atoms) {
+  auto enc = tensor_map_encoder();
+  if (!enc || atoms == 0) return false;
+  cuuint64_t dims[2] = {256, 2 * atoms};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, 2};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct DeviceInfo {
   int sms = 0;
   int pair_clusters[4] = {0, 0, 0, 0};   // co-resident CTA pairs of each pair-kernel mode (0: none)
@@ -1253,9 +1178,13 @@ int max_pair_clusters() {
 template <int MODE>
 cudaError_t launch_pair(int clusters, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                         cudaStream_t stream) {
+  CUtensorMap sa, sb;
+  if (!make_sf_map(&sa, p.a_sf, static_cast<uint64_t>(p.a_sf_tiles) * p.a_kt) ||
+      !make_sf_map(&sb, p.b_sf, static_cast<uint64_t>(p.b_sf_tiles) * p.b_kt))
+    return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config<MODE>(clusters, attr, stream);
-  return cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair<MODE>, a, b, p);
+  return cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair<MODE>, a, b, sa, sb, p);
 }
 
 bool device_setup(DeviceInfo** out) {
@@ -1345,6 +1274,8 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p1.timeout_ns = kWaitTimeoutNs;
   p1.a_kt = p1.KT;
   p1.b_kt = p1.KT;
+  p1.a_sf_tiles = static_cast<int>(L.r_pad / BM);
+  p1.b_sf_tiles = static_cast<int>(static_cast<int64_t>(E) * 2 * F / BM);
   p1.gu_out = gu_out;
   // persistent: one CTA per SM (shared memory, registers and TMEM each allow only one)
   if (dev->pair_clusters[0] > 0) {
@@ -1375,6 +1306,8 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p2.timeout_ns = kWaitTimeoutNs;
   p2.a_kt = p2.KT;
   p2.b_kt = p2.KT;
+  p2.a_sf_tiles = static_cast<int>(L.r_pad / BM);
+  p2.b_sf_tiles = static_cast<int>(static_cast<int64_t>(E) * H / BM);
   if (p2.BN == 256 && dev->pair_clusters[1] > 0) {
     const int c2 = static_cast<int>(
         std::min<int64_t>(dev->pair_clusters[1], std::max<int64_t>(1, static_cast<int64_t>(max_mtiles / 2) * p2.NT)));
@@ -1501,6 +1434,8 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   pd.b_kofs = static_cast<int>(H);
   pd.a_kt = static_cast<int>(H / BK);
   pd.b_kt = static_cast<int>(static_cast<int64_t>(E) * H / BK);
+  pd.a_sf_tiles = static_cast<int>(rp / BM);
+  pd.b_sf_tiles = static_cast<int>(F / BM);
   pd.n_fastest = 0;
   pd.gates = gates;
   pd.ldh = F;
@@ -1536,6 +1471,8 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   px.b_kofs = static_cast<int>(2 * F);
   px.a_kt = px.KT;
   px.b_kt = static_cast<int>(static_cast<int64_t>(E) * 2 * F / BK);
+  px.a_sf_tiles = static_cast<int>(rp / BM);
+  px.b_sf_tiles = static_cast<int>(H / BM);
   px.n_fastest = 1;
   px.y = static_cast<uint16_t*>(dx);
   px.ldy = H;
@@ -1555,6 +1492,8 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   pw.wg_m = H;
   pw.wg_n = F;
   pw.wg_m_fastest = 1;   // dy^T (H rows) is the smaller operand: keep it in L2, stream h^T once
+  pw.a_sf_tiles = static_cast<int>(H / BM);
+  pw.b_sf_tiles = static_cast<int>(F / BM);
   pw.dw = dw2;
   if ((st = run_pair<GEMM_WGRAD>(dev, E * pw.wg_mt * pw.wg_nt, mDyT, mHT, pw, stream)) != MXFP8_OK) return st;
   if (!mark(5)) return MXFP8_ERR_CUDA;
@@ -1566,6 +1505,8 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   pw.wg_m = 2 * F;
   pw.wg_n = H;
   pw.wg_m_fastest = 0;   // x^T (H rows) is the smaller operand: keep it in L2, stream dGU^T once
+  pw.a_sf_tiles = static_cast<int>(2 * F / BM);
+  pw.b_sf_tiles = static_cast<int>(H / BM);
   pw.dw = dw1;
   if ((st = run_pair<GEMM_WGRAD>(dev, E * pw.wg_mt * pw.wg_nt, mDguT, mXT, pw, stream)) != MXFP8_OK) return st;
   if (!mark(6)) return MXFP8_ERR_CUDA;
