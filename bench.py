@@ -231,6 +231,45 @@ WORKLOAD_TEXT = {
 }
 
 
+def library_mxfp8_gemms(R, H, F, dev, iters=10):
+    """Context only: cuBLASLt's MXFP8 GEMM (through torch._scaled_mm) on the dense shapes of the two
+    grouped GEMMs (M = routed rows, no expert grouping, bf16 output, no fused epilogue), timed with
+    CUDA events on synthetic E4M3 codes with unit scales.  Nothing of the library's path runs here."""
+    import torch
+    if not hasattr(torch, "float8_e8m0fnu"):
+        return {"unavailable": "this torch has no float8_e8m0fnu"}
+
+    def rup(a, b):
+        return (a + b - 1) // b * b
+
+    out = {"kind": "cuBLASLt MXFP8 (torch._scaled_mm, block scale 1x32, bf16 out)", "note":
+           "dense [M,K]x[K,N] without grouping, routing weight, SwiGLU or requantization"}
+    for name, (M, N, K) in (("grouped_linear1_shape", (R, 2 * F, H)), ("grouped_linear2_shape", (R, H, F))):
+        try:
+            g = torch.Generator(device=dev).manual_seed(3)
+            a = (torch.randn(M, K, device=dev, generator=g) * 0.5).to(torch.float8_e4m3fn)
+            b = (torch.randn(N, K, device=dev, generator=g) * 0.5).to(torch.float8_e4m3fn)
+            sa = torch.full((rup(M, 128) * rup(K // 32, 4),), 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+            sb = torch.full((rup(N, 128) * rup(K // 32, 4),), 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+            run = lambda: torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16)
+            for _ in range(3):
+                run()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(iters):
+                run()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / iters
+            out[name] = {"M": M, "N": N, "K": K, "ms": ms, "tflops": 2 * M * N * K / (ms * 1e-3) / 1e12}
+            del a, b, sa, sb
+        except Exception as ex:   # the library call is context, never a reason to fail the bench
+            out[name] = {"unavailable": repr(ex)[:200]}
+    torch.cuda.empty_cache()
+    return out
+
+
 def workload_config(w):
     return {"workload": f"{WORKLOAD_TEXT[w.name]}: E={w.E} top-{w.topk} T={w.T} (R={w.R} routed rows) "
                         f"H={w.H} F={w.F}, x~N(0,1), W~N(0,0.02)",
@@ -491,6 +530,7 @@ def run_native(args, world, rank, local):
         del xt, out
 
     bwd = measure_backward()
+    lib = library_mxfp8_gemms(R, H, F, dev) if args.only == "all" else None
 
     # ---- end to end through the public API with host buffers ----
     # Every step copies its inputs from pinned host memory and its output back.  Steps are
@@ -566,7 +606,7 @@ def run_native(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
             "config": workload_config(w), "roofline": roofline, "quantize": quant, "moe_layer": layer, "backward": bwd,
-            "e2e": e2e,
+            "e2e": e2e, "library_context": lib,
             "cpu_baseline": cpu, "clocks": clocks, "gpu_launches": 4 * args.steps,
             "weight_quantize_ms": weight_quant_ms, "peaks": {"source": peak_src, **peaks},
         }

@@ -23,15 +23,17 @@
 //
 // Main kernel (k_grouped_gemm_pair, persistent clusters of two CTAs on two SMs, 512 threads each):
 // one tcgen05.mma.cta_group::2 computes a 256 x 256 tile, each CTA loading its own 128 rows of A
-// and half of B (32 KB per K step), 6-stage data ring, 16-slot scale ring running ahead of it;
-// roles and synchronization are described above the kernel.  k_grouped_gemm is the single-CTA
+// and half of B (32 KB per K step) plus the step's scale atoms, 3 stages of two K steps, the
+// scales moved into TMEM by the MMA thread itself (tcgen05.cp); roles and synchronization are
+// described above the kernel.  k_grouped_gemm is the single-CTA
 // kernel (M=128, 4 stages of 48 KB): GroupedLinear 2 uses it when H % 256 != 0, and both forward
 // GEMMs use it where no CTA pair can be co-scheduled.  Its structure:
 //   TMA producer  A tile (128 rows x 128 K bytes), B tile (BN rows x 128) and the 512-byte scale
 //                 atoms of both, all completing on one mbarrier per stage.
 //   scale warps   four warps copy the stage's scale atoms into TMEM with tcgen05.st (one TMEM lane
-//                 quarter each) and signal the MMA issuer; doing this with tcgen05.cp from the
-//                 MMA thread stalled the tensor pipe (about a third of the kernel's time).
+//                 quarter each) and signal the MMA issuer (in this kernel, with one barrier wait
+//                 per 4 MMAs, tcgen05.cp from the MMA thread was slower; the pair kernel, with 8
+//                 MMAs per wait, issues its copies itself).
 //   MMA issuer    allocates TMEM; one thread issues 4 block-scaled MMAs (M=128, N=BN, K=32 each)
 //                 per stage into one fp32 accumulator of BN columns and commits the stage back.
 //   epilogue      eight warps read their 32 TMEM lanes (rows) and half of the columns into
