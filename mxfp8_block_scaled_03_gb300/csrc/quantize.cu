@@ -216,16 +216,22 @@ __global__ void __launch_bounds__(QT_THREADS, (ROW && COL) || GATHER ? 3 : 4) k_
 // the [K, m_out] code matrix, or compact [K, m_out / 32].  GATHER: source rows are the
 // expert-padded row space (as in k_quantize), padding rows are zeros.
 //
-// One CTA of 256 threads owns 128 source rows x 128 source columns: the tile is read with
-// 128-bit loads into shared memory (34 KB with padding), then thread t takes the column pair
-// 2 (t % 64), 2 (t % 64) + 1 and the 32-row block t / 64: it reads 32 packed bf16 pairs down the
-// columns (a warp reads 32 consecutive words of one row: no bank conflicts), takes both columns'
-// amax on the packed pairs, and writes each column's 32 codes as two 16-byte stores.  ROW: the
-// same tile also yields the row-wise MXFP8 of those rows (thread t: row t / 2, 32-column blocks
-// 2 (t % 2) and 2 (t % 2) + 1; tensor-core scale layout), so a tensor needed in both directions is
-// read from memory once.
+// One CTA of 256 threads owns 128 source rows x 128 source columns, read with 128-bit loads into
+// shared memory (34 KB with padding).  Word w (a bf16 pair) of tile row r sits at word
+// w ^ 8 (r / 32): rows 32 apart fall on different banks, so the column pass, whose warps read
+// four 32-row blocks at once, is free of bank conflicts.  Column pass: thread t takes the column
+// pair 2 (t / 4), 2 (t / 4) + 1 and the 32-row block t % 4; it reads 32 packed bf16 pairs down the
+// columns, takes both columns' amax on the packed pairs and writes each column's 32 codes (two
+// 16-byte stores), so the four threads of a column write its 128 codes as one line.  ROW: the same
+// tile also yields the row-wise MXFP8 of those rows (thread t: 32-column block t % 4 of rows t / 4
+// and t / 4 + 64; tensor-core scale layout), four threads writing a row's 128 codes as one line,
+// so a tensor needed in both directions is read from memory once.  (Storing 16 bytes per thread
+// to 32 different rows per warp instruction kept the L1 pipe 80% busy at 62% of HBM bandwidth.)
 constexpr int QTT_ROWS = 128;
 constexpr int QTT_COLS = 128;
+constexpr int QTT_W = QTT_COLS / 2 + 4;   // words per tile row (4 words of padding)
+// word swizzle of tile row r: 8 (r / 32) (multiples of 4 words keep 16-byte chunks whole)
+__device__ __forceinline__ int qtt_swz(int r) { return (r >> 5) << 3; }
 
 struct QuantTArgs {
   const uint16_t* x;
@@ -243,7 +249,7 @@ struct QuantTArgs {
 
 template <bool GATHER, bool ROW>
 __global__ void __launch_bounds__(256, 5) k_quantize_t(const QuantTArgs a) {   // 5 blocks per SM: 48 registers
-  __shared__ __align__(16) uint16_t tile[QTT_ROWS][QTT_COLS + 8];
+  __shared__ __align__(16) uint16_t tile[QTT_ROWS][2 * QTT_W];
   const int tid = threadIdx.x;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * QTT_ROWS;
   const int64_t col0 = static_cast<int64_t>(blockIdx.y) * QTT_COLS;
@@ -267,6 +273,7 @@ __global__ void __launch_bounds__(256, 5) k_quantize_t(const QuantTArgs a) {   /
     }
   }
   nsrc = nsrc < 0 ? 0 : (nsrc > QTT_ROWS ? QTT_ROWS : nsrc);
+  uint32_t* tw = reinterpret_cast<uint32_t*>(&tile[0][0]);   // words, row pitch QTT_W
   // load: 128 rows x 16 chunks of 16 bytes; thread t takes chunk t % 16 of rows t / 16 + 16 j
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -284,18 +291,19 @@ __global__ void __launch_bounds__(256, 5) k_quantize_t(const QuantTArgs a) {   /
       }
       if (src >= 0 && col0 + ch * 8 < a.K) w = __ldcs(reinterpret_cast<const uint4*>(a.x + src * a.K + col0 + ch * 8));
     }
-    *reinterpret_cast<uint4*>(&tile[rr][ch * 8]) = w;
+    *reinterpret_cast<uint4*>(tw + rr * QTT_W + ((4 * ch) ^ qtt_swz(rr))) = w;
   }
   __syncthreads();
   if constexpr (ROW) {
-    const int rr = tid >> 1;
 #pragma unroll
-    for (int b2 = 0; b2 < 2; ++b2) {
-      const int cb = 2 * (tid & 1) + b2;   // 32-column block inside the tile
+    for (int k = 0; k < 2; ++k) {
+      const int rr = tid / 4 + 64 * k;
+      const int cb = tid % 4;   // 32-column block inside the tile
       const int64_t rcol = col0 + cb * 32;
       uint4 w[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint4*>(&tile[rr][cb * 32 + 8 * j]);
+      for (int j = 0; j < 4; ++j)
+        w[j] = *reinterpret_cast<const uint4*>(tw + rr * QTT_W + ((16 * cb + 4 * j) ^ qtt_swz(rr)));
       uint32_t m2 = absmax_bf16x2(absmax_bf16x2(w[0].x, w[0].y), absmax_bf16x2(w[0].z, w[0].w));
 #pragma unroll
       for (int j = 1; j < 4; ++j)
@@ -303,24 +311,25 @@ __global__ void __launch_bounds__(256, 5) k_quantize_t(const QuantTArgs a) {   /
       if (rcol < a.K) {
         const uint32_t sfb = e8m0_from_amax(max_halves(m2));
         const float inv = e8m0_inverse_scale(sfb);
-        uint8_t* dst = a.q_row + (row0 + rr) * a.K + rcol;
         const uint2 q0 = quant8_bf16(w[0], inv), q1 = quant8_bf16(w[1], inv), q2 = quant8_bf16(w[2], inv),
                     q3 = quant8_bf16(w[3], inv);
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
-        reinterpret_cast<uint4*>(dst)[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
+        uint4* dst = reinterpret_cast<uint4*>(a.q_row + (row0 + rr) * a.K + rcol);   // 16-byte aligned
+        dst[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
+        dst[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
         a.sf_row[sf_mma_offset(row0 + rr, rcol >> 5, a.K / 128)] = static_cast<uint8_t>(sfb);
       }
     }
   }
-  const int cp = tid % (QTT_COLS / 2);   // column pair
-  const int rb = tid / (QTT_COLS / 2);   // 32-row block inside the tile
+  const int cp = tid / 4;   // column pair
+  const int rb = tid % 4;   // 32-row block inside the tile
   const int64_t col = col0 + 2 * cp;
   if (col >= a.K) return;
-  uint32_t pk[32];                        // packed bf16 pairs (column col in the low half)
+  uint32_t pk[32];          // packed bf16 pairs (column col in the low half)
   uint32_t m2 = 0;
+  const int wsw = cp ^ (8 * rb);   // the swizzled word of this column pair in rows of block rb
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    pk[i] = *reinterpret_cast<const uint32_t*>(&tile[rb * 32 + i][2 * cp]);
+    pk[i] = tw[(rb * 32 + i) * QTT_W + wsw];
     m2 = absmax_bf16x2(m2, pk[i]);
   }
   const int64_t blk = (row0 >> 5) + rb;
@@ -336,9 +345,9 @@ __global__ void __launch_bounds__(256, 5) k_quantize_t(const QuantTArgs a) {   /
       const float v2 = h ? bf16_hi(a2) : bf16_lo(a2), v3 = h ? bf16_hi(a3) : bf16_lo(a3);
       q[k] = e4m3x2(v0 * inv, v1 * inv) | (e4m3x2(v2 * inv, v3 * inv) << 16);
     }
-    uint8_t* dst = a.qT + (col + h) * a.m_out + row0 + rb * 32;
-    reinterpret_cast<uint4*>(dst)[0] = make_uint4(q[0], q[1], q[2], q[3]);
-    reinterpret_cast<uint4*>(dst)[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    uint4* dst = reinterpret_cast<uint4*>(a.qT + (col + h) * a.m_out + row0 + rb * 32);   // 16-byte aligned
+    dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
     if (a.mma)
       a.sfT[sf_mma_offset(col + h, blk, a.m_out / 128)] = static_cast<uint8_t>(sfb);
     else
