@@ -242,13 +242,9 @@ __device__ __forceinline__ uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t id
   return idesc | (id << 4) | (id << 29);
 }
 
-// Copy one 512-byte scale-factor atom from shared memory to TMEM columns [taddr, taddr+4),
+// tcgen05.cp of one 512-byte scale-factor atom from shared memory to TMEM columns [taddr, taddr+4),
 // replicated into all four 32-lane quarters (lane i, column j holds the 4 bytes of atom row i,
 // word j).
-__device__ __forceinline__ void tc_copy_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // Pair form: issued by the leader CTA, each CTA of the pair copies the atom at this shared-memory
 // address of its own into the same TMEM columns of its own.
 __device__ __forceinline__ void tc_copy_sf_pair(uint32_t taddr, uint64_t sdesc) {
