@@ -375,14 +375,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
       }
     }
     p.dgate_part[prow * (F / 128) + f0 / 128] = part;
-  } else if (MODE == GEMM_WGRAD) {
-    // v = 128 fp32 gradient entries of row a_row + r, columns n*256 + 128*half ..
-    if (t.n * 256 + 128 * half >= p.wg_n) return;   // half of the last column tile past N
-    float* drow = p.dw + (static_cast<int64_t>(t.e) * p.wg_m + t.a_row + r) * p.wg_n + t.n * 256 + 128 * half;
-#pragma unroll
-    for (int c = 0; c < 128; c += 8)
-      st_global_32B_cs(drow + c, make_uint4(v[c], v[c + 1], v[c + 2], v[c + 3]),
-                       make_uint4(v[c + 4], v[c + 5], v[c + 6], v[c + 7]));
   } else {
     if (r < t.valid) {
       const int ncols = BN / 2;
@@ -684,7 +676,12 @@ constexpr int P_SUBBUF_BYTES = P_STEP_BYTES + 2048;           // tiles, scale at
 constexpr int P_STAGE_BYTES = P_SUB * P_SUBBUF_BYTES;
 constexpr int P_SF_SLOTS = P_STAGES * P_SUB;                  // one TMEM scale slot per sub-buffer
 constexpr int P_DATA_BYTES = P_STAGES * P_STAGE_BYTES;
-constexpr int P_BAR_OFFSET = P_DATA_BYTES;
+// GEMM_WGRAD epilogue: each epilogue warp stages its 32 rows x 8 fp32 columns in one of two 1 KB
+// buffers (32-byte rows, 32B swizzle) that a TMA store then writes out
+constexpr int P_WG_CHUNK = 8;                                  // fp32 columns per TMA store
+constexpr int P_WG_BUF_BYTES = 32 * P_WG_CHUNK * 4;            // 1 KB
+constexpr int P_EPI_BYTES = NUM_EPI_WARPS * 2 * P_WG_BUF_BYTES;
+constexpr int P_BAR_OFFSET = P_DATA_BYTES + P_EPI_BYTES;
 constexpr int P_NUM_BARS = 2 * P_STAGES + 3;
 constexpr int P_SMEM_BYTES = P_BAR_OFFSET + P_NUM_BARS * 8 + 8 + 1024;
 constexpr uint32_t P_SFA_COL = 256;                           // 4 columns per slot
@@ -811,7 +808,7 @@ template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                        const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_BAR_OFFSET);
@@ -1034,8 +1031,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(leader_acc_empty);   // the leader may overwrite TMEM
       acc_phase ^= 1u;
-      epilogue_tile<MODE>(p, t, v, r, half, 256);
+      if constexpr (MODE == GEMM_WGRAD) {
+        // 128 fp32 columns of this warp's 32 rows, 8 columns per TMA store from a double-buffered
+        // 1 KB staging area: a warp instruction writes 512 contiguous bytes of shared memory, where
+        // row-per-lane global stores touched 32 rows per instruction and held the epilogue up.
+        if (t.n * 256 + 128 * half < p.wg_n) {
+          const int col0 = t.n * 256 + 128 * half;
+          const int grow = t.e * p.wg_m + t.a_row + quarter * 32;   // row in the [E * wg_m, wg_n] view
+          uint8_t* wbuf = smem + P_DATA_BYTES + (warp - FIRST_EPI_WARP) * 2 * P_WG_BUF_BYTES;
+#pragma unroll
+          for (int c = 0; c < 128; c += P_WG_CHUNK) {
+            uint8_t* buf = wbuf + ((c / P_WG_CHUNK) & 1) * P_WG_BUF_BYTES;
+            if (lane == 0) bulk_wait_read_le1();   // the store that last used this buffer has read it
+            __syncwarp();
+            // row `lane`: two 16-byte chunks, 32B swizzle (chunk j of row i at j ^ ((i >> 2) & 1))
+            const int sw = (lane >> 2) & 1;
+            *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * sw) = make_uint4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+            *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * (sw ^ 1)) =
+                make_uint4(v[c + 4], v[c + 5], v[c + 6], v[c + 7]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, buf, col0 + c, grow);
+              bulk_commit_group();
+            }
+          }
+        }
+      } else {
+        epilogue_tile<MODE>(p, t, v, r, half, 256);
+      }
     }
+    if (MODE == GEMM_WGRAD && lane == 0) bulk_wait_all();   // stores complete before the CTA exits
   }
 
   tc_fence_before();
@@ -1141,6 +1167,20 @@ bool make_sf_map(CUtensorMap* m, const void* base, uint64_t atoms) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The fp32 weight gradient [E * wg_m, wg_n] as the target of TMA stores: boxes of 32 rows x 8
+// columns (32-byte rows, 32B swizzle), matching the epilogue's staging buffers.
+bool make_dw_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  auto enc = tensor_map_encoder();
+  if (!enc || rows == 0 || cols == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(P_WG_CHUNK), 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct DeviceInfo {
   int sms = 0;
   int pair_clusters[4] = {0, 0, 0, 0};   // co-resident CTA pairs of each pair-kernel mode (0: none)
@@ -1180,13 +1220,15 @@ int max_pair_clusters() {
 template <int MODE>
 cudaError_t launch_pair(int clusters, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                         cudaStream_t stream) {
-  CUtensorMap sa, sb;
+  CUtensorMap sa, sb, d = a;   // d: the weight-gradient output (other modes do not use it)
   if (!make_sf_map(&sa, p.a_sf, static_cast<uint64_t>(p.a_sf_tiles) * p.a_kt) ||
       !make_sf_map(&sb, p.b_sf, static_cast<uint64_t>(p.b_sf_tiles) * p.b_kt))
     return cudaErrorInvalidValue;
+  if (MODE == GEMM_WGRAD && !make_dw_map(&d, p.dw, static_cast<uint64_t>(p.E) * p.wg_m, p.wg_n))
+    return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config<MODE>(clusters, attr, stream);
-  return cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair<MODE>, a, b, sa, sb, p);
+  return cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair<MODE>, a, b, sa, sb, d, p);
 }
 
 bool device_setup(DeviceInfo** out) {
