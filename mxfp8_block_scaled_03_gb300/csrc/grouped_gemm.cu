@@ -655,16 +655,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //   full[s]      (leader)  both CTAs' tile copies complete on the leader's barrier (.cta_group::2
 //                          copies); the leader's producer posts the byte count of both halves
 //   empty[s]     (both)    the leader's MMA commit, multicast to both CTAs
+// and the accumulator hand-off:
+//   acc_full     (both)    the tile's MMAs completed (leader's commit, multicast)
+//   acc_empty    (leader)  both CTAs' epilogues read their accumulator out (16 warp arrivals)
 // The block scales of a K step (this CTA's A atom and both B atoms, 3 x 512 bytes) travel in the
 // same stage as its tiles, by TMA onto the same barrier.  The MMA thread copies them into TMEM with
 // tcgen05.cp just before the step's MMAs: copies and MMAs issued by one thread run in order, so no
 // other warp and no other barrier takes part.  A TMEM scale slot belongs to one sub-buffer of the
 // ring and is rewritten only after the stage's empty barrier, i.e. after the MMAs that read it.
-// (A version with a separate 16-slot scale ring filled by four tcgen05.st warps and one more
-// producer was 17% slower on GroupedLinear 1: its barriers sat on the path of every stage.)
-// and the accumulator hand-off:
-//   acc_full     (both)    the tile's MMAs completed (leader's commit, multicast)
-//   acc_empty    (leader)  both CTAs' epilogues read their accumulator out (16 warp arrivals)
+// (A separate 16-slot scale ring, filled by four tcgen05.st warps and a second producer and
+// synchronized by three more barrier kinds, was about 3% slower on GroupedLinear 1.)
 // Warp roles: warp 4 producer (both CTAs), warp 5 MMA issuer (leader CTA; the MMA warp of the
 // second CTA only takes part in the TMEM allocation), warps 8-15 epilogue; the other role warps idle.
 // ---------------------------------------------------------------------------------------------
