@@ -948,7 +948,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!pair_lane_wait(acc_empty, acc_phase ^ 1u, true, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) break;
           tc_fence_after();
           for (int kb = 0; kb < steps; kb += P_SUB) {
-            // full implies the stage's scales are staged (the leader's producer waited for them)
+            // full: the stage's tiles and scale atoms are in both CTAs' shared memory
             if (!pair_lane_wait(&full[stage], phase, false, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) {
               ok = false;
               break;
