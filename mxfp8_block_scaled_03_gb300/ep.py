@@ -1,0 +1,136 @@
+"""Expert parallelism for the MoE layer around the fused MXFP8 expert MLP.
+
+Each rank of a process group owns E / world consecutive experts (rank r: experts
+r * E_loc .. (r + 1) * E_loc - 1) and holds only their quantized weights; tokens travel to the
+ranks that own their experts and their outputs travel back (page "Efficient MoE training for
+biological foundation models", How to run the recipe: the Mixtral-8x7B configuration spreads its
+experts over eight GPUs, with the data- and expert-parallel sizes multiplying to the GPU count;
+Key technical approaches item 1: tokens are gathered per expert and counted by split_sizes).
+All ranks pass routing weights, or none does.
+
+One forward, on every rank of the group:
+  1. ``moe_permute`` of the rank's own (token, slot) choices over all E experts.  Because rank
+     r's experts are consecutive ids, the sorted rows bound for one rank are one contiguous run.
+  2. The per-expert counts travel with one all-to-all ([world, E_loc] int32 each way); their row
+     sums become host split sizes (the one host synchronization of the layer: an all-to-all of
+     variable sizes needs them on the host).
+  3. The sorted token rows (gathered from x_tokens by ``moe_combine`` over one slot, an exact
+     copy) and their routing weights go to their owners with one all-to-all each.
+  4. The owner receives, from each source in turn, rows sorted by its local experts.  A stable
+     ``moe_permute`` of the received rows by local expert (one slot each) gives the expert-major
+     order, the local split sizes and the routing weights in that order; the fused forward
+     (``grouped_mlp_fwd_tokens``) gathers the rows in that order inside its activation quantize.
+  5. ``moe_combine`` over one slot puts the outputs back in the order received, one all-to-all
+     returns them to their sources, and ``moe_combine`` over the k slots sums each token's expert
+     outputs (the routing weight was applied inside ScaledSwiGLU).
+
+Every step that touches the rows runs in the library's kernels; the host only computes the
+local expert id of each received row from the exchanged counts (world * E_loc numbers).  With
+one rank the exchanges are copies and the result equals the single-GPU MoE layer bit for bit.
+
+The compute steps are reached through an ``ops`` object so that the exchange logic can be run
+with other implementations of the same four operations (``KernelOps`` is the library's).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+class KernelOps:
+    """The four compute steps of the layer on the library's CUDA kernels; expert outputs are
+    bf16 (``y_dtype``)."""
+
+    def __init__(self, mx=None):
+        import torch
+        if mx is None:
+            import mxfp8_block_scaled_03_gb300 as mx
+        self.mx = mx
+        self.y_dtype = torch.bfloat16
+
+    def permute(self, experts, gates, E: int):
+        split, row_of_slot, token_of_row, gates_sorted, _ = self.mx.moe_permute(experts, gates, E)
+        return split, row_of_slot, token_of_row, gates_sorted
+
+    def gather_rows(self, x, index):
+        return self.mx.moe_combine(x, index.view(-1, 1))
+
+    def expert_mlp(self, x_rows, token_of_row, split, gates_sorted, weights):
+        return self.mx.grouped_mlp_fwd_tokens(x_rows, token_of_row, split, gates_sorted, *weights)
+
+    def combine(self, y_rows, row_of_slot):
+        return self.mx.moe_combine(y_rows, row_of_slot)
+
+
+def _exchange(out, inp, out_splits, in_splits, group):
+    """all_to_all_single along dim 0; 16-bit rows travel as bytes (the exchange is a copy, and
+    not every backend moves 16-bit integers)."""
+    import torch
+    import torch.distributed as dist
+    if inp.element_size() == 2:
+        out, inp = out.view(torch.uint8), inp.view(torch.uint8)
+    dist.all_to_all_single(out, inp, out_splits, in_splits, group=group)
+
+
+def local_experts_of_received_rows(recv_split: np.ndarray) -> np.ndarray:
+    """Local expert id of every received row, in the order received: the rows from source s
+    come after those of sources 0 .. s-1, sorted by local expert, recv_split[s, e] of expert e."""
+    rs = np.asarray(recv_split, dtype=np.int64)
+    world, E_loc = rs.shape
+    parts = [np.repeat(np.arange(E_loc, dtype=np.int32), rs[s]) for s in range(world)]
+    return np.concatenate(parts) if parts else np.zeros(0, dtype=np.int32)
+
+
+def ep_moe_forward(x_tokens, experts, gates, weights, E: int, group=None, ops=None):
+    """MoE layer forward with the experts spread over the ranks of ``group``.
+
+    x_tokens [T, H] (this rank's tokens), experts int32 [T, k] (global expert ids in [0, E)),
+    gates float32 [T, k] or None, weights = (w1_q, w1_sf, w2_q, w2_sf) of this rank's E / world
+    experts (the layout ``grouped_mlp_fwd`` takes).  E must be a multiple of the group size.
+    Returns out [T, H]: out[t] = sum over t's k slots of expert(slot)(x[t]) scaled by its gate.
+    """
+    import torch
+    import torch.distributed as dist
+
+    ops = ops or KernelOps()
+    world = dist.get_world_size(group)
+    if E % world != 0:
+        raise ValueError(f"{E} experts do not divide over {world} ranks")
+    E_loc = E // world
+    T, k = experts.shape
+    H = x_tokens.shape[1]
+    dev = x_tokens.device
+
+    # 1. sort this rank's choices by expert: the rows bound for rank r are one run
+    split, row_of_slot, token_of_row, gates_sorted = ops.permute(experts, gates, E)
+
+    # 2. per-expert counts both ways, row counts on the host
+    send_split = split.view(world, E_loc).contiguous()
+    recv_split = torch.empty_like(send_split)
+    dist.all_to_all_single(recv_split, send_split, group=group)
+    recv_split_h = recv_split.cpu().numpy()
+    send_counts = send_split.sum(1).cpu().tolist()
+    recv_counts = [int(c) for c in recv_split_h.sum(1)]
+    R_recv = sum(recv_counts)
+
+    # 3. rows and routing weights to their owners
+    x_send = ops.gather_rows(x_tokens, token_of_row)
+    x_recv = torch.empty((R_recv, H), dtype=x_send.dtype, device=dev)
+    _exchange(x_recv, x_send, recv_counts, send_counts, group)
+    g_recv = None
+    if gates_sorted is not None:
+        g_recv = torch.empty(R_recv, dtype=gates_sorted.dtype, device=dev)
+        _exchange(g_recv, gates_sorted, recv_counts, send_counts, group)
+
+    # 4. the owner's experts over the received rows, grouped expert-major
+    if R_recv > 0:
+        local_e = torch.from_numpy(local_experts_of_received_rows(recv_split_h)).to(dev)
+        split_l, ros_l, tor_l, gs_l = ops.permute(local_e.view(-1, 1),
+                                                 None if g_recv is None else g_recv.view(-1, 1), E_loc)
+        y_sorted = ops.expert_mlp(x_recv, tor_l, split_l, gs_l, weights)
+        # 5. outputs back in the order received, then home
+        y_recv = ops.combine(y_sorted, ros_l)
+    else:
+        y_recv = torch.empty((0, H), dtype=ops.y_dtype, device=dev)
+    y_ret = torch.empty((T * k, H), dtype=ops.y_dtype, device=dev)
+    _exchange(y_ret, y_recv, send_counts, recv_counts, group)
+    return ops.combine(y_ret, row_of_slot)
