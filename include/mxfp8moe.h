@@ -163,6 +163,17 @@ int grouped_mlp_fwd_tokens(const void* x_tokens, int64_t T, const int32_t* token
 int moe_combine(const void* y_rows, const int32_t* row_of_slot, int64_t T, int k, int64_t H, void* out,
                 void* stream);
 
+/*
+ * moe_gather_rows -- dst[i] = src[index[i]] for i < n: rows of row_bytes bytes, copied bit for
+ * bit whatever their element type (token rows to the ranks that own their experts and back,
+ * routing-weight gradients to (token, slot) order).  src (device) [nsrc rows], index (device)
+ * int32 [n], dst (device, out) [n rows], fully overwritten; a row whose index lies outside
+ * [0, nsrc) is written as zeros.  Requirements: row_bytes % 4 == 0, 4-byte aligned pointers
+ * (16-byte rows on 16-byte aligned pointers move as 16-byte words).  n == 0 is a no-op.
+ */
+int moe_gather_rows(const void* src, int64_t nsrc, int64_t row_bytes, const int32_t* index, int64_t n, void* dst,
+                    void* stream);
+
 /* grouped_mlp_fwd with per-kernel timing: identical work and results, and additionally records
  * the 5 caller-created CUDA events stage_events[0..4] (cudaEvent_t as void*, host array) on
  * `stream` before the schedule, activation-quantize, GroupedLinear-1 (+ScaledSwiGLU, requant)
@@ -255,7 +266,7 @@ int grouped_mlp_bwd_timed(const void* x_sorted, int64_t R, int64_t H, int64_t F,
  * sorted row r reads row token_of_row[r] of x_tokens [T, H] and of d_out_tokens [T, H].  That
  * gather is the gradient of moe_combine; the caller finishes the layer's backward with
  * moe_combine(dx_rows, row_of_slot) (the gradient of the token gather) and picks
- * dgates_sorted[row_of_slot[t, j]] for the routing weight of (t, j).  Other arguments, outputs
+ * dgates_sorted[row_of_slot[t, j]] for the routing weight of (t, j) (moe_gather_rows).  Other arguments, outputs
  * and errors as grouped_mlp_fwd_train / grouped_mlp_bwd (dx_rows and dgates_sorted in sorted-row
  * order); token ids outside [0, T) read zero rows and set MXFP8_ERR_INVALID_ARG in the workspace
  * error word. */

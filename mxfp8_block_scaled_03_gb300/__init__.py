@@ -22,13 +22,15 @@ import ctypes
 import os
 import threading
 
+import numpy as np
+
 from . import build_ext
 
 __all__ = [
     "MXFP8Error", "ROWWISE", "COLWISE", "SF_COMPACT", "SF_MMA", "lib", "library_path",
     "mxfp8_sf_bytes", "mxfp8_quantize", "grouped_mlp_workspace_size", "grouped_mlp_workspace_layout",
     "grouped_mlp_fwd", "grouped_mlp_fwd_noalloc", "grouped_mlp_fwd_tokens", "moe_permute",
-    "moe_permute_workspace_size", "moe_combine", "mxfp8_check_device_error", "mxfp8_quantize_colwise_t",
+    "moe_permute_workspace_size", "moe_combine", "moe_gather_rows", "mxfp8_check_device_error", "mxfp8_quantize_colwise_t",
     "grouped_mlp_saved_bytes", "grouped_mlp_fwd_train", "grouped_mlp_bwd_workspace_size", "grouped_mlp_bwd",
     "grouped_mlp_fwd_tokens_train", "grouped_mlp_bwd_tokens", "mxfp8_status_string", "mxfp8_abi_version",
 ]
@@ -108,6 +110,8 @@ def lib() -> ctypes.CDLL:
             L.moe_permute.argtypes = [P, P, i64, i32, i32, P, P, P, P, P, sz, P]
             L.moe_combine.restype = i32
             L.moe_combine.argtypes = [P, P, i64, i32, i64, P, P]
+            L.moe_gather_rows.restype = i32
+            L.moe_gather_rows.argtypes = [P, i64, i64, P, i64, P, P]
             L.mxfp8_check_device_error.restype = i32
             L.mxfp8_check_device_error.argtypes = [P, P, P]
             _lib = L
@@ -423,6 +427,20 @@ def moe_combine(y_rows, row_of_slot, out=None, stream=None):
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=y_rows.device)
     _check(lib().moe_combine(_ptr(y_rows), _ptr(row_of_slot), T, k, H, _ptr(out), _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_gather_rows(src, index, out=None, stream=None):
+    """out[i] = src[index[i]] (rows copied bit for bit; rows of an index outside [0, len(src)) are
+    zeros).  src [N, ...] (rows of a multiple of 4 bytes), index int32 [n]."""
+    import torch
+    n = int(index.numel())
+    row_shape = tuple(src.shape[1:])
+    if out is None:
+        out = torch.empty((n,) + row_shape, dtype=src.dtype, device=src.device)
+    row_bytes = src.element_size() * (int(np.prod(row_shape)) if row_shape else 1)
+    _check(lib().moe_gather_rows(_ptr(src), int(src.shape[0]), row_bytes, _ptr(index), n, _ptr(out), _stream(stream)),
+           "moe_gather_rows")
     return out
 
 

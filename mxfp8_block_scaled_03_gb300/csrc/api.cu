@@ -181,6 +181,20 @@ int moe_combine(const void* y_rows, const int32_t* row_of_slot, int64_t T, int k
   return e == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
 }
 
+int moe_gather_rows(const void* src, int64_t nsrc, int64_t row_bytes, const int32_t* index, int64_t n, void* dst,
+                    void* stream) {
+  if (nsrc < 0 || n < 0 || row_bytes <= 0 || row_bytes % 4 != 0) return MXFP8_ERR_INVALID_ARG;
+  if (n == 0) return MXFP8_OK;
+  if (index == nullptr || dst == nullptr || (nsrc > 0 && src == nullptr)) return MXFP8_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(src) & 3u) != 0 || (reinterpret_cast<uintptr_t>(dst) & 3u) != 0)
+    return MXFP8_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MXFP8_ERR_CUDA;
+  const cudaError_t e = launch_gather_rows(src, nsrc, row_bytes, index, n, dst, sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXFP8_OK : MXFP8_ERR_CUDA;
+}
+
 size_t grouped_mlp_saved_bytes(int64_t R, int64_t H, int64_t F, int E) {
   WsLayout L;
   if (!ws_layout(R, H, F, E, &L)) return 0;

@@ -18,6 +18,9 @@
 // writes them back as bf16 with one 16-byte store.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstdint>
+
 #include "mx_device.cuh"
 #include "mx_internal.h"
 #include "mxfp8moe.h"
@@ -130,7 +133,46 @@ __global__ void __launch_bounds__(COMBINE_THREADS) k_combine(const uint16_t* y, 
   __stcs(reinterpret_cast<uint4*>(out + t * H + col), o);
 }
 
+// dst[i, :] = src[index[i], :] for rows of `words` 32-bit words (zeros where index[i] is outside
+// [0, nsrc)); a pure copy, so any element type travels bit for bit.  One thread per 16 bytes
+// when rows are whole 16-byte chunks, else per word.
+template <bool VEC>
+__global__ void __launch_bounds__(256) k_gather_rows(const uint32_t* src, int64_t nsrc, int64_t words,
+                                                     const int32_t* index, int64_t n, uint32_t* dst) {
+  const int64_t per_row = VEC ? words / 4 : words;
+  const int64_t total = n * per_row;
+  for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < total;
+       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = q / per_row, c = q - i * per_row;
+    const int64_t r = __ldg(index + i);
+    const bool in = r >= 0 && r < nsrc;
+    if (VEC) {
+      const uint4 v = in ? __ldg(reinterpret_cast<const uint4*>(src + r * words) + c) : make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(dst + i * words)[c] = v;
+    } else {
+      dst[i * words + c] = in ? __ldg(src + r * words + c) : 0u;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(const void* src, int64_t nsrc, int64_t row_bytes, const int32_t* index, int64_t n,
+                               void* dst, int sms, cudaStream_t stream) {
+  const int64_t words = row_bytes / 4;
+  const bool vec = row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+  const int64_t items = n * (vec ? words / 4 : words);
+  const int64_t blocks = std::min<int64_t>((items + 255) / 256, static_cast<int64_t>(sms) * 8);
+  if (blocks <= 0) return cudaSuccess;
+  if (vec)
+    k_gather_rows<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<const uint32_t*>(src), nsrc,
+                                                                           words, index, n, static_cast<uint32_t*>(dst));
+  else
+    k_gather_rows<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<const uint32_t*>(src), nsrc,
+                                                                            words, index, n, static_cast<uint32_t*>(dst));
+  return cudaGetLastError();
+}
 
 size_t permute_workspace_bytes(int64_t n, int E) {
   const int64_t nchunks = (n + PERMUTE_CHUNK - 1) / PERMUTE_CHUNK;

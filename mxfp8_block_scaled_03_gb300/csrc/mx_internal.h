@@ -80,6 +80,8 @@ size_t permute_workspace_bytes(int64_t n, int E);
 cudaError_t launch_permute(const int32_t* experts, const float* gates, int64_t T, int k, int E, int32_t* split_sizes,
                            int32_t* row_of_slot, int32_t* token_of_row, float* gates_sorted, void* workspace,
                            cudaStream_t stream);
+cudaError_t launch_gather_rows(const void* src, int64_t nsrc, int64_t row_bytes, const int32_t* index, int64_t n,
+                               void* dst, int sms, cudaStream_t stream);
 cudaError_t launch_combine(const void* y, const int32_t* row_of_slot, int64_t T, int k, int64_t H, void* out,
                            cudaStream_t stream);
 

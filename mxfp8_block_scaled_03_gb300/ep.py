@@ -14,22 +14,30 @@ One forward, on every rank of the group:
   2. The per-expert counts travel with one all-to-all ([world, E_loc] int32 each way); their row
      sums become host split sizes (the one host synchronization of the layer: an all-to-all of
      variable sizes needs them on the host).
-  3. The sorted token rows (gathered from x_tokens by ``moe_combine`` over one slot, an exact
-     copy) and their routing weights go to their owners with one all-to-all each.
+  3. The sorted token rows (gathered from x_tokens by ``moe_gather_rows``) and their routing
+     weights go to their owners with one all-to-all each.
   4. The owner receives, from each source in turn, rows sorted by its local experts.  A stable
      ``moe_permute`` of the received rows by local expert (one slot each) gives the expert-major
      order, the local split sizes and the routing weights in that order; the fused forward
      (``grouped_mlp_fwd_tokens``) gathers the rows in that order inside its activation quantize.
-  5. ``moe_combine`` over one slot puts the outputs back in the order received, one all-to-all
-     returns them to their sources, and ``moe_combine`` over the k slots sums each token's expert
-     outputs (the routing weight was applied inside ScaledSwiGLU).
+  5. ``moe_gather_rows`` puts the outputs back in the order received, one all-to-all returns
+     them to their sources, and ``moe_combine`` sums each token's k expert outputs (the routing
+     weight was applied inside ScaledSwiGLU).
+
+Training (``ep_moe_forward_train`` / ``ep_moe_backward``): the forward also saves the owner's
+pre-activations and the routing of the call; the backward sends each sorted row's output
+gradient (its token's row of d_out: the gradient of the combine) to the owner in the same way,
+runs ``grouped_mlp_bwd_tokens`` there (this rank's experts' weight gradients stay on the rank),
+and returns dx rows and routing-weight gradients along the forward's path in reverse; each
+source sums its tokens' k dx rows (``moe_combine``, the gradient of the token gather) and picks
+the routing-weight gradient of each (token, slot).
 
 Every step that touches the rows runs in the library's kernels; the host only computes the
 local expert id of each received row from the exchanged counts (world * E_loc numbers).  With
-one rank the exchanges are copies and the result equals the single-GPU MoE layer bit for bit.
+one rank the exchanges are copies and the results equal the single-GPU MoE layer bit for bit.
 
 The compute steps are reached through an ``ops`` object so that the exchange logic can be run
-with other implementations of the same four operations (``KernelOps`` is the library's).
+with other implementations of the same operations (``KernelOps`` is the library's).
 """
 from __future__ import annotations
 
@@ -37,8 +45,8 @@ import numpy as np
 
 
 class KernelOps:
-    """The four compute steps of the layer on the library's CUDA kernels; expert outputs are
-    bf16 (``y_dtype``)."""
+    """The compute steps of the layer on the library's CUDA kernels; expert outputs and input
+    gradients are bf16 (``y_dtype``)."""
 
     def __init__(self, mx=None):
         import torch
@@ -46,16 +54,25 @@ class KernelOps:
             import mxfp8_block_scaled_03_gb300 as mx
         self.mx = mx
         self.y_dtype = torch.bfloat16
+        self.dg_dtype = torch.float32
 
     def permute(self, experts, gates, E: int):
         split, row_of_slot, token_of_row, gates_sorted, _ = self.mx.moe_permute(experts, gates, E)
         return split, row_of_slot, token_of_row, gates_sorted
 
     def gather_rows(self, x, index):
-        return self.mx.moe_combine(x, index.view(-1, 1))
+        return self.mx.moe_gather_rows(x, index.reshape(-1))
 
     def expert_mlp(self, x_rows, token_of_row, split, gates_sorted, weights):
         return self.mx.grouped_mlp_fwd_tokens(x_rows, token_of_row, split, gates_sorted, *weights)
+
+    def expert_mlp_train(self, x_rows, token_of_row, split, gates_sorted, weights):
+        return self.mx.grouped_mlp_fwd_tokens_train(x_rows, token_of_row, split, gates_sorted, *weights)
+
+    def expert_mlp_bwd(self, x_rows, token_of_row, split, gates_sorted, saved, weights_t, dy_rows):
+        dx, dg, dw1, dw2, _ = self.mx.grouped_mlp_bwd_tokens(x_rows, token_of_row, split, gates_sorted, saved,
+                                                             *weights_t, dy_rows)
+        return dx, dg, dw1, dw2
 
     def combine(self, y_rows, row_of_slot):
         return self.mx.moe_combine(y_rows, row_of_slot)
@@ -80,18 +97,21 @@ def local_experts_of_received_rows(recv_split: np.ndarray) -> np.ndarray:
     return np.concatenate(parts) if parts else np.zeros(0, dtype=np.int32)
 
 
-def ep_moe_forward(x_tokens, experts, gates, weights, E: int, group=None, ops=None):
-    """MoE layer forward with the experts spread over the ranks of ``group``.
+class EpContext:
+    """What the backward needs from a training forward: the routing of this rank's choices and
+    of the rows it received, the exchange sizes, the received rows and the saved
+    pre-activations of this rank's experts."""
 
-    x_tokens [T, H] (this rank's tokens), experts int32 [T, k] (global expert ids in [0, E)),
-    gates float32 [T, k] or None, weights = (w1_q, w1_sf, w2_q, w2_sf) of this rank's E / world
-    experts (the layout ``grouped_mlp_fwd`` takes).  E must be a multiple of the group size.
-    Returns out [T, H]: out[t] = sum over t's k slots of expert(slot)(x[t]) scaled by its gate.
-    """
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+
+def _dispatch(x_tokens, experts, gates, E, group, ops):
+    """Steps 1-3: sort this rank's choices, exchange counts, rows and routing weights, and sort
+    the received rows by local expert.  Returns a context (without the forward's outputs)."""
     import torch
     import torch.distributed as dist
 
-    ops = ops or KernelOps()
     world = dist.get_world_size(group)
     if E % world != 0:
         raise ValueError(f"{E} experts do not divide over {world} ranks")
@@ -108,7 +128,7 @@ def ep_moe_forward(x_tokens, experts, gates, weights, E: int, group=None, ops=No
     recv_split = torch.empty_like(send_split)
     dist.all_to_all_single(recv_split, send_split, group=group)
     recv_split_h = recv_split.cpu().numpy()
-    send_counts = send_split.sum(1).cpu().tolist()
+    send_counts = [int(c) for c in send_split.sum(1).cpu().tolist()]
     recv_counts = [int(c) for c in recv_split_h.sum(1)]
     R_recv = sum(recv_counts)
 
@@ -121,16 +141,81 @@ def ep_moe_forward(x_tokens, experts, gates, weights, E: int, group=None, ops=No
         g_recv = torch.empty(R_recv, dtype=gates_sorted.dtype, device=dev)
         _exchange(g_recv, gates_sorted, recv_counts, send_counts, group)
 
-    # 4. the owner's experts over the received rows, grouped expert-major
+    # the received rows in expert-major order (stable: sources stay in order)
+    split_l = ros_l = tor_l = gs_l = None
     if R_recv > 0:
         local_e = torch.from_numpy(local_experts_of_received_rows(recv_split_h)).to(dev)
         split_l, ros_l, tor_l, gs_l = ops.permute(local_e.view(-1, 1),
                                                  None if g_recv is None else g_recv.view(-1, 1), E_loc)
-        y_sorted = ops.expert_mlp(x_recv, tor_l, split_l, gs_l, weights)
-        # 5. outputs back in the order received, then home
-        y_recv = ops.combine(y_sorted, ros_l)
+    return EpContext(T=T, k=k, H=H, dev=dev, row_of_slot=row_of_slot, token_of_row=token_of_row,
+                     send_counts=send_counts, recv_counts=recv_counts, R_recv=R_recv, x_recv=x_recv,
+                     with_gates=gates_sorted is not None, split_l=split_l, ros_l=ros_l, tor_l=tor_l, gs_l=gs_l,
+                     saved=None)
+
+
+def _return_rows(rows_sorted, ctx, group, ops, dtype, width):
+    """Rows computed by the owner in expert-major order -> back to their sources, in each
+    source's sorted order (steps 4-5 of the forward, and the backward's way home)."""
+    import torch
+    if ctx.R_recv > 0:
+        back = ops.gather_rows(rows_sorted, ctx.ros_l)
     else:
-        y_recv = torch.empty((0, H), dtype=ops.y_dtype, device=dev)
-    y_ret = torch.empty((T * k, H), dtype=ops.y_dtype, device=dev)
-    _exchange(y_ret, y_recv, send_counts, recv_counts, group)
-    return ops.combine(y_ret, row_of_slot)
+        back = torch.empty((0,) + width, dtype=dtype, device=ctx.dev)
+    ret = torch.empty((ctx.T * ctx.k,) + width, dtype=dtype, device=ctx.dev)
+    _exchange(ret, back, ctx.send_counts, ctx.recv_counts, group)
+    return ret
+
+
+def ep_moe_forward(x_tokens, experts, gates, weights, E: int, group=None, ops=None):
+    """MoE layer forward with the experts spread over the ranks of ``group``.
+
+    x_tokens [T, H] (this rank's tokens), experts int32 [T, k] (global expert ids in [0, E)),
+    gates float32 [T, k] or None, weights = (w1_q, w1_sf, w2_q, w2_sf) of this rank's E / world
+    experts (the layout ``grouped_mlp_fwd`` takes).  E must be a multiple of the group size.
+    Returns out [T, H]: out[t] = sum over t's k slots of expert(slot)(x[t]) scaled by its gate.
+    """
+    ops = ops or KernelOps()
+    ctx = _dispatch(x_tokens, experts, gates, E, group, ops)
+    y_sorted = None
+    if ctx.R_recv > 0:
+        y_sorted = ops.expert_mlp(ctx.x_recv, ctx.tor_l, ctx.split_l, ctx.gs_l, weights)
+    y_ret = _return_rows(y_sorted, ctx, group, ops, ops.y_dtype, (ctx.H,))
+    return ops.combine(y_ret, ctx.row_of_slot)
+
+
+def ep_moe_forward_train(x_tokens, experts, gates, weights, E: int, group=None, ops=None):
+    """ep_moe_forward that also keeps what ep_moe_backward needs.  Returns (out, ctx)."""
+    ops = ops or KernelOps()
+    ctx = _dispatch(x_tokens, experts, gates, E, group, ops)
+    y_sorted = None
+    if ctx.R_recv > 0:
+        y_sorted, ctx.saved = ops.expert_mlp_train(ctx.x_recv, ctx.tor_l, ctx.split_l, ctx.gs_l, weights)
+    y_ret = _return_rows(y_sorted, ctx, group, ops, ops.y_dtype, (ctx.H,))
+    return ops.combine(y_ret, ctx.row_of_slot), ctx
+
+
+def ep_moe_backward(d_out, ctx, weights_t, group=None, ops=None):
+    """Backward of ep_moe_forward_train.
+
+    d_out [T, H] (gradient of this rank's output rows), ctx from the forward, weights_t =
+    (w1t_q, w1t_sf, w2t_q, w2t_sf) of this rank's experts quantized along their other axis (the
+    layout ``grouped_mlp_bwd`` takes).  Returns (dx [T, H], dgates [T, k] or None, dW1, dW2), the
+    weight gradients those of this rank's experts ([E_loc, 2F, H] and [E_loc, H, F]; None when no
+    row reached them)."""
+    import torch
+    ops = ops or KernelOps()
+    # the gradient of the combine: each sorted row's output gradient is its token's row of d_out
+    dy_send = ops.gather_rows(d_out, ctx.token_of_row)
+    dy_recv = torch.empty((ctx.R_recv, ctx.H), dtype=dy_send.dtype, device=ctx.dev)
+    _exchange(dy_recv, dy_send, ctx.recv_counts, ctx.send_counts, group)
+    dx_sorted = dg_sorted = dw1 = dw2 = None
+    if ctx.R_recv > 0:
+        dx_sorted, dg_sorted, dw1, dw2 = ops.expert_mlp_bwd(ctx.x_recv, ctx.tor_l, ctx.split_l, ctx.gs_l, ctx.saved,
+                                                            weights_t, dy_recv)
+    dx_ret = _return_rows(dx_sorted, ctx, group, ops, ops.y_dtype, (ctx.H,))
+    dx = ops.combine(dx_ret, ctx.row_of_slot)   # the gradient of the token gather: sum over slots
+    dgates = None
+    if ctx.with_gates:
+        dg_ret = _return_rows(dg_sorted, ctx, group, ops, ops.dg_dtype, ())
+        dgates = ops.gather_rows(dg_ret, ctx.row_of_slot).view(ctx.T, ctx.k)
+    return dx, dgates, dw1, dw2

@@ -1,6 +1,7 @@
 """Expert-parallel MoE layer on the GPU with one NCCL rank (every call in this test suite has one
 GPU): the exchanges are copies, so the layer must equal the single-GPU MoE layer (moe_permute ->
-grouped_mlp_fwd_tokens -> moe_combine) bit for bit.
+grouped_mlp_fwd_tokens -> moe_combine, and its backward) bit for bit.  Also the row gather the
+layer moves rows with (moe_gather_rows), bit-exact against numpy indexing.
 
 Page "Efficient MoE training for biological foundation models", How to run the recipe (experts
 spread over the GPUs) and Key technical approaches item 1.  The exchange logic over several ranks
@@ -71,3 +72,64 @@ def test_one_rank_equals_the_moe_layer(mx, nccl_group, name, with_gates):
     b = ref.view(torch.int16).cpu().numpy()
     assert np.array_equal(a, b), f"{int((a != b).sum())} elements differ"
     assert np.abs(b.view(np.uint16).astype(np.int64)).max() > 0
+
+
+@pytest.mark.parametrize("dtype,width", [("bf16", 4096), ("f32", 1), ("f32", 3), ("i32", 8)])
+def test_gather_rows_bit_exact(mx, dtype, width):
+    import torch
+    rng = np.random.default_rng(width)
+    n_src, n = 1000, 2500
+    if dtype == "bf16":
+        src_np = rng.integers(0, 1 << 16, size=(n_src, width), dtype=np.uint16)
+        src = torch.from_numpy(src_np.view(np.int16)).cuda().view(torch.bfloat16)
+    elif dtype == "f32":
+        src_np = rng.integers(0, 1 << 32, size=(n_src, width), dtype=np.uint32)   # any bit pattern, NaNs included
+        src = torch.from_numpy(src_np.view(np.int32)).cuda().view(torch.float32)
+    else:
+        src_np = rng.integers(0, 1 << 32, size=(n_src, width), dtype=np.uint32)
+        src = torch.from_numpy(src_np.view(np.int32)).cuda()
+    if width == 1:
+        src = src.view(-1)
+    idx = rng.integers(-3, n_src + 3, size=n).astype(np.int32)   # a few out of range: zero rows
+    got = mx.moe_gather_rows(src, torch.from_numpy(idx).cuda())
+    bits = got.view(torch.int16 if dtype == "bf16" else torch.int32).cpu().numpy().reshape(n, -1)
+    ref = np.zeros((n, width), dtype=src_np.dtype)
+    ok = (idx >= 0) & (idx < n_src)
+    ref[ok] = src_np[idx[ok]]
+    assert np.array_equal(bits.view(src_np.dtype), ref)
+
+
+@pytest.mark.parametrize("with_gates", [True, False])
+def test_one_rank_training_equals_the_moe_layer(mx, nccl_group, with_gates):
+    import torch
+    from mxfp8_block_scaled_03_gb300 import ep
+    w = W.moe_workload("tiny")
+    x = G.to_dev_bf16(w.x_tokens)
+    ex = G.to_dev(w.topk_experts.astype(np.int32))
+    g = G.to_dev(w.topk_gates) if with_gates else None
+    wts = _weights(mx, w)
+    w1t = mx.mxfp8_quantize_colwise_t(G.to_dev_bf16(w.w1))
+    w2t = mx.mxfp8_quantize_colwise_t(G.to_dev_bf16(w.w2))
+    wts_t = (w1t[0], w1t[1], w2t[0], w2t[1])
+    d_out = G.to_dev_bf16(W.bf16_bits(np.random.default_rng(4).standard_normal(w.x_tokens.shape).astype(np.float32)))
+    # the single-GPU layer and its backward
+    split, ros, tor, gs, _ = mx.moe_permute(ex, g, w.E)
+    y_rows, saved = mx.grouped_mlp_fwd_tokens_train(x, tor, split, gs, *wts)
+    ref = mx.moe_combine(y_rows, ros)
+    dx_rows, dg_rows, dw1, dw2, _ = mx.grouped_mlp_bwd_tokens(x, tor, split, gs, saved, *wts_t, d_out)
+    dx_ref = mx.moe_combine(dx_rows, ros)
+    # through the expert-parallel path
+    out, ctx = ep.ep_moe_forward_train(x, ex, g, wts, w.E)
+    dx, dg, edw1, edw2 = ep.ep_moe_backward(d_out, ctx, wts_t)
+    torch.cuda.synchronize()
+
+    def bits(t):
+        return t.contiguous().view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32).cpu().numpy()
+
+    assert np.array_equal(bits(out), bits(ref))
+    assert np.array_equal(bits(dx), bits(dx_ref))
+    assert np.array_equal(bits(edw1), bits(dw1)) and np.array_equal(bits(edw2), bits(dw2))
+    if with_gates:
+        assert np.array_equal(bits(dg), bits(dg_rows[ros.long()]))
+    else:
+        assert dg is None
