@@ -115,6 +115,10 @@ def _dispatch(x_tokens, experts, gates, E, group, ops):
     world = dist.get_world_size(group)
     if E % world != 0:
         raise ValueError(f"{E} experts do not divide over {world} ranks")
+    if experts.dim() != 2 or experts.dtype != torch.int32 or experts.shape[0] != x_tokens.shape[0]:
+        raise ValueError("experts must be int32 [T, k] with T = rows of x_tokens")
+    if gates is not None and tuple(gates.shape) != tuple(experts.shape):
+        raise ValueError("gates must be [T, k] like experts")
     E_loc = E // world
     T, k = experts.shape
     H = x_tokens.shape[1]
@@ -123,12 +127,13 @@ def _dispatch(x_tokens, experts, gates, E, group, ops):
     # 1. sort this rank's choices by expert: the rows bound for rank r are one run
     split, row_of_slot, token_of_row, gates_sorted = ops.permute(experts, gates, E)
 
-    # 2. per-expert counts both ways, row counts on the host
+    # 2. per-expert counts both ways, row counts on the host (one copy)
     send_split = split.view(world, E_loc).contiguous()
     recv_split = torch.empty_like(send_split)
     dist.all_to_all_single(recv_split, send_split, group=group)
-    recv_split_h = recv_split.cpu().numpy()
-    send_counts = [int(c) for c in send_split.sum(1).cpu().tolist()]
+    both = torch.stack([send_split, recv_split]).cpu().numpy()
+    send_counts = [int(c) for c in both[0].sum(1)]
+    recv_split_h = both[1]
     recv_counts = [int(c) for c in recv_split_h.sum(1)]
     R_recv = sum(recv_counts)
 
