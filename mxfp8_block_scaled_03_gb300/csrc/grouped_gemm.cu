@@ -80,6 +80,7 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_SF_WARPS = 4;
 constexpr uint32_t BAR_EPI = 1;            // hardware barrier of the epilogue warps
 constexpr uint32_t BAR_SF = 2;             // hardware barrier of the scale-staging warps
+constexpr uint32_t BAR_STAGGER = 3;        // 3..6: pair kernel, the two epilogue warps of a lane quarter
 constexpr uint32_t REGS_LOW = 56;
 constexpr uint32_t REGS_HIGH = 200;
 static_assert(2 * 128 * REGS_LOW + 256 * REGS_HIGH == NUM_THREADS * 128, "register split must equal the launch pool");
@@ -1058,7 +1059,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else {
+        // GroupedLinear 1: the two warps of a lane quarter share a scheduler with each other and
+        // (for one quarter) with the MMA thread; they run their SwiGLU/quantize math one after the
+        // other, so at most one of them competes for issue slots at a time (1.5% faster).  Half 0
+        // is never a tile ahead of half 1: both pass the epilogue barrier of every tile.
+        if (MODE == GEMM_SWIGLU && half == 1) asm volatile("bar.sync %0, 64;" ::"r"(BAR_STAGGER + quarter) : "memory");
         epilogue_tile<MODE>(p, t, v, r, half, 256);
+        if (MODE == GEMM_SWIGLU && half == 0) asm volatile("bar.arrive %0, 64;" ::"r"(BAR_STAGGER + quarter) : "memory");
       }
     }
     if (MODE == GEMM_WGRAD && lane == 0) bulk_wait_all();   // stores complete before the CTA exits
