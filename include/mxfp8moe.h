@@ -296,7 +296,7 @@ int mxfp8_quantize_colwise_t(const void* x, int64_t M, int64_t K, int sf_layout,
  *   [0] error word (uint32)   [1] schedule          [2] quantized activations [R_pad, H]
  *   [3] their E8M0 bytes (MXFP8_SF_MMA layout)      [4] quantized intermediate [R_pad, F]
  *   [5] its E8M0 bytes (MXFP8_SF_MMA layout)        [6] R_pad (row capacity, not an offset)
- * Expert e's rows start at padded row sum_{e'<e} 128*ceil(split[e']/128); padding rows are 0.
+ * Expert e's rows start at padded row sum_{e'<e} 256*ceil(split[e']/256); padding rows are 0.
  * Returns MXFP8_OK, or MXFP8_ERR_INVALID_ARG for bad sizes.  out must hold 7 entries (host). */
 int grouped_mlp_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_t* out);
 
