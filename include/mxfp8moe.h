@@ -21,7 +21,8 @@
  *     (host) are ordinary host memory read during the call.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All work
  *     is enqueued on it; no call synchronizes the host except mxfp8_check_device_error.
- *   - Every device pointer must be 16-byte aligned.  bf16 tensors are row-major IEEE bfloat16.
+ *   - Every device pointer must be 16-byte aligned unless its call says otherwise.  bf16
+ *     tensors are row-major IEEE bfloat16.
  *   - Return value: an mxfp8_status.  Argument errors are detected on the host before anything
  *     is enqueued and leave all buffers untouched.  Conditions only visible on the device
  *     (split_sizes that do not add up to R, a pipeline wait that timed out) set bits in the
