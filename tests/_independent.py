@@ -73,3 +73,27 @@ def decode(codes: np.ndarray, sf: np.ndarray) -> np.ndarray:
 
 def silu(g: float) -> float:
     return g / (1.0 + math.exp(-g))
+
+
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """binary64 -> nearest bfloat16 value (ties to the even bit pattern), as binary64.
+
+    torch converts float64 to bfloat16 through float32, which rounds twice; here torch's result
+    only seeds a search: of its bit pattern and the two neighbouring patterns, the one nearest to
+    v wins (the differences are exact in binary64: the candidates lie within a factor of two of
+    |v|), and a tie goes to the even pattern."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    seed = torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().astype(np.int64) & 0xFFFF
+    cand = np.stack([np.maximum(seed - 1, 0), seed, seed + 1])
+    vals = (cand.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    d = np.abs(vals - a[None])
+    best = np.argmin(d, axis=0)
+    dmin = np.take_along_axis(d, best[None], axis=0)[0]
+    tie = (d == dmin[None]).sum(axis=0) > 1
+    even = np.where(cand % 2 == 0, 0, 1)
+    # among the tied candidates take the one with an even pattern
+    tb = np.argmin(np.where(d == dmin[None], even, 2), axis=0)
+    pick = np.where(tie, tb, best)
+    out = np.take_along_axis(vals, pick[None], axis=0)[0]
+    return np.where(np.signbit(v), -out, out)

@@ -10,7 +10,10 @@ check
     ragged problem with an empty expert;
   - the quantization axes, with inputs built so that quantizing along the wrong axis changes
     the result (a large element crushes its block neighbours to zero along one axis only);
-  - power-of-two scaling of dy, which MXFP8 and bf16 rounding commute with exactly.
+  - power-of-two scaling of dy, which MXFP8 and bf16 rounding commute with exactly;
+  - the whole quantized backward (every bf16 rounding and every MXFP8 step in its place)
+    against an independent torch-float64 restatement with the search quantizer, on a ragged
+    problem with an empty expert and partial 32-row blocks.
 """
 import numpy as np
 import pytest
@@ -151,3 +154,81 @@ def test_rejects_bad_entries(oracle):
         oracle.grouped_mlp_bwd_dw(w.x_sorted, w.split_sizes, None, *wq[:4], dy, 2, np.array([[0, 64, 0]]))
     with pytest.raises(ValueError):
         oracle.grouped_mlp_bwd_dw(w.x_sorted, w.split_sizes, None, *wq[:4], dy, 3, np.array([[0, 0, 0]]))
+
+
+def _rowq(v):
+    """Row-wise MXFP8 (blocks of 32 along the last axis) through the independent quantizer."""
+    q, s = ind.quantize_rows_bruteforce(np.ascontiguousarray(v, dtype=np.float64))
+    return ind.decode(q, s)
+
+
+def test_quantized_backward_matches_independent_restatement(oracle):
+    """The whole quantized backward restated step by step in torch float64 with the independent
+    search quantizer and a direct bf16 rounding, on a ragged problem with an empty expert and
+    partial 32-row blocks.  Steps, in the reading the oracle documents:
+      a = dq(Q_row(x));  g, u = bf16(a W1g^T), bf16(a W1u^T)  (the forward's saved pre-activations)
+      dh = dq(Q_row(dy)) W2q   (W2 quantized along H)
+      dG = dh gate u silu'(g),  dU = dh gate silu(g),  dgate = sum dh silu(g) u
+      dGU = bf16([dG | dU]);  dx = dq(Q_row(dGU)) W1q  (both quantized along 2F)
+      h = bf16(gate silu(g) u)
+      dW2[e] = dq(Q_col(dy_e))^T dq(Q_col(h_e)),  dW1[e] = dq(Q_col(dGU_e))^T dq(Q_col(x_e))
+    Dropping the row-wise quantization of dGU, or moving any bf16 rounding, changes dx, dGU or the
+    weight gradients far beyond the 1e-12 bar."""
+    rng = np.random.default_rng(7)
+    split = np.array([5, 0, 40, 19], dtype=np.int32)
+    E, H, F = 4, 64, 64
+    R = int(split.sum())
+    x = W.bf16_bits(rng.standard_normal((R, H)).astype(np.float32))
+    dy = W.bf16_bits(rng.standard_normal((R, H)).astype(np.float32))
+    w1 = W.bf16_bits((rng.standard_normal((E * 2 * F, H)) * 0.15).astype(np.float32))
+    w2 = W.bf16_bits((rng.standard_normal((E * H, F)) * 0.15).astype(np.float32))
+    gates = rng.uniform(0.1, 1.0, R).astype(np.float32)
+    wq = _weights(oracle, w1, w2, E)
+    rows = np.arange(R)
+    dx_o, dgate_o, dgu_o, h_o = oracle.grouped_mlp_bwd_rows(x, split, gates, *wq, dy, rows)
+    dw2_o = oracle.grouped_mlp_bwd_dw(x, split, gates, *wq[:4], dy, 2, _all_entries(E, H, F))
+    dw1_o = oracle.grouped_mlp_bwd_dw(x, split, gates, *wq[:4], dy, 1, _all_entries(E, 2 * F, H))
+
+    f64 = lambda b: W.bf16_to_f32(b).astype(np.float64)
+    xf, dyf = f64(x), f64(dy)
+    w1f = f64(w1).reshape(E, 2 * F, H)
+    w2f = f64(w2).reshape(E, H, F)
+    off = np.concatenate([[0], np.cumsum(split)])
+    dx = np.zeros((R, H))
+    dgate = np.zeros(R)
+    dgu = np.zeros((R, 2 * F))
+    hb = np.zeros((R, F))
+    dw2 = np.zeros((E, H, F))
+    dw1 = np.zeros((E, 2 * F, H))
+    T = torch.from_numpy
+    for e in range(E):
+        r0, r1 = off[e], off[e + 1]
+        if r1 == r0:
+            continue
+        W1q = _rowq(w1f[e])                   # [2F, H], blocks along H (forward operand)
+        W2q_t = _rowq(w2f[e].T)               # [F, H]: W2 quantized along H
+        W1q_t = _rowq(w1f[e].T)               # [H, 2F]: W1 quantized along 2F
+        a = _rowq(xf[r0:r1])
+        g = ind.bf16_round((T(a) @ T(W1q[:F]).T).numpy())
+        u = ind.bf16_round((T(a) @ T(W1q[F:]).T).numpy())
+        gt = gates[r0:r1].astype(np.float64)[:, None]
+        sig = 1.0 / (1.0 + np.exp(-g))
+        s = g * sig
+        ds = sig * (1.0 + g * (1.0 - sig))
+        dh = (T(_rowq(dyf[r0:r1])) @ T(W2q_t).T).numpy()
+        dGU = ind.bf16_round(np.concatenate([dh * gt * u * ds, dh * gt * s], axis=1))
+        dgu[r0:r1] = dGU
+        dgate[r0:r1] = (dh * s * u).sum(axis=1)
+        dx[r0:r1] = (T(_rowq(dGU)) @ T(W1q_t).T).numpy()
+        h = ind.bf16_round(gt * s * u)
+        hb[r0:r1] = h
+        dw2[e] = (T(_colq(dyf[r0:r1])).T @ T(_colq(h))).numpy()
+        dw1[e] = (T(_colq(dGU)).T @ T(_colq(xf[r0:r1]))).numpy()
+
+    assert np.array_equal(f64(dgu_o), dgu)
+    assert np.array_equal(f64(h_o), hb)
+    np.testing.assert_allclose(dx_o, dx, rtol=1e-12, atol=1e-12 * np.abs(dx).max())
+    np.testing.assert_allclose(dgate_o, dgate, rtol=1e-12, atol=1e-12 * np.abs(dgate).max())
+    np.testing.assert_allclose(dw2_o, dw2.ravel(), rtol=1e-12, atol=1e-12 * np.abs(dw2).max())
+    np.testing.assert_allclose(dw1_o, dw1.ravel(), rtol=1e-12, atol=1e-12 * np.abs(dw1).max())
+    assert np.all(dw1[1] == 0) and np.all(dw2[1] == 0)
