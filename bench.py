@@ -231,10 +231,84 @@ WORKLOAD_TEXT = {
 }
 
 
+# ------------------------------------------------------------------------------------------------
+# GPU leg
+# ------------------------------------------------------------------------------------------------
+def _events(n):
+    import torch
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def gpu_numa_node(local: int):
+    """NUMA node of the host memory closest to this GPU (the node of its PCI device), or None."""
+    import torch
+    pr = torch.cuda.get_device_properties(local)
+    ids = [getattr(pr, a, None) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")]
+    paths = []
+    if None not in ids:
+        paths.append(f"/sys/bus/pci/devices/{ids[0]:04x}:{ids[1]:02x}:{ids[2]:02x}.0/numa_node")
+    try:
+        uuid = str(getattr(pr, "uuid", ""))
+        out = subprocess.run(["nvidia-smi", "--query-gpu=uuid,pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout
+        for line in out.splitlines():
+            u, bus = [t.strip() for t in line.split(",")]
+            if uuid and uuid in u:
+                dom, rest = bus.split(":", 1)
+                paths.append(f"/sys/bus/pci/devices/{int(dom, 16):04x}:{rest.lower()}/numa_node")
+    except Exception:
+        pass
+    for path in paths:
+        try:
+            node = int(open(path).read().strip())
+            if node >= 0:
+                return node
+        except Exception:
+            continue
+    return None
+
+
+def node_cpus(node: int):
+    try:
+        text = open(f"/sys/devices/system/node/node{node}/cpulist").read().strip()
+    except Exception:
+        return set()
+    cpus = set()
+    for part in text.split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus
+
+
+def numa_pages(ptr: int):
+    """{node: pages} of the mapping of this process that holds address ptr (/proc/self/numa_maps)."""
+    try:
+        best = None
+        for line in open("/proc/self/numa_maps"):
+            parts = line.split()
+            start = int(parts[0], 16)
+            if start <= ptr and (best is None or start > best[0]):
+                best = (start, parts)
+        if best is None:
+            return None
+        nodes = {}
+        for t in best[1]:
+            if t.startswith("N") and "=" in t:
+                k, v = t[1:].split("=")
+                nodes[int(k)] = int(v)
+        return nodes or None
+    except Exception:
+        return None
+
+
 def library_mxfp8_gemms(R, H, F, dev, iters=10):
     """Context only: cuBLASLt's MXFP8 GEMM (through torch._scaled_mm) on the dense shapes of the two
-    grouped GEMMs (M = routed rows, no expert grouping, bf16 output, no fused epilogue), timed with
-    CUDA events on synthetic E4M3 codes with unit scales.  Nothing of the library's path runs here."""
+    grouped GEMMs (M = routed rows, no expert grouping, bf16 output, no fused epilogue) and on the
+    8192^3 square, timed with CUDA events on synthetic E4M3 codes with unit scales.  Nothing of the
+    library's path runs here."""
     import torch
     if not hasattr(torch, "float8_e8m0fnu"):
         return {"unavailable": "this torch has no float8_e8m0fnu"}
@@ -244,7 +318,8 @@ def library_mxfp8_gemms(R, H, F, dev, iters=10):
 
     out = {"kind": "cuBLASLt MXFP8 (torch._scaled_mm, block scale 1x32, bf16 out)", "note":
            "dense [M,K]x[K,N] without grouping, routing weight, SwiGLU or requantization"}
-    for name, (M, N, K) in (("grouped_linear1_shape", (R, 2 * F, H)), ("grouped_linear2_shape", (R, H, F))):
+    for name, (M, N, K) in (("grouped_linear1_shape", (R, 2 * F, H)), ("grouped_linear2_shape", (R, H, F)),
+                            ("square_8192", (8192, 8192, 8192))):
         try:
             g = torch.Generator(device=dev).manual_seed(3)
             a = (torch.randn(M, K, device=dev, generator=g) * 0.5).to(torch.float8_e4m3fn)
@@ -255,7 +330,7 @@ def library_mxfp8_gemms(R, H, F, dev, iters=10):
             for _ in range(3):
                 run()
             torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0, e1 = _events(2)
             e0.record()
             for _ in range(iters):
                 run()
@@ -270,6 +345,32 @@ def library_mxfp8_gemms(R, H, F, dev, iters=10):
     return out
 
 
+def mma_loop_peak(mx, dev):
+    """The library's own back-to-back block-scaled pair-MMA loop (mxfp8_mma_peak): TFLOP/s of the
+    tensor pipe with operands resident in shared memory."""
+    import torch
+    ws = torch.zeros(64, dtype=torch.uint8, device=dev)
+    iters = 1 << 18
+    mx.mxfp8_mma_peak(iters // 16, ws)
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(3):
+        e0, e1 = _events(2)
+        e0.record()
+        n = mx.mxfp8_mma_peak(iters, ws)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        tf = n * iters * 4 * 2.0 * 256 * 256 * 32 / (ms * 1e-3) / 1e12
+        best = tf if best is None else max(best, tf)
+    st, bits = mx.mxfp8_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"MMA peak loop error word {bits:#x}")
+    return {"tflops": best, "clusters": n, "mma_per_cluster": 4 * iters,
+            "kind": "mxfp8_mma_peak: tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale M=256 N=256 K=32, "
+                    "operands resident in shared memory, best of 3 launches"}
+
+
 def workload_config(w):
     return {"workload": f"{WORKLOAD_TEXT[w.name]}: E={w.E} top-{w.topk} T={w.T} (R={w.R} routed rows) "
                         f"H={w.H} F={w.F}, x~N(0,1), W~N(0,0.02)",
@@ -278,9 +379,145 @@ def workload_config(w):
             "parallelism": "replicas"}
 
 
-# ------------------------------------------------------------------------------------------------
-# GPU leg
-# ------------------------------------------------------------------------------------------------
+class Forward:
+    """Device-resident inputs of one workload and its grouped_mlp_fwd step."""
+
+    def __init__(self, mx, w, dev):
+        import numpy as np
+        import torch
+        self.mx, self.w, self.dev = mx, w, dev
+        bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        self.x = bf(w.x_sorted)
+        self.split = torch.from_numpy(w.split_sizes).to(dev)
+        self.gates = torch.from_numpy(w.gates).to(dev) if w.gates is not None else None
+        w1, w2 = bf(w.w1), bf(w.w2)
+        for _ in range(2):
+            self.w1q, self.w1s, _, _ = mx.mxfp8_quantize(w1, sf_layout=mx.SF_MMA)
+            self.w2q, self.w2s, _, _ = mx.mxfp8_quantize(w2, sf_layout=mx.SF_MMA)
+        e0, e1 = _events(2)
+        e0.record()
+        mx.mxfp8_quantize(w1, sf_layout=mx.SF_MMA, out=[self.w1q, self.w1s, None, None])
+        mx.mxfp8_quantize(w2, sf_layout=mx.SF_MMA, out=[self.w2q, self.w2s, None, None])
+        e1.record()
+        torch.cuda.synchronize()
+        self.weight_quant_ms = e0.elapsed_time(e1)
+        self.w1_bf16, self.w2_bf16 = w1, w2      # kept for the backward's transposed weights
+        R, H, F, E = w.R, w.H, w.F, w.E
+        self.ws = torch.empty(mx.grouped_mlp_workspace_size(R, H, F, E), dtype=torch.uint8, device=dev)
+        self.y = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+        self.flops = 6.0 * R * H * F
+
+    def step(self, events=None):
+        self.mx.grouped_mlp_fwd(self.x, self.split, self.gates, self.w1q, self.w1s, self.w2q, self.w2s, y=self.y,
+                                workspace=self.ws, stage_events=events)
+
+    def check(self, when):
+        st, bits = self.mx.mxfp8_check_device_error(self.ws)
+        if st != 0:
+            raise RuntimeError(f"device error word {bits:#x} {when}")
+
+    def time(self, steps, warmup, world=1, clocks=None):
+        """Per-step device time (events around K steps) and per-kernel times (events the library
+        records between its kernels on the same stream)."""
+        import torch
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        self.check("after warm-up")
+        stage_ev = [_events(5) for _ in range(steps)]
+        for evs in stage_ev:          # torch creates the CUDA event on first record; the library re-records it
+            for ev in evs:
+                ev.record()
+        torch.cuda.synchronize()
+        t_start, t_end = _events(2)
+        ctx = ClockSampler(clocks) if clocks is not None else None
+        if ctx is not None:
+            ctx.__enter__()
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start.record()
+        for i in range(steps):
+            self.step(stage_ev[i])
+        t_end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        if ctx is not None:
+            ctx.__exit__(None, None, None)
+        self.clocks = ctx.summary() if ctx is not None else None
+        step_ms = max_over_ranks(world, t_start.elapsed_time(t_end) / steps)
+        names = ["schedule", "quantize_x", "grouped_linear1_swiglu_requant", "grouped_linear2"]
+        kern_ms = {n: sum(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev) / steps for j, n in enumerate(names)}
+        self.check("after timed steps")
+        return step_ms, kern_ms
+
+
+def forward_summary(fwd, step_ms, kern_ms, fp8_peak, mma_peak, world=1):
+    w = fwd.w
+    R, H, F = w.R, w.H, w.F
+    g1 = 4.0 * R * H * F / (kern_ms["grouped_linear1_swiglu_requant"] * 1e-3) / 1e12
+    g2 = 2.0 * R * H * F / (kern_ms["grouped_linear2"] * 1e-3) / 1e12
+    value = world * fwd.flops / (step_ms * 1e-3) / 1e12
+    out = {"workload": w.name, "R": R, "H": H, "F": F, "E": w.E, "ms": step_ms, "tflops": value,
+           "frac_of_peak": value / world / fp8_peak, "kernel_ms": kern_ms,
+           "grouped_linear1": {"tflops": g1, "frac": g1 / fp8_peak},
+           "grouped_linear2": {"tflops": g2, "frac": g2 / fp8_peak}}
+    if mma_peak:
+        out["frac_of_measured_mxfp8_peak"] = value / world / mma_peak
+        out["grouped_linear1"]["frac_of_measured_mxfp8_peak"] = g1 / mma_peak
+        out["grouped_linear2"]["frac_of_measured_mxfp8_peak"] = g2 / mma_peak
+    return out
+
+
+def quantize_sweep(mx, dev, peaks, steps):
+    """Stand-alone MXFP8 quantize of the sweep's three bf16 matrices, row-wise and row + column.
+    Inputs that fit in L2 (the two smaller shapes) are timed one launch at a time with L2 flushed
+    (a 512 MiB buffer written) before each; the largest (470 MB) is timed over back-to-back
+    launches, its input far above L2."""
+    import numpy as np
+    import torch
+    from mxfp8_block_scaled_03_gb300 import workloads as W
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    out = []
+    for (M, K) in ((4096, 4096), (8192, 4096), (16384, 14336)):
+        x = torch.from_numpy(W.quant_matrix(M, K, seed=0).view(np.int16)).to(dev).view(torch.bfloat16)
+        small = M * K * 2 < 128 << 20
+        for dirs, col in (("row", False), ("row+col", True)):
+            buf = list(mx.mxfp8_quantize(x, rowwise=True, colwise=col))
+            for _ in range(3):
+                mx.mxfp8_quantize(x, rowwise=True, colwise=col, out=buf)
+            torch.cuda.synchronize()
+            n = max(10, steps)
+            if small:
+                tot = 0.0
+                for _ in range(n):
+                    flush.fill_(1)
+                    e0, e1 = _events(2)
+                    e0.record()
+                    mx.mxfp8_quantize(x, rowwise=True, colwise=col, out=buf)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    tot += e0.elapsed_time(e1)
+                ms = tot / n
+            else:
+                e0, e1 = _events(2)
+                e0.record()
+                for _ in range(n):
+                    mx.mxfp8_quantize(x, rowwise=True, colwise=col, out=buf)
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / n
+            nbytes = M * K * (2 + (2 if col else 1) * (1 + 1 / 32))
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out.append({"shape": [M, K], "directions": dirs, "ms": ms, "achieved": gbs, "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
+                        "l2": "flushed before each launch" if small else "no flush: input above L2"})
+            del buf
+        del x
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_native(args, world, rank, local):
     import numpy as np
     import torch
@@ -294,70 +531,25 @@ def run_native(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+
+    # run on the cores (and first-touch host memory on the NUMA node) next to this GPU
+    numa = {"gpu_node": gpu_numa_node(local)}
+    if numa["gpu_node"] is not None and hasattr(os, "sched_setaffinity"):
+        cpus = node_cpus(numa["gpu_node"]) & set(os.sched_getaffinity(0))
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+            numa["bound_cpus"] = len(cpus)
 
     w = W.moe_workload(args.workload, seed=0)
     R, H, F, E = w.R, w.H, w.F, w.E
     flops = 6.0 * R * H * F
-
-    def bf(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    x = bf(w.x_sorted)
-    split = torch.from_numpy(w.split_sizes).to(dev)
-    gates = torch.from_numpy(w.gates).to(dev) if w.gates is not None else None
-    w1 = bf(w.w1)
-    w2 = bf(w.w2)
-    # weights quantized once (timed separately)
-    for _ in range(2):
-        w1q, w1s, _, _ = mx.mxfp8_quantize(w1, sf_layout=mx.SF_MMA)
-        w2q, w2s, _, _ = mx.mxfp8_quantize(w2, sf_layout=mx.SF_MMA)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    mx.mxfp8_quantize(w1, sf_layout=mx.SF_MMA, out=[w1q, w1s, None, None])
-    mx.mxfp8_quantize(w2, sf_layout=mx.SF_MMA, out=[w2q, w2s, None, None])
-    e1.record()
-    torch.cuda.synchronize()
-    weight_quant_ms = e0.elapsed_time(e1)
-    del w1, w2
-    ws = torch.empty(mx.grouped_mlp_workspace_size(R, H, F, E), dtype=torch.uint8, device=dev)
-    y = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
-
-    def step(events=None):
-        mx.grouped_mlp_fwd(x, split, gates, w1q, w1s, w2q, w2s, y=y, workspace=ws, stage_events=events)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    st, bits = mx.mxfp8_check_device_error(ws)
-    if st != 0:
-        raise RuntimeError(f"device error word {bits:#x} after warm-up")
-
-    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    for evs in stage_ev:          # torch creates the CUDA event on first record; the library re-records it
-        for ev in evs:
-            ev.record()
-    torch.cuda.synchronize()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier(world)
-        torch.cuda.synchronize()
-        t_start.record()
-        for i in range(args.steps):
-            step(stage_ev[i])
-        t_end.record()
-        torch.cuda.synchronize()
-        barrier(world)
-    clocks = clk.summary()
-    step_ms = t_start.elapsed_time(t_end) / args.steps
-    step_ms = max_over_ranks(world, step_ms)
-    names = ["schedule", "quantize_x", "grouped_linear1_swiglu_requant", "grouped_linear2"]
-    kern_ms = {n: sum(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev) / args.steps for j, n in enumerate(names)}
-    st, bits = mx.mxfp8_check_device_error(ws)
-    if st != 0:
-        raise RuntimeError(f"device error word {bits:#x} after timed steps")
-
+    fwd = Forward(mx, w, dev)
+    x, split, gates, y, ws = fwd.x, fwd.split, fwd.gates, fwd.y, fwd.ws
+    w1q, w1s, w2q, w2s = fwd.w1q, fwd.w1s, fwd.w2q, fwd.w2s
+    step_ms, kern_ms = fwd.time(args.steps, args.warmup, world, clocks=local)
+    clocks = fwd.clocks
     value = world * flops / (step_ms * 1e-3) / 1e12
-    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     traffic = load_traffic()
     g1_flops = 4.0 * R * H * F
     g1_tflops = g1_flops / (kern_ms["grouped_linear1_swiglu_requant"] * 1e-3) / 1e12
@@ -371,14 +563,15 @@ def run_native(args, world, rank, local):
                 "traffic": traffic.get("grouped_linear1_bytes_per_launch"),
                 "step_frac_of_peak": value / world / fp8_peak,
                 "kernel_ms": kern_ms,
-                "grouped_linear2": {"achieved": g2_tflops, "frac": g2_tflops / fp8_peak}}
+                "grouped_linear2": {"achieved": g2_tflops, "frac": g2_tflops / fp8_peak,
+                                    "traffic": traffic.get("grouped_linear2_bytes_per_launch")}}
 
     def measure_backward():
         # ---- backward (training): fwd_train saves [G | U]; the backward runs on a resident dy ----
         bwd = None
         if H % 256 == 0:
-            w1b, w2b = bf(w.w1), bf(w.w2)
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w1b, w2b = fwd.w1_bf16, fwd.w2_bf16
+            t0, t1 = _events(2)
             w1t = mx.mxfp8_quantize_colwise_t(w1b)
             w2t = mx.mxfp8_quantize_colwise_t(w2b)
             t0.record()
@@ -387,7 +580,6 @@ def run_native(args, world, rank, local):
             t1.record()
             torch.cuda.synchronize()
             wt_ms = t0.elapsed_time(t1)
-            del w1b, w2b
             gen = torch.Generator(device=dev)
             gen.manual_seed(1)
             dy = torch.randn((R, H), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
@@ -415,19 +607,19 @@ def run_native(args, world, rank, local):
                 if st != 0:
                     raise RuntimeError(f"device error word {bits:#x} in the backward")
             nb = max(3, args.steps)
-            bev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(nb)]
+            bev = [_events(7) for _ in range(nb)]
             for evs in bev:
                 for ev in evs:
                     ev.record()
             torch.cuda.synchronize()
-            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0, f1 = _events(2)
             f0.record()
             for _ in range(nb):
                 fwd_train()
             f1.record()
             torch.cuda.synchronize()
             ftrain_ms = f0.elapsed_time(f1) / nb
-            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0, b1 = _events(2)
             b0.record()
             for i in range(nb):
                 bwd_step(bev[i])
@@ -437,18 +629,17 @@ def run_native(args, world, rank, local):
             names = ["quantize_dy_x", "dgrad2_swiglu_bwd", "quantize_dgu_h_dgate", "dgrad1", "wgrad2", "wgrad1"]
             stage = {n: sum(e[j].elapsed_time(e[j + 1]) for e in bev) / nb for j, n in enumerate(names)}
             bflops = 12.0 * R * H * F
-            fp8_peak_b = peaks["bf16_tflops"] * FP8_OVER_BF16
             gemm_tf = {"dgrad2_swiglu_bwd": 2.0 * R * H * F, "dgrad1": 4.0 * R * H * F, "wgrad2": 2.0 * R * H * F,
                        "wgrad1": 4.0 * R * H * F}
             bwd = {"ms": bwd_ms, "tflops": bflops / (bwd_ms * 1e-3) / 1e12, "flops_per_step": bflops,
                    "stage_ms": stage,
-                   "gemm_frac_of_peak": {k: v / (stage[k] * 1e-3) / 1e12 / fp8_peak_b for k, v in gemm_tf.items()},
+                   "gemm_frac_of_peak": {k: v / (stage[k] * 1e-3) / 1e12 / fp8_peak for k, v in gemm_tf.items()},
                    "fwd_train_ms": ftrain_ms,
                    "train_step_tflops": 18.0 * R * H * F / ((bwd_ms + ftrain_ms) * 1e-3) / 1e12,
                    "weight_quantize_transposed_ms": wt_ms,
                    "note": "flops = 12 R H F (dh, dx, dW2, dW1); dy resident, no L2 flush (operands above L2)"}
             del dy, saved, bws, dx, dgt, dw1, dw2, w1t, w2t
-
+            torch.cuda.empty_cache()
         return bwd
 
     if args.only == "bwd":
@@ -461,13 +652,27 @@ def run_native(args, world, rank, local):
                               "roofline": roofline}), flush=True)
         return
 
-    # ---- stand-alone quantize (row + column) ----
-    qx = bf(W.quant_matrix(*QUANT_SHAPE, seed=0))
+    # ---- the measured MXFP8 peak: the larger of cuBLASLt at 8192^3 and the library's MMA loop ----
+    lib = library_mxfp8_gemms(R, H, F, dev)
+    mma = mma_loop_peak(mx, dev)
+    cands = {"mma_loop": mma["tflops"]}
+    sq = lib.get("square_8192", {}) if isinstance(lib, dict) else {}
+    if "tflops" in sq:
+        cands["cublaslt_8192"] = sq["tflops"]
+    mpeak_src = max(cands, key=cands.get)
+    mpeak = cands[mpeak_src]
+    peak_measured = {"value": mpeak, "unit": "TFLOP/s", "source": mpeak_src, "candidates": cands, "mma_loop": mma}
+    roofline["frac_of_measured_mxfp8_peak"] = g1_tflops / mpeak
+    roofline["step_frac_of_measured_mxfp8_peak"] = value / world / mpeak
+    roofline["grouped_linear2"]["frac_of_measured_mxfp8_peak"] = g2_tflops / mpeak
+
+    # ---- stand-alone quantize (row + column) of the largest sweep shape: the headline quantize ----
+    qx = torch.from_numpy(W.quant_matrix(*QUANT_SHAPE, seed=0).view(np.int16)).to(dev).view(torch.bfloat16)
     M, K = QUANT_SHAPE
     qout = list(mx.mxfp8_quantize(qx, rowwise=True, colwise=True))
     for _ in range(max(3, args.warmup)):
         mx.mxfp8_quantize(qx, rowwise=True, colwise=True, out=qout)
-    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    q0, q1 = _events(2)
     torch.cuda.synchronize()
     qsteps = max(10, args.steps)
     q0.record()
@@ -483,10 +688,13 @@ def run_native(args, world, rank, local):
              "algorithmic_bytes_per_launch": q_bytes, "traffic": traffic.get("quantize_bytes_per_launch"),
              "l2": "no flush: 470 MB input > L2"}
     del qx, qout
+    torch.cuda.empty_cache()
+    sweep = quantize_sweep(mx, dev, peaks, args.steps)
 
     # ---- the MoE layer around the forward: permute -> gathered forward -> combine ----
     layer = None
     if w.topk_experts is not None:
+        bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
         xt = bf(w.x_tokens)
         exd = torch.from_numpy(w.topk_experts).to(dev)
         gtd = torch.from_numpy(w.topk_gates).to(dev)
@@ -508,7 +716,7 @@ def run_native(args, world, rank, local):
             mx.moe_combine(y, p_ros, out=out)
             evs[3].record()
 
-        lev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(max(3, args.steps))]
+        lev = [_events(4) for _ in range(max(3, args.steps))]
         for _ in range(max(3, args.warmup)):
             layer_step(lev[0])
         torch.cuda.synchronize()
@@ -530,22 +738,66 @@ def run_native(args, world, rank, local):
         del xt, out
 
     bwd = measure_backward()
-    lib = library_mxfp8_gemms(R, H, F, dev) if args.only == "all" else None
+
+    # ---- the other configurations of the sweep: forward of each, per kernel ----
+    configs = {}
+    if args.workload == "mixtral" and args.only == "all" and not args.no_configs:
+        for name in ("llama", "fine", "tiny"):
+            wo = W.moe_workload(name, seed=0)
+            f2 = Forward(mx, wo, dev)
+            n = max(args.steps, 20)
+            ms2, km2 = f2.time(n, max(3, args.warmup))
+            configs[name] = forward_summary(f2, ms2, km2, fp8_peak, mpeak)
+            configs[name]["steps"] = n
+            if name == "tiny":
+                configs[name]["note"] = "latency-bound (0.4 GFLOP): ms is the per-call device time"
+            del f2
+            torch.cuda.empty_cache()
 
     # ---- end to end through the public API with host buffers ----
     # Every step copies its inputs from pinned host memory and its output back.  Steps are
     # pipelined over three streams with double-buffered device x / y: the host->device copy of
-    # step i+1 and the device->host copy of step i-1 run while step i computes.
+    # step i+1 and the device->host copy of step i-1 run while step i computes.  The pinned
+    # buffers are allocated (and first touched) by this process while it runs on the cores of
+    # the GPU's NUMA node.
     xh = torch.from_numpy(np.ascontiguousarray(w.x_sorted).view(np.int16)).view(torch.bfloat16).pin_memory()
     sh = torch.from_numpy(w.split_sizes).pin_memory()
     gh = torch.from_numpy(w.gates).pin_memory() if w.gates is not None else None
     yh = torch.empty((R, H), dtype=torch.bfloat16).pin_memory()
+    yh.zero_()
+    numa["x_host_pages"] = numa_pages(xh.data_ptr())
+    numa["y_host_pages"] = numa_pages(yh.data_ptr())
     xd = [torch.empty_like(x) for _ in range(2)]
     sd = [torch.empty_like(split) for _ in range(2)]
     gd = [torch.empty_like(gates) if gates is not None else None for _ in range(2)]
     yd = [torch.empty_like(y) for _ in range(2)]
     s_comp = torch.cuda.current_stream()
     s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+
+    # each copy direction alone (same buffers, same streams)
+    def copy_gbs(fn, nbytes, stream):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = _events(2)
+        e0.record(stream)
+        for _ in range(5):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 5
+        return {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9}
+
+    def h2d_only():
+        with torch.cuda.stream(s_h2d):
+            xd[0].copy_(xh, non_blocking=True)
+
+    def d2h_only():
+        with torch.cuda.stream(s_d2h):
+            yh.copy_(yd[0], non_blocking=True)
+
+    copies = {"h2d_x": copy_gbs(h2d_only, xh.numel() * 2, s_h2d), "d2h_y": copy_gbs(d2h_only, yh.numel() * 2, s_d2h)}
+
     ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "comp", "d2h")}
     for k in ev:
         for e in ev[k]:
@@ -569,11 +821,11 @@ def run_native(args, world, rank, local):
             yh.copy_(yd[b], non_blocking=True)
             ev["d2h"][b].record(s_d2h)
 
-    for i in range(2):
+    for i in range(max(5, args.warmup)):
         e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0, a1 = _events(2)
     a0.record(s_comp)
     for i in range(args.steps):
         e2e_step(i)
@@ -584,14 +836,19 @@ def run_native(args, world, rank, local):
     barrier(world)
     h2d = xh.numel() * 2 + sh.numel() * 4 + (gh.numel() * 4 if gh is not None else 0)
     d2h = yh.numel() * 2
+    bound_ms = max(step_ms, copies["h2d_x"]["ms"], copies["d2h_y"]["ms"])
     e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "copy_alone": copies, "numa": numa,
+           "expected_ms": bound_ms, "ratio_to_expected": e2e_ms / bound_ms,
            "path": "pinned host x/split_sizes/gates -> device, grouped_mlp_fwd, y -> pinned host; "
-                   "three streams, copies of neighbouring steps overlap the forward"}
+                   "three streams, copies of neighbouring steps overlap the forward; "
+                   "expected_ms = max(device step, x copy alone, y copy alone)"}
 
     # ---- CPU oracle baseline on a bounded sample (rank 0 only, N=1 only) ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if hasattr(os, "sched_setaffinity") and "bound_cpus" in numa:
+            os.sched_setaffinity(0, range(os.cpu_count() or 1))   # the oracle uses every host core
         # calibrate on a short call, then time one call sized to about --cpu-seconds
         s = OracleSample(w, nrows=args.oracle_rows)
         t = s.run()
@@ -605,10 +862,11 @@ def run_native(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
-            "config": workload_config(w), "roofline": roofline, "quantize": quant, "moe_layer": layer, "backward": bwd,
+            "config": workload_config(w), "roofline": roofline, "peak_mxfp8_measured": peak_measured,
+            "quantize": quant, "quantize_sweep": sweep, "configs": configs, "moe_layer": layer, "backward": bwd,
             "e2e": e2e, "library_context": lib,
             "cpu_baseline": cpu, "clocks": clocks, "gpu_launches": 4 * args.steps,
-            "weight_quantize_ms": weight_quant_ms, "peaks": {"source": peak_src, **peaks},
+            "weight_quantize_ms": fwd.weight_quant_ms, "peaks": {"source": peak_src, **peaks},
         }
         print(json.dumps(line), flush=True)
 
@@ -621,6 +879,7 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--oracle-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the forward of the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="length of the timed oracle call behind cpu_baseline")
     ap.add_argument("--workload", choices=["mixtral", "llama", "fine", "tiny"], default=WORKLOAD,

@@ -192,17 +192,21 @@ int grouped_mlp_fwd_timed(const void* x_sorted, int64_t R, int64_t H, int64_t F,
  * The pages have no counterpart: this is a library convenience, not a step of the method.
  * Some callers cannot call cudaMalloc where they run the forward (allocator hooks, out-of-memory
  * handlers, hosts whose memory pool is owned elsewhere).  This variant takes the same inputs and
- * output as grouped_mlp_fwd but no workspace: its scratch is one 64 MiB file-scope device array
- * that every GPU loading the library holds until the process exits.
+ * output as grouped_mlp_fwd but no workspace: its scratch is one 64 MiB file-scope device array.
  *   - Problems whose grouped_mlp_workspace_size() exceeds 64 MiB return MXFP8_ERR_WORKSPACE
  *     before anything is enqueued.
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress with
- *     that device current); make that first call before any stream capture.
+ *   - The first call on a device is a set-up call: with that device current it looks up the
+ *     array's device address (cudaGetSymbolAddress) and sets the kernels' launch attributes.
+ *     Under CUDA's lazy module loading (the default) this is when the array and the library's
+ *     kernels are loaded onto that device, which takes device memory inside the driver; the
+ *     device then holds the array until the process exits.  So make the first call on each
+ *     device while allocation is still allowed, and before any stream capture.  Later calls on
+ *     that device allocate nothing.
  *   - All calls on a device share the array and leave the last call's contents in it; nothing
  *     in it needs to start at zero.  Calls that overlap on the GPU race on it.
  *   - Device-side conditions (split_sizes not summing to R, a timed-out wait) are not reported;
  *     use grouped_mlp_fwd with a workspace and mxfp8_check_device_error to see them.
- *   - Nothing is allocated or freed. */
+ *   - No call makes cudaMalloc, cudaFree or any allocating library call. */
 int grouped_mlp_fwd_noalloc(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E,
                             const int32_t* split_sizes, const float* gates,
                             const uint8_t* w1_q, const uint8_t* w1_sf,
@@ -306,6 +310,18 @@ int grouped_mlp_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_
  * MXFP8_ERR_DEVICE_TIMEOUT.  Works on grouped_mlp_fwd and moe_permute workspaces.  The raw bits go to
  * *flags when flags is not NULL (host). */
 int mxfp8_check_device_error(const void* workspace, void* stream, uint32_t* flags);
+
+/* mxfp8_mma_peak -- measurement aid, with no counterpart on the pages: the rate of the
+ * block-scaled tensor-core instruction this library's GEMMs are built on, on the device at hand
+ * (the roofline their TFLOP/s are reported against).  Launches one cluster of two CTAs per pair
+ * of SMs (as many as fit; their number goes to *clusters, host); each cluster issues `iters`
+ * K steps of four tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale (M = 256, N = 256, K = 32,
+ * E4M3 x E4M3, UE8M0 scales) back to back on operands resident in shared memory, so one launch
+ * performs clusters * iters * 4 * 2*256*256*32 floating-point operations; time it with events
+ * on `stream`.  workspace (device, 4-byte aligned, >= 4 bytes) receives an error word
+ * (mxfp8_check_device_error reports MXFP8_ERR_DEVICE_TIMEOUT if the final wait ran out).
+ * Requirements: 0 <= iters <= 2^24. */
+int mxfp8_mma_peak(int64_t iters, void* workspace, int* clusters, void* stream);
 
 /* Static description of a status code. */
 const char* mxfp8_status_string(int status);

@@ -33,6 +33,7 @@ __all__ = [
     "moe_permute_workspace_size", "moe_combine", "moe_gather_rows", "mxfp8_check_device_error", "mxfp8_quantize_colwise_t",
     "grouped_mlp_saved_bytes", "grouped_mlp_fwd_train", "grouped_mlp_bwd_workspace_size", "grouped_mlp_bwd",
     "grouped_mlp_fwd_tokens_train", "grouped_mlp_bwd_tokens", "mxfp8_status_string", "mxfp8_abi_version",
+    "mxfp8_mma_peak",
 ]
 
 ROWWISE = 1
@@ -114,6 +115,8 @@ def lib() -> ctypes.CDLL:
             L.moe_gather_rows.argtypes = [P, i64, i64, P, i64, P, P]
             L.mxfp8_check_device_error.restype = i32
             L.mxfp8_check_device_error.argtypes = [P, P, P]
+            L.mxfp8_mma_peak.restype = i32
+            L.mxfp8_mma_peak.argtypes = [i64, P, P, P]
             _lib = L
     return _lib
 
@@ -442,6 +445,14 @@ def moe_gather_rows(src, index, out=None, stream=None):
     _check(lib().moe_gather_rows(_ptr(src), int(src.shape[0]), row_bytes, _ptr(index), n, _ptr(out), _stream(stream)),
            "moe_gather_rows")
     return out
+
+
+def mxfp8_mma_peak(iters: int, workspace, stream=None) -> int:
+    """Enqueue the block-scaled MMA rate measurement (see include/mxfp8moe.h); returns the number
+    of CTA-pair clusters launched.  `workspace`: a CUDA tensor of at least 4 bytes."""
+    n = ctypes.c_int(0)
+    _check(lib().mxfp8_mma_peak(int(iters), _ptr(workspace), ctypes.byref(n), _stream(stream)), "mxfp8_mma_peak")
+    return int(n.value)
 
 
 def mxfp8_check_device_error(workspace, stream=None) -> tuple[int, int]:

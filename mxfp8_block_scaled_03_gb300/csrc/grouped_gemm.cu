@@ -120,7 +120,8 @@ struct GemmParams {
   uint16_t* y;
   int64_t ldy;             // H
   uint32_t* err;
-  uint64_t timeout_ns;
+  uint64_t timeout_ns;     // limit of each pipeline wait (producer, MMA, epilogue, scale staging)
+  uint64_t drain_ns;       // limit of each teardown wait for copies or MMAs still in flight
   // operand addressing of the pair kernel
   int a_kt;                // scale atoms per 128-row tile of A (K extent of A / 128)
   int b_kt;                // same for B
@@ -539,7 +540,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0)
         for (int s = 0; s < STAGES; ++s)
           if ((issued_mask >> s) & 1u)
-            if (!mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, p.timeout_ns))
+            if (!mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, p.drain_ns))
               atomicOr(p.err, ERR_TIMEOUT_DRAIN);
       __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -580,7 +581,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (issued) {
           tc_commit(drained);
-          if (!mbar_wait_bounded(drained, 0, nullptr, p.timeout_ns)) atomicOr(p.err, ERR_TIMEOUT_DRAIN);
+          if (!mbar_wait_bounded(drained, 0, nullptr, p.drain_ns)) atomicOr(p.err, ERR_TIMEOUT_DRAIN);
         }
       }
       __syncwarp();
@@ -851,6 +852,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int first_unit = static_cast<int>(cluster_index());
   const int unit_stride = static_cast<int>(cluster_count());
   const uint32_t peer_abort = map_to_cta(const_cast<int*>(abort_flag), rank ^ 1u);
+  uint32_t prod_issued = 0;   // producer warp: stages it issued copies for
   if (warp < FIRST_EPI_WARP) {
     regs_dec<P_REGS_LOW>();
     if (warp == WARP_PRODUCER) {
@@ -916,20 +918,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // Copies must land before the CTA exits.  The leader's barriers count both CTAs' copies and
       // the MMA warp waits for every stage it consumes; after an abort, the leader waits here
-      // (bounded) and the second CTA, whose copies complete on the leader's barriers, gives its
-      // copies in flight a fixed 200 us to land (they depend on nothing but memory).
-      if (lane == 0) {
-        if (leader) {
-          for (int s = 0; s < P_STAGES; ++s)
-            if ((issued_mask >> s) & 1u)
-              if (!mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, p.timeout_ns))
-                atomicOr(p.err, ERR_TIMEOUT_DRAIN);
-        } else if (!ok || *abort_flag) {
-          const uint64_t t0 = globaltimer_ns();
-          while (globaltimer_ns() - t0 < 200000ull) {
-          }
-        }
-      }
+      // (bounded) for the stages it issued.  The second CTA's copies complete on the leader's
+      // barriers, so it cannot wait for them itself: after the pair's closing cluster barrier,
+      // where every abort raised in either CTA is visible, it gives them a fixed 200 us to land
+      // (they depend on nothing but memory) before a second cluster barrier lets either CTA exit.
+      if (lane == 0 && leader)
+        for (int s = 0; s < P_STAGES; ++s)
+          if ((issued_mask >> s) & 1u)
+            if (!mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, p.drain_ns))
+              atomicOr(p.err, ERR_TIMEOUT_DRAIN);
+      prod_issued = issued_mask;
       __syncwarp();
     } else if (warp == WARP_MMA && leader) {
       // ---------------- pair MMA issuer (leader CTA; the loop runs in lane 0 alone) ----------------
@@ -987,7 +985,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (issued) {
           tc_commit_pair_local(drained);
-          if (!mbar_wait_bounded(drained, 0, nullptr, p.timeout_ns)) atomicOr(p.err, ERR_TIMEOUT_DRAIN);
+          if (!mbar_wait_bounded(drained, 0, nullptr, p.drain_ns)) atomicOr(p.err, ERR_TIMEOUT_DRAIN);
         }
       }
       __syncwarp();
@@ -1074,6 +1072,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();   // all pair MMAs are done and no remote arrive targets an exited CTA
+  if (!leader && warp == WARP_PRODUCER && lane == 0 && prod_issued != 0 && *abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 200000ull) {
+    }
+  }
+  cluster_sync_all();   // the second CTA's copies have landed on the leader's barriers
   if (warp == WARP_MMA) {
     __syncwarp();
     tc_fence_after();
@@ -1132,6 +1136,18 @@ __global__ void __launch_bounds__(1024) k_schedule(const int32_t* split, int E, 
 }
 
 // ---- host side -------------------------------------------------------------------------------
+
+// Limit of every pipeline wait: 2 s, or the value in ns of the environment variable
+// MXFP8MOE_WAIT_LIMIT_NS when it holds a positive integer (read at each call; failure-path tests
+// use it to make waits run out without any change to the kernels).  Teardown waits for copies and
+// MMAs in flight always keep the full 2 s.
+uint64_t pipeline_wait_ns() {
+  const char* v = getenv("MXFP8MOE_WAIT_LIMIT_NS");
+  if (v == nullptr || *v == 0) return kWaitTimeoutNs;
+  char* end = nullptr;
+  const unsigned long long n = strtoull(v, &end, 10);
+  return (end != nullptr && *end == 0 && n > 0) ? static_cast<uint64_t>(n) : kWaitTimeoutNs;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1322,7 +1338,8 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p1.hsf = hsf;
   p1.ldh = F;
   p1.err = &meta->error;
-  p1.timeout_ns = kWaitTimeoutNs;
+  p1.timeout_ns = pipeline_wait_ns();
+  p1.drain_ns = kWaitTimeoutNs;
   p1.a_kt = p1.KT;
   p1.b_kt = p1.KT;
   p1.a_sf_tiles = static_cast<int>(L.r_pad / BM);
@@ -1354,7 +1371,8 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p2.y = static_cast<uint16_t*>(y);
   p2.ldy = H;
   p2.err = &meta->error;
-  p2.timeout_ns = kWaitTimeoutNs;
+  p2.timeout_ns = p1.timeout_ns;
+  p2.drain_ns = kWaitTimeoutNs;
   p2.a_kt = p2.KT;
   p2.b_kt = p2.KT;
   p2.a_sf_tiles = static_cast<int>(L.r_pad / BM);
@@ -1470,7 +1488,8 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   base.E = E;
   base.F = static_cast<int>(F);
   base.err = &meta->error;
-  base.timeout_ns = kWaitTimeoutNs;
+  base.timeout_ns = pipeline_wait_ns();
+  base.drain_ns = kWaitTimeoutNs;
   int st;
 
   // 1: dh = dy W2 (W2 quantized along H) with the ScaledSwiGLU backward -> dGU, h, dgate parts

@@ -9,12 +9,16 @@
 // caller-provided workspace.  The caller still passes every input and output buffer.
 //
 // Facts a caller must know:
-//   - The array is kNoAllocScratchBytes (64 MiB) on every GPU that loads this library, held
-//     until the process exits.  Problems whose workspace (grouped_mlp_workspace_size) exceeds it
-//     are rejected with MXFP8_ERR_WORKSPACE before anything is enqueued.
-//   - The array's device address is looked up once per device (cudaGetSymbolAddress with that
-//     device current) by the first call made on that device; make that first call before any
-//     stream capture.
+//   - The array is kNoAllocScratchBytes (64 MiB).  It lives in a module of its own, which CUDA
+//     loads (lazy module loading, the default) on the first call made on a device; from then on
+//     that device holds it until the process exits.  Problems whose workspace
+//     (grouped_mlp_workspace_size) exceeds it are rejected with MXFP8_ERR_WORKSPACE before
+//     anything is enqueued.
+//   - The first call on a device is the set-up call: with that device current it looks up the
+//     array's device address (cudaGetSymbolAddress), which makes CUDA load the array, and it sets
+//     the kernels' launch attributes, which loads the library's kernels.  Both take device memory
+//     inside the driver, so make that first call on each device while allocation is still
+//     allowed, and before any stream capture.  Calls after it allocate nothing.
 //   - Every call on a device shares the one array and leaves the last call's contents in it.
 //     Nothing in it needs to start at zero: each call rewrites the schedule, the error word and
 //     every scratch row it reads.  Calls that overlap on the GPU (different streams, or
@@ -22,8 +26,8 @@
 //   - Device-side conditions (split_sizes that do not sum to R, a timed-out wait) are recorded
 //     in the array's error word, which this entry point does not expose; callers that need to
 //     read them use grouped_mlp_fwd with their own workspace.
-//   - No call here allocates or frees memory (no cudaMalloc/cudaFree or allocating library
-//     routine).
+//   - No call here calls cudaMalloc, cudaFree or an allocating library routine; after the
+//     set-up call on a device, nothing on that device is allocated at all.
 #include <cuda_runtime.h>
 
 #include <mutex>

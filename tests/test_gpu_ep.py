@@ -3,6 +3,10 @@ GPU): the exchanges are copies, so the layer must equal the single-GPU MoE layer
 grouped_mlp_fwd_tokens -> moe_combine, and its backward) bit for bit.  Also the row gather the
 layer moves rows with (moe_gather_rows), bit-exact against numpy indexing.
 
+The expert-parallel layer's forward output, input gradient and routing-weight gradients are
+also put beside the oracle's combined layer directly (element by element at the forward's y
+tolerances), on every token of the tiny workload and on sampled tokens of the Mixtral-shaped one.
+
 Page "Efficient MoE training for biological foundation models", How to run the recipe (experts
 spread over the GPUs) and Key technical approaches item 1.  The exchange logic over several ranks
 is covered on CPU by tests/test_ep_gloo.py.
@@ -133,3 +137,53 @@ def test_one_rank_training_equals_the_moe_layer(mx, nccl_group, with_gates):
         assert np.array_equal(bits(dg), bits(dg_rows[ros.long()]))
     else:
         assert dg is None
+
+
+def _tokens(w, name):
+    if name == "tiny":
+        return np.arange(w.T)
+    rng = np.random.default_rng(5)
+    return np.unique(np.concatenate([[0, 1, w.T - 1], rng.choice(w.T, 21, replace=False)]))
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral"])
+def test_ep_layer_forward_and_backward_match_oracle(mx, nccl_group, oracle, name):
+    """ep_moe_forward_train -> ep_moe_backward on one NCCL rank against the oracle: the oracle's
+    own permutation of the router choices, its binary64 forward and backward of the sorted rows
+    (the output gradient of row r is d_out[token_of_row[r]]), and its combine."""
+    import torch
+    from mxfp8_block_scaled_03_gb300 import ep
+    w = W.moe_workload(name)
+    x = G.to_dev_bf16(w.x_tokens)
+    ex = G.to_dev(w.topk_experts.astype(np.int32))
+    g = G.to_dev(w.topk_gates)
+    w1, w2 = G.to_dev_bf16(w.w1), G.to_dev_bf16(w.w2)
+    wts = _weights(mx, w)
+    w1t = mx.mxfp8_quantize_colwise_t(w1)
+    w2t = mx.mxfp8_quantize_colwise_t(w2)
+    d_out = W.bf16_bits(np.random.default_rng(8).standard_normal((w.T, w.H)).astype(np.float32))
+    out, ctx = ep.ep_moe_forward_train(x, ex, g, wts, w.E)
+    out_inf = ep.ep_moe_forward(x, ex, g, wts, w.E)
+    dx, dg, _, _ = ep.ep_moe_backward(G.to_dev_bf16(d_out), ctx, (w1t[0], w1t[1], w2t[0], w2t[1]))
+    torch.cuda.synchronize()
+    f64 = lambda t: t.float().cpu().numpy().astype(np.float64)
+    out, out_inf, dx, dg = f64(out), f64(out_inf), f64(dx), dg.cpu().numpy().astype(np.float64)
+
+    split, ros, tor, gs = oracle.moe_permute(w.topk_experts, w.topk_gates, w.E)
+    x_sorted = w.x_tokens[tor]
+    toks = _tokens(w, name)
+    rows = ros[toks].reshape(-1)
+    o1q, o1s = oracle.quantize_rowwise(w.w1)
+    o2q, o2s = oracle.quantize_rowwise(w.w2)
+    o2tq, o2ts = oracle.quantize_transposed(w.w2, w.E)
+    o1tq, o1ts = oracle.quantize_transposed(w.w1, w.E)
+    y_ref, _, _ = oracle.grouped_mlp_rows(x_sorted, split, gs, o1q, o1s, o2q, o2s, rows, want_intermediate=False)
+    out_ref = y_ref.reshape(len(toks), w.topk, w.H).sum(axis=1)
+    rdx, rdg, _, _ = oracle.grouped_mlp_bwd_rows(x_sorted, split, gs, o1q, o1s, o2tq, o2ts, o1tq, o1ts,
+                                                 d_out[tor], rows)
+    dx_ref = rdx.reshape(len(toks), w.topk, w.H).sum(axis=1)
+    dg_ref = rdg.reshape(len(toks), w.topk)
+    for what, got, ref in (("forward (training)", out[toks], out_ref), ("forward", out_inf[toks], out_ref),
+                           ("dx", dx[toks], dx_ref), ("d gates", dg[toks], dg_ref)):
+        rel, mxe = G.y_errors(got, ref)
+        assert rel <= G.Y_REL_TOL and mxe <= G.Y_MAX_TOL, f"{what}: rel {rel:.3e} max {mxe:.3e}"
