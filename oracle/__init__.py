@@ -20,7 +20,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "mxfp8_oracle.c")
+_SRCS = [os.path.join(_HERE, "mxfp8_oracle.c"), os.path.join(_HERE, "nvfp4_oracle.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
@@ -34,10 +34,11 @@ SPLIT_MISMATCH = 6
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (no FMA contraction, so x86-64 and aarch64 agree)."""
     os.makedirs(_BUILD, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB_PATH) or any(os.path.getmtime(_LIB_PATH) < os.path.getmtime(p)
+                                                      for p in _SRCS):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-                               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+                               "-ffp-contract=off", *_SRCS, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -78,6 +79,28 @@ def lib() -> ctypes.CDLL:
                                                  ctypes.c_int, P, i64, P, ctypes.c_int, ctypes.c_int]
             L.ora_round_bf16.restype = ctypes.c_double
             L.ora_round_bf16.argtypes = [ctypes.c_double]
+            f32 = ctypes.c_float
+            L.ora_e2m1_decode.restype = ctypes.c_double
+            L.ora_e2m1_decode.argtypes = [ctypes.c_uint8]
+            L.ora_e2m1_encode.restype = ctypes.c_uint8
+            L.ora_e2m1_encode.argtypes = [ctypes.c_double]
+            L.ora_e2m1_encode_array.restype = None
+            L.ora_e2m1_encode_array.argtypes = [P, i64, P]
+            L.ora_nvfp4_encode_scale.restype = f32
+            L.ora_nvfp4_encode_scale.argtypes = [f32]
+            L.ora_nvfp4_quantize_block.restype = ctypes.c_uint8
+            L.ora_nvfp4_quantize_block.argtypes = [P, ctypes.c_int, f32, P]
+            L.ora_nvfp4_dequant.restype = ctypes.c_double
+            L.ora_nvfp4_dequant.argtypes = [ctypes.c_uint8, ctypes.c_uint8, f32]
+            L.ora_bf16_amax.restype = f32
+            L.ora_bf16_amax.argtypes = [P, i64]
+            L.ora_nvfp4_quantize_rowwise.restype = ctypes.c_int
+            L.ora_nvfp4_quantize_rowwise.argtypes = [P, i64, i64, P, P, P, ctypes.c_int]
+            L.ora_nvfp4_quantize_f32.restype = ctypes.c_int
+            L.ora_nvfp4_quantize_f32.argtypes = [P, i64, i64, f32, P, P]
+            L.ora_nvfp4_grouped_mlp_rows.restype = ctypes.c_int
+            L.ora_nvfp4_grouped_mlp_rows.argtypes = [P, i64, i64, i64, ctypes.c_int, P, P, P, P, f32, P, P, f32, f32,
+                                                     P, i64, P, P, P, P, ctypes.c_int]
             L.ora_moe_combine.restype = ctypes.c_int
             L.ora_moe_combine.argtypes = [P, P, i64, ctypes.c_int, i64, P]
             _lib = L
@@ -272,3 +295,96 @@ def grouped_mlp_bwd_dw(x_bf16, split_sizes, gates, w1q, w1sf, w2tq, w2tsf, dy_bf
     if rc != OK:
         raise ValueError(f"oracle grouped_mlp_bwd_dw rejected the arguments (status {rc})")
     return out
+
+
+# ------------------------------------------------------------------------------------------------
+# NVFP4 (nvfp4_oracle.c): E2M1 codes one per byte (sign in bit 3), E4M3 block-scale codes per 16
+# values, per-tensor binary32 encode scale s_enc = 2688 / amax.
+# ------------------------------------------------------------------------------------------------
+def e2m1_decode(codes: np.ndarray) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.vectorize(lambda v: lib().ora_e2m1_decode(int(v)), otypes=[np.float64])(c)
+
+
+def e2m1_encode(values: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib().ora_e2m1_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def nvfp4_encode_scale(amax: float) -> float:
+    return float(lib().ora_nvfp4_encode_scale(float(amax)))
+
+
+def nvfp4_quantize_block(values, s_enc: float) -> tuple[np.ndarray, int]:
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    assert 0 < v.size <= 16
+    codes = np.empty(v.size, dtype=np.uint8)
+    sf = lib().ora_nvfp4_quantize_block(_ptr(v), v.size, float(s_enc), _ptr(codes))
+    return codes, int(sf)
+
+
+def nvfp4_quantize_rowwise(x_bf16: np.ndarray, nthreads: int | None = None):
+    """[M, K] bf16 bits -> (E2M1 codes [M, K] one per byte, E4M3 scale codes [M, K/16], s_enc)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), dtype=np.uint8)
+    sf = np.empty((M, K // 16), dtype=np.uint8)
+    s = ctypes.c_float(0.0)
+    rc = lib().ora_nvfp4_quantize_rowwise(_ptr(x), M, K, _ptr(q), _ptr(sf), ctypes.byref(s),
+                                          nthreads or default_threads())
+    if rc != OK:
+        raise ValueError(f"oracle nvfp4_quantize_rowwise rejected the arguments (status {rc})")
+    return q, sf, float(s.value)
+
+
+def nvfp4_quantize_f32(v: np.ndarray, s_enc: float):
+    """Row-wise NVFP4 of binary32 values [M, K] under a given encode scale."""
+    a = np.ascontiguousarray(v, dtype=np.float32)
+    M, K = a.shape
+    q = np.empty((M, K), dtype=np.uint8)
+    sf = np.empty((M, K // 16), dtype=np.uint8)
+    rc = lib().ora_nvfp4_quantize_f32(_ptr(a), M, K, float(s_enc), _ptr(q), _ptr(sf))
+    if rc != OK:
+        raise ValueError(f"oracle nvfp4_quantize_f32 rejected the arguments (status {rc})")
+    return q, sf
+
+
+def nvfp4_dequantize(q: np.ndarray, sf: np.ndarray, s_enc: float) -> np.ndarray:
+    """Value of row-wise NVFP4 codes [.., K] with block-scale codes [.., K/16], in binary64."""
+    vals = e2m1_decode(q)
+    return vals * np.repeat(e4m3_decode(sf), 16, axis=-1) / np.float64(np.float32(s_enc))
+
+
+def bf16_amax(x_bf16: np.ndarray) -> float:
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    return float(lib().ora_bf16_amax(_ptr(x), x.size))
+
+
+def nvfp4_grouped_mlp_rows(x_bf16, split_sizes, gates, w1, w2, h_amax: float, rows, nthreads=None,
+                           want_intermediate=True):
+    """Rows of the NVFP4 grouped MLP forward in binary64.  w1 = (codes, scale codes, s_enc) of
+    W1 [E*2F, H] and w2 likewise of W2 [E*H, F], as nvfp4_quantize_rowwise returns them.
+    Returns (y [n, H], hq [n, F] codes, hsf [n, F/16] scale codes, s_x)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    R, H = x.shape
+    split = np.ascontiguousarray(split_sizes, dtype=np.int32)
+    E = split.size
+    F = w2[0].shape[1]
+    g = None if gates is None else np.ascontiguousarray(gates, dtype=np.float32)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.size
+    y = np.empty((n, H), dtype=np.float64)
+    hq = np.empty((n, F), dtype=np.uint8) if want_intermediate else None
+    hsf = np.empty((n, F // 16), dtype=np.uint8) if want_intermediate else None
+    w1q, w1s = (np.ascontiguousarray(a, dtype=np.uint8) for a in w1[:2])
+    w2q, w2s = (np.ascontiguousarray(a, dtype=np.uint8) for a in w2[:2])
+    s_x = ctypes.c_float(0.0)
+    rc = lib().ora_nvfp4_grouped_mlp_rows(_ptr(x), R, H, F, E, _ptr(split), _ptr(g), _ptr(w1q), _ptr(w1s),
+                                          float(w1[2]), _ptr(w2q), _ptr(w2s), float(w2[2]), float(h_amax),
+                                          _ptr(rows), n, _ptr(y), _ptr(hq), _ptr(hsf), ctypes.byref(s_x),
+                                          nthreads or default_threads())
+    if rc != OK:
+        raise ValueError(f"oracle nvfp4_grouped_mlp_rows rejected the arguments (status {rc})")
+    return y, hq, hsf, float(s_x.value)

@@ -146,7 +146,7 @@ static void* ora_job_main(void* p) {
     return NULL;
 }
 
-static void ora_parallel(ora_range_fn fn, void* ctx, int64_t n, int nthreads) {
+void ora_parallel(ora_range_fn fn, void* ctx, int64_t n, int nthreads) {
     pthread_t th[256];
     ora_job jobs[256];
     int t;

@@ -97,3 +97,27 @@ def bf16_round(v: np.ndarray) -> np.ndarray:
     pick = np.where(tie, tb, best)
     out = np.take_along_axis(vals, pick[None], axis=0)[0]
     return np.where(np.signbit(v), -out, out)
+
+
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)   # codes 0..7 (format definition)
+
+
+def e2m1_nearest_code(t: np.ndarray) -> np.ndarray:
+    """Brute-force nearest E2M1 code by search over the eight magnitudes; ties -> even code;
+    |t| > 6 -> 6; sign (also of zero) in bit 3."""
+    t = np.asarray(t, dtype=np.float64)
+    a = np.abs(t)
+    mags = np.array(E2M1_MAGNITUDES)
+    d = np.abs(a[..., None] - mags)
+    best = d.min(axis=-1, keepdims=True)
+    cand = np.where(d == best, np.arange(8), 99)
+    even = np.where(cand % 2 == 0, cand, 99).min(axis=-1)
+    pick = np.where(even < 99, even, cand.min(axis=-1))
+    pick = np.where(a >= 6.0, 7, pick)
+    return (pick | (np.signbit(t).astype(np.int64) << 3)).astype(np.uint8)
+
+
+def e2m1_value(codes: np.ndarray) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.int64)
+    mag = np.array(E2M1_MAGNITUDES)[c & 7]
+    return np.where(c & 8, -mag, mag)
