@@ -38,6 +38,7 @@ WORKLOAD = "mixtral"
 QUANT_SHAPE = (16384, 14336)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 vs 2.25 PFLOP/s per GPU)
+FP4_OVER_BF16 = 6.0          # nominal dense ratio (13.5 vs 2.25 PFLOP/s per GPU)
 KERNEL_SOURCES = ["mxfp8_block_scaled_03_gb300/csrc/grouped_gemm.cu", "mxfp8_block_scaled_03_gb300/csrc/mx_device.cuh",
                   "mxfp8_block_scaled_03_gb300/csrc/quantize.cu"]
 
@@ -345,30 +346,34 @@ def library_mxfp8_gemms(R, H, F, dev, iters=10):
     return out
 
 
-def mma_loop_peak(mx, dev):
+def mma_loop_peak(mx, dev, fmt=0):
     """The library's own back-to-back block-scaled pair-MMA loop (mxfp8_mma_peak): TFLOP/s of the
-    tensor pipe with operands resident in shared memory."""
+    tensor pipe with operands resident in shared memory (fmt 0: MXFP8, K = 32 per MMA; fmt 1:
+    NVFP4, K = 64 per MMA)."""
     import torch
     ws = torch.zeros(64, dtype=torch.uint8, device=dev)
     iters = 1 << 18
-    mx.mxfp8_mma_peak(iters // 16, ws)
+    kmma = 64 if fmt == 1 else 32
+    mx.mxfp8_mma_peak(iters // 16, ws, fmt)
     torch.cuda.synchronize()
     best = None
     for _ in range(3):
         e0, e1 = _events(2)
         e0.record()
-        n = mx.mxfp8_mma_peak(iters, ws)
+        n = mx.mxfp8_mma_peak(iters, ws, fmt)
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
-        tf = n * iters * 4 * 2.0 * 256 * 256 * 32 / (ms * 1e-3) / 1e12
+        tf = n * iters * 4 * 2.0 * 256 * 256 * kmma / (ms * 1e-3) / 1e12
         best = tf if best is None else max(best, tf)
     st, bits = mx.mxfp8_check_device_error(ws)
     if st != 0:
         raise RuntimeError(f"MMA peak loop error word {bits:#x}")
+    kind = "kind::mxf4nvf4.block_scale.scale_vec::4X M=256 N=256 K=64" if fmt == 1 else \
+        "kind::mxf8f6f4.block_scale M=256 N=256 K=32"
     return {"tflops": best, "clusters": n, "mma_per_cluster": 4 * iters,
-            "kind": "mxfp8_mma_peak: tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale M=256 N=256 K=32, "
-                    "operands resident in shared memory, best of 3 launches"}
+            "kind": f"mxfp8_mma_peak: tcgen05.mma.cta_group::2.{kind}, operands resident in shared memory, "
+                    "best of 3 launches"}
 
 
 def workload_config(w):
@@ -514,6 +519,67 @@ def quantize_sweep(mx, dev, peaks, steps):
             del buf
         del x
     del flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def nvfp4_forward(mx, fwd, steps, warmup, peaks):
+    """The NVFP4 variant of the same forward (nvfp4_grouped_mlp_fwd) on the same resident inputs:
+    weights quantized once to NVFP4 (timed apart), the intermediate's encode scale from the largest
+    |h| a first call observed (the delayed scaling a training loop would use)."""
+    import torch
+    w = fwd.w
+    R, H, F, E = w.R, w.H, w.F, w.E
+    out = {}
+    t0, t1 = _events(2)
+    w1 = mx.nvfp4_quantize(fwd.w1_bf16, sf_layout=mx.SF_MMA)
+    w2 = mx.nvfp4_quantize(fwd.w2_bf16, sf_layout=mx.SF_MMA)
+    t0.record()
+    mx.nvfp4_quantize(fwd.w1_bf16, sf_layout=mx.SF_MMA, out=w1)
+    mx.nvfp4_quantize(fwd.w2_bf16, sf_layout=mx.SF_MMA, out=w2)
+    t1.record()
+    torch.cuda.synchronize()
+    out["weight_quantize_ms"] = t0.elapsed_time(t1)
+    ws = torch.empty(mx.nvfp4_grouped_mlp_workspace_size(R, H, F, E), dtype=torch.uint8, device=fwd.dev)
+    y = torch.empty((R, H), dtype=torch.bfloat16, device=fwd.dev)
+    lay = mx.nvfp4_grouped_mlp_workspace_layout(R, H, F, E)
+    mx.nvfp4_grouped_mlp_fwd(fwd.x, fwd.split, fwd.gates, w1, w2, 1.0, y=y, workspace=ws)
+    torch.cuda.synchronize()
+    h_amax = float(ws[lay[1] + 4:lay[1] + 8].view(torch.float32).item())
+    out["h_amax"] = h_amax
+
+    def step(evs=None):
+        mx.nvfp4_grouped_mlp_fwd(fwd.x, fwd.split, fwd.gates, w1, w2, h_amax, y=y, workspace=ws, stage_events=evs)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    st, bits = mx.mxfp8_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {bits:#x} in the NVFP4 forward")
+    sev = [_events(5) for _ in range(steps)]
+    for evs in sev:
+        for ev in evs:
+            ev.record()
+    torch.cuda.synchronize()
+    a0, a1 = _events(2)
+    a0.record()
+    for i in range(steps):
+        step(sev[i])
+    a1.record()
+    torch.cuda.synchronize()
+    ms = a0.elapsed_time(a1) / steps
+    names = ["schedule", "amax_quantize_x", "grouped_linear1_swiglu_requant", "grouped_linear2"]
+    km = {n: sum(e[j].elapsed_time(e[j + 1]) for e in sev) / steps for j, n in enumerate(names)}
+    nominal = peaks["bf16_tflops"] * FP4_OVER_BF16
+    g1 = 4.0 * R * H * F / (km["grouped_linear1_swiglu_requant"] * 1e-3) / 1e12
+    g2 = 2.0 * R * H * F / (km["grouped_linear2"] * 1e-3) / 1e12
+    out.update({"ms": ms, "tflops": fwd.flops / (ms * 1e-3) / 1e12, "kernel_ms": km,
+                "grouped_linear1": {"tflops": g1, "frac": g1 / nominal},
+                "grouped_linear2": {"tflops": g2, "frac": g2 / nominal},
+                "peak": nominal, "peak_source": f"bf16_tflops x {FP4_OVER_BF16:.0f} (nominal dense fp4/bf16 ratio)",
+                "dtype": "e2m1 (UE4M3 block scales, fp32 accumulate)"})
+    del ws, y, w1, w2
     torch.cuda.empty_cache()
     return out
 
@@ -739,6 +805,16 @@ def run_native(args, world, rank, local):
 
     bwd = measure_backward()
 
+    # ---- the NVFP4 variant of the same forward ----
+    nv = None
+    if args.only == "all" and H % 256 == 0:
+        nv = nvfp4_forward(mx, fwd, max(args.steps, 10), max(3, args.warmup), peaks)
+        nv_mma = mma_loop_peak(mx, dev, fmt=1)
+        nv["mma_loop_peak"] = nv_mma
+        nv["frac_of_measured_nvfp4_peak"] = nv["tflops"] / nv_mma["tflops"]
+        for k in ("grouped_linear1", "grouped_linear2"):
+            nv[k]["frac_of_measured_nvfp4_peak"] = nv[k]["tflops"] / nv_mma["tflops"]
+
     # ---- the other configurations of the sweep: forward of each, per kernel ----
     configs = {}
     if args.workload == "mixtral" and args.only == "all" and not args.no_configs:
@@ -863,7 +939,8 @@ def run_native(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
             "config": workload_config(w), "roofline": roofline, "peak_mxfp8_measured": peak_measured,
-            "quantize": quant, "quantize_sweep": sweep, "configs": configs, "moe_layer": layer, "backward": bwd,
+            "quantize": quant, "quantize_sweep": sweep, "configs": configs, "nvfp4": nv, "moe_layer": layer,
+            "backward": bwd,
             "e2e": e2e, "library_context": lib,
             "cpu_baseline": cpu, "clocks": clocks, "gpu_launches": 4 * args.steps,
             "weight_quantize_ms": fwd.weight_quant_ms, "peaks": {"source": peak_src, **peaks},

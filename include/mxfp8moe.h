@@ -311,17 +311,80 @@ int grouped_mlp_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_
  * *flags when flags is not NULL (host). */
 int mxfp8_check_device_error(const void* workspace, void* stream, uint32_t* flags);
 
+/*
+ * NVFP4 variant of the chain.  The page "TransformerEngine-accelerated Llama 3 training with
+ * native PyTorch training loop" lists NVFP4 beside MXFP8 among its quantized-training recipes
+ * (feature table; section "Quantized Training (FP8 / MXFP8 / NVFP4)") and defines nothing of
+ * it; this library takes NVIDIA's published NVFP4:
+ *   - elements E2M1 (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 with a sign), stored two per byte: value
+ *     2i of a row in the low nibble of byte i, value 2i+1 in its high nibble, sign in bit 3;
+ *   - one E4M3 scale code per 16 consecutive values of a row;
+ *   - one binary32 encode scale per tensor, s_enc = 448 * 6 / amax(tensor) (1 if amax = 0, at
+ *     most FLT_MAX), kept as the tensor's amax (a device float);
+ *   - block quantization in binary32, round to nearest even, saturating:
+ *       S = E4M3(fl32(fl32(amax_block / 6) * s_enc)),  r = fl32(s_enc / S) (0 if S = 0),
+ *       code_i = E2M1(fl32(v_i * r));  the pair stands for code_i * S / s_enc.
+ * Scale layouts: MXFP8_SF_COMPACT is [M, K/16] row-major.  MXFP8_SF_MMA is the tensor-core
+ * layout of MXFP8_SF_MMA with 16-value blocks in place of 32-value ones and each row's blocks
+ * padded to a multiple of 16 (K to a multiple of 256) with zero codes: atom (rt, kt) of 128
+ * rows x 4 blocks at byte 512 * (rt * 4*ceil(K/256) + kt), row 32j+i, block 4kt+b at 16i+4j+b.
+ *
+ * nvfp4_sf_bytes -- bytes of the scale-code buffer (0 on bad arguments).
+ * nvfp4_quantize -- NVFP4 of a bf16 matrix.
+ *   x    (device) bf16 [M, K] row-major, finite.   q (device, out) codes [M, K/2].
+ *   sf   (device, out) nvfp4_sf_bytes(M, K, sf_layout) bytes.
+ *   amax (device, out) float: max |x| over the whole matrix (it defines s_enc; pass it to
+ *        nvfp4_grouped_mlp_fwd with the codes).  Two kernels: a reduction for amax, then the
+ *        quantization.
+ *   Requirements: K % 16 == 0; with MXFP8_SF_MMA also M % 128 == 0, K % 128 == 0; 16-byte aligned
+ *   x and q, 4-byte aligned amax.  Results are bit-exact with the rule above.
+ */
+size_t nvfp4_sf_bytes(int64_t M, int64_t K, int sf_layout);
+int nvfp4_quantize(const void* x, int64_t M, int64_t K, int sf_layout, uint8_t* q, uint8_t* sf, float* amax,
+                   void* stream);
+
+/*
+ * nvfp4_grouped_mlp_fwd -- grouped_mlp_fwd with NVFP4 operands (tcgen05 kind::mxf4nvf4 block-scaled
+ * MMA, CTA pairs):
+ *     xq_r = NVFP4 of x_sorted row r under the encode scale of max|x_sorted| (computed inside);
+ *     g, u = xq_r W1[e, gate/up]^T, h = gate_r * silu(g) * u  (fp32 accumulation, dequantized by
+ *            1 / (s_x s_w1));
+ *     hq = NVFP4 of h along F under the encode scale of h_amax (values beyond it saturate: the
+ *          intermediate's largest value is not known before GroupedLinear 1 has run, so the
+ *          caller supplies the magnitude, e.g. the one the previous call observed);
+ *     y_r = bf16( hq W2[e]^T / (s_h s_w2) ).
+ *   w1_q/w1_sf/w1_amax: nvfp4_quantize(W1 [E*2F, H], MXFP8_SF_MMA) outputs (rows [0, F) of each
+ *   expert gate, [F, 2F) up); w2_q/w2_sf/w2_amax: the same for W2 [E*H, F].
+ *   h_amax (host) > 0.  stage_events: NULL, or 5 caller-created events recorded around the
+ *   schedule, activation amax + quantize, GroupedLinear 1 (+ScaledSwiGLU, requant) and
+ *   GroupedLinear 2 stages.  Other arguments as grouped_mlp_fwd; the workspace
+ *   (nvfp4_grouped_mlp_workspace_size bytes, 256-byte aligned) also receives, as float bits, the
+ *   largest |x| and the largest |h| the call saw (nvfp4_grouped_mlp_workspace_layout entry 1:
+ *   two words).  Requirements: H % 256 == 0, F % 128 == 0, 1 <= E <= 1024, a GPU where two-CTA
+ *   clusters fit (MXFP8_ERR_UNSUPPORTED otherwise).  Device-side errors as for grouped_mlp_fwd.
+ * nvfp4_grouped_mlp_workspace_layout -- byte offsets: [0] error word, [1] the two amax words,
+ *   [2] x codes [R_pad, H/2], [3] their scale codes (MXFP8_SF_MMA), [4] h codes [R_pad, F/2],
+ *   [5] their scale codes (MXFP8_SF_MMA), [6] R_pad (not an offset).  out: 7 entries (host).
+ */
+size_t nvfp4_grouped_mlp_workspace_size(int64_t R, int64_t H, int64_t F, int E);
+int nvfp4_grouped_mlp_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_t* out);
+int nvfp4_grouped_mlp_fwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
+                          const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const float* w1_amax,
+                          const uint8_t* w2_q, const uint8_t* w2_sf, const float* w2_amax, float h_amax, void* y,
+                          void* workspace, size_t workspace_bytes, void* stream, void* const* stage_events);
+
 /* mxfp8_mma_peak -- measurement aid, with no counterpart on the pages: the rate of the
  * block-scaled tensor-core instruction this library's GEMMs are built on, on the device at hand
  * (the roofline their TFLOP/s are reported against).  Launches one cluster of two CTAs per pair
  * of SMs (as many as fit; their number goes to *clusters, host); each cluster issues `iters`
- * K steps of four tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale (M = 256, N = 256, K = 32,
- * E4M3 x E4M3, UE8M0 scales) back to back on operands resident in shared memory, so one launch
- * performs clusters * iters * 4 * 2*256*256*32 floating-point operations; time it with events
- * on `stream`.  workspace (device, 4-byte aligned, >= 4 bytes) receives an error word
- * (mxfp8_check_device_error reports MXFP8_ERR_DEVICE_TIMEOUT if the final wait ran out).
- * Requirements: 0 <= iters <= 2^24. */
-int mxfp8_mma_peak(int64_t iters, void* workspace, int* clusters, void* stream);
+ * K steps of four tcgen05.mma.cta_group::2 block-scaled MMAs (M = 256, N = 256) back to back on
+ * operands resident in shared memory: format 0 = kind::mxf8f6f4 (E4M3, UE8M0 scales, K = 32), so
+ * one launch performs clusters * iters * 4 * 2*256*256*32 floating-point operations; format 1 =
+ * kind::mxf4nvf4 (E2M1, UE4M3 scales, K = 64): clusters * iters * 4 * 2*256*256*64.  Time it
+ * with events on `stream`.  workspace (device, 4-byte aligned, >= 4 bytes) receives an error
+ * word (mxfp8_check_device_error reports MXFP8_ERR_DEVICE_TIMEOUT if the final wait ran out).
+ * Requirements: 0 <= iters <= 2^24, format 0 or 1. */
+int mxfp8_mma_peak(int64_t iters, int format, void* workspace, int* clusters, void* stream);
 
 /* Static description of a status code. */
 const char* mxfp8_status_string(int status);

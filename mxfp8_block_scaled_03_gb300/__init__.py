@@ -33,7 +33,8 @@ __all__ = [
     "moe_permute_workspace_size", "moe_combine", "moe_gather_rows", "mxfp8_check_device_error", "mxfp8_quantize_colwise_t",
     "grouped_mlp_saved_bytes", "grouped_mlp_fwd_train", "grouped_mlp_bwd_workspace_size", "grouped_mlp_bwd",
     "grouped_mlp_fwd_tokens_train", "grouped_mlp_bwd_tokens", "mxfp8_status_string", "mxfp8_abi_version",
-    "mxfp8_mma_peak",
+    "mxfp8_mma_peak", "nvfp4_sf_bytes", "nvfp4_quantize", "nvfp4_grouped_mlp_workspace_size",
+    "nvfp4_grouped_mlp_workspace_layout", "nvfp4_grouped_mlp_fwd",
 ]
 
 ROWWISE = 1
@@ -115,8 +116,19 @@ def lib() -> ctypes.CDLL:
             L.moe_gather_rows.argtypes = [P, i64, i64, P, i64, P, P]
             L.mxfp8_check_device_error.restype = i32
             L.mxfp8_check_device_error.argtypes = [P, P, P]
+            f32 = ctypes.c_float
+            L.nvfp4_sf_bytes.restype = sz
+            L.nvfp4_sf_bytes.argtypes = [i64, i64, i32]
+            L.nvfp4_quantize.restype = i32
+            L.nvfp4_quantize.argtypes = [P, i64, i64, i32, P, P, P, P]
+            L.nvfp4_grouped_mlp_workspace_size.restype = sz
+            L.nvfp4_grouped_mlp_workspace_size.argtypes = [i64, i64, i64, i32]
+            L.nvfp4_grouped_mlp_workspace_layout.restype = i32
+            L.nvfp4_grouped_mlp_workspace_layout.argtypes = [i64, i64, i64, i32, P]
+            L.nvfp4_grouped_mlp_fwd.restype = i32
+            L.nvfp4_grouped_mlp_fwd.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, f32, P, P, sz, P, P]
             L.mxfp8_mma_peak.restype = i32
-            L.mxfp8_mma_peak.argtypes = [i64, P, P, P]
+            L.mxfp8_mma_peak.argtypes = [i64, i32, P, P, P]
             _lib = L
     return _lib
 
@@ -447,11 +459,75 @@ def moe_gather_rows(src, index, out=None, stream=None):
     return out
 
 
-def mxfp8_mma_peak(iters: int, workspace, stream=None) -> int:
-    """Enqueue the block-scaled MMA rate measurement (see include/mxfp8moe.h); returns the number
-    of CTA-pair clusters launched.  `workspace`: a CUDA tensor of at least 4 bytes."""
+def nvfp4_sf_bytes(M: int, K: int, sf_layout: int = SF_COMPACT) -> int:
+    return int(lib().nvfp4_sf_bytes(M, K, sf_layout))
+
+
+def nvfp4_quantize(x, sf_layout: int = SF_COMPACT, out=None, stream=None):
+    """NVFP4 of a bf16 [M, K] CUDA tensor.  Returns (codes uint8 [M, K/2], scale codes uint8,
+    amax float32 [1]: max |x|, which defines the per-tensor encode scale).  `out` may pass the
+    three to be reused."""
+    import torch
+    M, K = x.shape
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous()
+    if out is None:
+        out = (torch.empty((M, K // 2), dtype=torch.uint8, device=x.device),
+               torch.empty(max(1, nvfp4_sf_bytes(M, K, sf_layout)), dtype=torch.uint8, device=x.device),
+               torch.empty(1, dtype=torch.float32, device=x.device))
+    q, sf, amax = out
+    _check(lib().nvfp4_quantize(_ptr(x), M, K, sf_layout, _ptr(q), _ptr(sf), _ptr(amax), _stream(stream)),
+           "nvfp4_quantize")
+    return q, sf, amax
+
+
+def nvfp4_grouped_mlp_workspace_size(R: int, H: int, F: int, E: int) -> int:
+    return int(lib().nvfp4_grouped_mlp_workspace_size(R, H, F, E))
+
+
+def nvfp4_grouped_mlp_workspace_layout(R: int, H: int, F: int, E: int) -> list[int]:
+    out = (ctypes.c_uint64 * 7)()
+    _check(lib().nvfp4_grouped_mlp_workspace_layout(R, H, F, E, out), "nvfp4_grouped_mlp_workspace_layout")
+    return list(out)
+
+
+def nvfp4_grouped_mlp_fwd(x_sorted, split_sizes, gates, w1, w2, h_amax: float, y=None, workspace=None, stream=None,
+                          stage_events=None):
+    """NVFP4 grouped expert MLP forward.  w1 = (codes, scale codes in SF_MMA layout, amax) from
+    nvfp4_quantize of W1 [E*2F, H]; w2 likewise of W2 [E*H, F]; h_amax: the magnitude the
+    intermediate's encode scale is derived from.  Returns y bf16 [R, H]."""
+    import torch
+    R, H = x_sorted.shape
+    E = int(split_sizes.numel())
+    F = int(w2[0].shape[1]) * 2
+    assert x_sorted.dtype == torch.bfloat16 and split_sizes.dtype == torch.int32
+    assert gates is None or gates.dtype == torch.float32
+    for t in (x_sorted, split_sizes, gates, *w1, *w2):
+        assert t is None or (t.is_cuda and t.is_contiguous())
+    if y is None:
+        y = torch.empty((R, H), dtype=torch.bfloat16, device=x_sorted.device)
+    if workspace is None:
+        workspace = torch.empty(nvfp4_grouped_mlp_workspace_size(R, H, F, E), dtype=torch.uint8,
+                                device=x_sorted.device)
+    ev = None
+    if stage_events is not None:   # 5 torch.cuda.Event(enable_timing=True), already recorded once
+        handles = [int(e.cuda_event) for e in stage_events]
+        if len(handles) != 5 or not all(handles):
+            raise ValueError("stage_events: 5 CUDA events that have been recorded at least once")
+        ev = (ctypes.c_void_p * 5)(*handles)
+    _check(lib().nvfp4_grouped_mlp_fwd(_ptr(x_sorted), R, H, F, E, _ptr(split_sizes), _ptr(gates), _ptr(w1[0]),
+                                       _ptr(w1[1]), _ptr(w1[2]), _ptr(w2[0]), _ptr(w2[1]), _ptr(w2[2]),
+                                       float(h_amax), _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream),
+                                       ev), "nvfp4_grouped_mlp_fwd")
+    return y
+
+
+def mxfp8_mma_peak(iters: int, workspace, fmt: int = 0, stream=None) -> int:
+    """Enqueue the block-scaled MMA rate measurement (see include/mxfp8moe.h; fmt 0 MXFP8, 1
+    NVFP4); returns the number of CTA-pair clusters launched.  `workspace`: a CUDA tensor of at
+    least 4 bytes."""
     n = ctypes.c_int(0)
-    _check(lib().mxfp8_mma_peak(int(iters), _ptr(workspace), ctypes.byref(n), _stream(stream)), "mxfp8_mma_peak")
+    _check(lib().mxfp8_mma_peak(int(iters), int(fmt), _ptr(workspace), ctypes.byref(n), _stream(stream)),
+           "mxfp8_mma_peak")
     return int(n.value)
 
 

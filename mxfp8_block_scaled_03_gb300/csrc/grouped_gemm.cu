@@ -100,6 +100,16 @@ static_assert(SFB_COL + 8 * STAGES <= TMEM_COLS, "TMEM budget");
 // GEMM_WGRAD   weight gradient of every expert: A^T B over the expert's rows (K varies by expert)
 enum GemmMode { GEMM_SWIGLU = 0, GEMM_OUT = 1, GEMM_DGRAD = 2, GEMM_WGRAD = 3 };
 
+// Operand formats of the pair kernel.
+//   FMT_MX  MXFP8: E4M3 bytes, one UE8M0 scale per 32 values of K.  A K step (BK = 128 bytes of a
+//           row) is four MMAs of K = 32 sharing one 512-byte scale atom per 128 rows (the MMA
+//           selects the byte of each 32-bit scale word).
+//   FMT_NV  NVFP4: packed E2M1 (two values per byte), one UE4M3 scale per 16 values.  A K step
+//           (128 bytes = 256 values of a row) is four MMAs of K = 64, each with its own atom of
+//           four scales per row: four atoms per 128 rows per step.  Only the forward GEMMs
+//           (GEMM_SWIGLU, GEMM_OUT) run on it.
+enum PairFmt { FMT_MX = 0, FMT_NV = 1 };
+
 struct GemmParams {
   const SchedHeader* meta;
   const uint8_t* a_sf;     // scale bytes of A (tensor-core layout, padded rows)
@@ -144,6 +154,13 @@ struct GemmParams {
                            // 0 when every tile is whole
   int64_t wg_m, wg_n;      // rows and columns of each expert's gradient block
   float* dw;               // [E, M, N] fp32
+  // NVFP4 operands (FMT_NV): the per-tensor magnitudes the encode scales 2688 / amax come from
+  const float* nv_amax_a;  // device (A = x: written by the amax kernel); NULL: nv_amax_a_val
+  float nv_amax_a_val;     // A = h in GroupedLinear 2: the caller's magnitude for the intermediate
+  const float* nv_amax_b;  // device: the weight's magnitude (written by its quantization)
+  float nv_out_amax;       // GEMM_SWIGLU: magnitude the intermediate's encode scale derives from
+  uint32_t* nv_out_seen;   // GEMM_SWIGLU: largest |h| of the call (float bits, atomicMax) or NULL
+  int64_t h_kt;            // GEMM_SWIGLU: scale atoms per 128-row tile of h
 };
 
 struct TileInfo {
@@ -246,10 +263,60 @@ __device__ __forceinline__ int64_t gu_offset(int64_t prow, int64_t j, int64_t tw
 //                h = gate_r * silu(G) * U, two 32-blocks requantized to E4M3 codes + E8M0 bytes
 //                (written straight into the tensor-core scale layout GroupedLinear 2 reads).
 //   GEMM_OUT:    v[0..BN/2) columns BN/2*half.. -> bf16, stored for the expert's real rows only.
-template <int MODE>
+//   NVFP4 (FMT_NV): accumulators are first multiplied by alpha = 1 / (s_a s_b), the product of the
+//                operands' per-tensor decode scales; GEMM_SWIGLU requantizes h to NVFP4 under the
+//                encode scale s_out (four 16-value blocks per thread, E4M3 block scales).
+template <int MODE, int FMT = FMT_MX>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& t, const uint32_t* v, int r,
-                                              int half, int BN) {
-  if (MODE == GEMM_SWIGLU) {
+                                              int half, int BN, float alpha = 1.0f, float s_out = 1.0f) {
+  if (MODE == GEMM_SWIGLU && FMT == FMT_NV) {
+    const bool real = r < t.valid;
+    const float gate = real ? (p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f) : 0.0f;
+    const int64_t prow = t.pad_row0 + r;
+    const int c0 = t.n * 128 + 64 * half;                     // first column of F this thread holds
+    const uint64_t one2 = f2_pack(1.0f, 1.0f), al2 = f2_pack(alpha, alpha), gate2 = f2_pack(gate, gate);
+    uint32_t q[8];
+    uint32_t sfw = 0;
+    float hmax = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {   // 16-value blocks
+      float h[16];
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = 16 * b + 2 * i;
+        const uint64_t g = f2_mul(f2_pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), al2);
+        const uint64_t up = f2_mul(f2_pack(__uint_as_float(v[64 + c]), __uint_as_float(v[64 + c + 1])), al2);
+        const uint64_t d = f2_add(f2_pack(__expf(-f2_lo(g)), __expf(-f2_hi(g))), one2);   // 1 + e^-g
+        const uint64_t sig = f2_pack(__fdividef(1.0f, f2_lo(d)), __fdividef(1.0f, f2_hi(d)));
+        const uint64_t hv = f2_mul(f2_mul(f2_mul(g, sig), up), gate2);
+        h[2 * i] = f2_lo(hv);
+        h[2 * i + 1] = f2_hi(hv);
+        amax = fmaxf(amax, fmaxf(fabsf(h[2 * i]), fabsf(h[2 * i + 1])));
+      }
+      float rm;
+      const uint32_t sfc = nv_block_scale(amax, s_out, &rm);
+      q[2 * b] = e2m1x8(__fmul_rn(h[0], rm), __fmul_rn(h[1], rm), __fmul_rn(h[2], rm), __fmul_rn(h[3], rm),
+                        __fmul_rn(h[4], rm), __fmul_rn(h[5], rm), __fmul_rn(h[6], rm), __fmul_rn(h[7], rm));
+      q[2 * b + 1] = e2m1x8(__fmul_rn(h[8], rm), __fmul_rn(h[9], rm), __fmul_rn(h[10], rm), __fmul_rn(h[11], rm),
+                            __fmul_rn(h[12], rm), __fmul_rn(h[13], rm), __fmul_rn(h[14], rm), __fmul_rn(h[15], rm));
+      sfw |= sfc << (8 * b);
+      hmax = fmaxf(hmax, amax);
+    }
+    // 64 codes = 32 bytes of row prow; the 4 block scales are one 32-bit word of one atom
+    st_global_32B(p.hq + prow * (p.ldh / 2) + c0 / 2, make_uint4(q[0], q[1], q[2], q[3]),
+                  make_uint4(q[4], q[5], q[6], q[7]));
+    const int64_t atom = (prow / BM) * p.h_kt + c0 / 64;
+    uint8_t* sfp = p.hsf + atom * SF_ATOM + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+    *reinterpret_cast<uint32_t*>(sfp) = sfw;
+    // F % 256 == 128: GroupedLinear 2's last K step runs half past F, over two atoms of zero codes
+    // (the TMA fills its codes with zeros); the last column tile gives them zero scales
+    if (p.ldh % 256 != 0 && t.n == p.ldh / 128 - 1) *reinterpret_cast<uint32_t*>(sfp + 2 * SF_ATOM) = 0u;
+    if (p.nv_out_seen != nullptr) {
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(hmax));   // non-negative floats
+      if ((threadIdx.x & 31) == 0) atomicMax(p.nv_out_seen, m);
+    }
+  } else if (MODE == GEMM_SWIGLU) {
     const bool real = r < t.valid;
     const float gate = real ? (p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f) : 0.0f;
     uint8_t* hrow = p.hq + static_cast<int64_t>(t.pad_row0 + r) * p.ldh + t.n * 128 + 64 * half;
@@ -381,6 +448,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     if (r < t.valid) {
       const int ncols = BN / 2;
       uint16_t* yrow = p.y + static_cast<int64_t>(t.src_row0 + r) * p.ldy + t.n * BN + ncols * half;
+      auto val = [&](int i) {
+        if constexpr (FMT == FMT_NV) return __fmul_rn(__uint_as_float(v[i]), alpha);
+        return __uint_as_float(v[i]);
+      };
 #pragma unroll
       for (int c = 0; c < 128; c += 16) {
         if (c < ncols) {   // 16 columns = one 32-byte store
@@ -388,10 +459,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const int cc = c + 8 * k;
-            o[k].x = pack_bf16x2(__uint_as_float(v[cc + 0]), __uint_as_float(v[cc + 1]));
-            o[k].y = pack_bf16x2(__uint_as_float(v[cc + 2]), __uint_as_float(v[cc + 3]));
-            o[k].z = pack_bf16x2(__uint_as_float(v[cc + 4]), __uint_as_float(v[cc + 5]));
-            o[k].w = pack_bf16x2(__uint_as_float(v[cc + 6]), __uint_as_float(v[cc + 7]));
+            o[k].x = pack_bf16x2(val(cc + 0), val(cc + 1));
+            o[k].y = pack_bf16x2(val(cc + 2), val(cc + 3));
+            o[k].z = pack_bf16x2(val(cc + 4), val(cc + 5));
+            o[k].w = pack_bf16x2(val(cc + 6), val(cc + 7));
           }
           st_global_32B(yrow + c, o[0], o[1]);
         }
@@ -670,31 +741,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // Warp roles: warp 4 producer (both CTAs), warp 5 MMA issuer (leader CTA; the MMA warp of the
 // second CTA only takes part in the TMEM allocation), warps 8-15 epilogue; the other role warps idle.
 // ---------------------------------------------------------------------------------------------
-constexpr int P_STAGES = 3;
-constexpr int P_SUB = 2;                                      // K steps per stage
 constexpr int P_STEP_BYTES = 2 * 128 * BK;                    // own A tile + own half of the B tile
-constexpr int P_SF_BYTES = 3 * SF_ATOM;                       // own A atom + both B atoms of the step
-constexpr int P_SUBBUF_BYTES = P_STEP_BYTES + 2048;           // tiles, scale atoms, pad to 1 KB
-constexpr int P_STAGE_BYTES = P_SUB * P_SUBBUF_BYTES;
-constexpr int P_SF_SLOTS = P_STAGES * P_SUB;                  // one TMEM scale slot per sub-buffer
-constexpr int P_DATA_BYTES = P_STAGES * P_STAGE_BYTES;
 // GEMM_WGRAD epilogue: each epilogue warp stages its 32 rows x 8 fp32 columns in one of two 1 KB
 // buffers (32-byte rows, 32B swizzle) that a TMA store then writes out
 constexpr int P_WG_CHUNK = 8;                                  // fp32 columns per TMA store
 constexpr int P_WG_BUF_BYTES = 32 * P_WG_CHUNK * 4;            // 1 KB
 constexpr int P_EPI_BYTES = NUM_EPI_WARPS * 2 * P_WG_BUF_BYTES;
-constexpr int P_BAR_OFFSET = P_DATA_BYTES + P_EPI_BYTES;
-constexpr int P_NUM_BARS = 2 * P_STAGES + 3;
-constexpr int P_SMEM_BYTES = P_BAR_OFFSET + P_NUM_BARS * 8 + 8 + 1024;
-constexpr uint32_t P_SFA_COL = 256;                           // 4 columns per slot
-constexpr uint32_t P_SFB_COL = P_SFA_COL + 4 * P_SF_SLOTS;    // 8 columns per slot
 constexpr uint32_t P_REGS_LOW = 64;
 constexpr uint32_t P_REGS_HIGH = 192;
 static_assert(2 * 128 * P_REGS_LOW + 256 * P_REGS_HIGH == NUM_THREADS * 128, "register split must equal the launch pool");
-static_assert(P_STEP_BYTES % 1024 == 0 && P_SUBBUF_BYTES % 1024 == 0, "pair stages keep 1024-byte alignment");
-static_assert(P_STEP_BYTES + P_SF_BYTES <= P_SUBBUF_BYTES, "scale atoms fit behind the tiles");
-static_assert(P_SFA_COL + 4 * P_SF_SLOTS <= P_SFB_COL && P_SFB_COL + 8 * P_SF_SLOTS <= TMEM_COLS, "pair TMEM budget");
-static_assert(P_SMEM_BYTES <= 232448, "pair shared memory budget");
+
+// Shared-memory and TMEM layout of the pair kernel per format.  A stage holds SUB K steps; a
+// step's sub-buffer holds the CTA's own A tile, its half of the B tile and the step's scale atoms
+// (own A atoms, then the atoms of both B halves).  One TMEM scale slot per sub-buffer.  NVFP4's
+// larger scale slots (48 columns) leave TMEM room for 4 slots next to the 256-column accumulator,
+// hence 2 stages.
+template <int FMT>
+struct PairLayout {
+  static constexpr int SF_ATOMS = FMT == FMT_NV ? 4 : 1;      // scale atoms per 128 rows per K step
+  static constexpr int STAGES = FMT == FMT_NV ? 2 : 3;
+  static constexpr int SUB = 2;                               // K steps per stage
+  static constexpr int SF_BYTES = 3 * SF_ATOMS * SF_ATOM;
+  static constexpr int SUBBUF_BYTES = P_STEP_BYTES + (SF_BYTES + 1023) / 1024 * 1024;
+  static constexpr int STAGE_BYTES = SUB * SUBBUF_BYTES;
+  static constexpr int SF_SLOTS = STAGES * SUB;
+  static constexpr int DATA_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFFSET = DATA_BYTES + P_EPI_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 3;
+  static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 8 + 1024;
+  static constexpr uint32_t SFA_COL = 256;                         // 4 * SF_ATOMS columns per slot
+  static constexpr uint32_t SFB_COL = SFA_COL + 4 * SF_ATOMS * SF_SLOTS;   // 8 * SF_ATOMS per slot
+  static_assert(P_STEP_BYTES % 1024 == 0 && SUBBUF_BYTES % 1024 == 0, "pair stages keep 1024-byte alignment");
+  static_assert(SFB_COL + 8 * SF_ATOMS * SF_SLOTS <= TMEM_COLS, "pair TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "pair shared memory budget");
+};
 
 // Pair unit u -> (expert, column tile, pair of row tiles); this CTA takes row tile 2q + rank.
 // Experts own an even number of 128-row tiles (their rows are padded to a multiple of 256).
@@ -806,16 +886,17 @@ __device__ __forceinline__ bool pair_lane_wait(uint64_t* bar, uint32_t parity, b
   return false;
 }
 
-template <int MODE>
+template <int MODE, int FMT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+  using L = PairLayout<FMT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_BAR_OFFSET);
-  uint64_t* empty = full + P_STAGES;
-  uint64_t* acc_full = empty + P_STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFFSET);
+  uint64_t* empty = full + L::STAGES;
+  uint64_t* acc_full = empty + L::STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drained = acc_empty + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drained + 1);
@@ -827,7 +908,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < P_STAGES; ++s) {
+    for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -869,10 +950,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int b_own = rank == 0 ? t.b_row0 : t.b_row1;
         // scale atoms (512 bytes: 128 rows x 4 blocks) of the tile's first K step; step kb adds kb.
         // Past the end of B (half of a last tile) any valid atom will do: those B rows are zeros.
-        const int a_atom0 = (t.a_row / 128) * p.a_kt + t.a_k0 / BK;
-        const int b_atom0 = (t.b_row0 / 128) * p.b_kt + t.b_k0 / BK;
+        const int a_atom0 = (t.a_row / 128) * p.a_kt + L::SF_ATOMS * (t.a_k0 / BK);
+        const int b_atom0 = (t.b_row0 / 128) * p.b_kt + L::SF_ATOMS * (t.b_k0 / BK);
         const int b_row1 = (p.b_rows > 0 && t.b_row1 >= p.b_rows) ? t.b_row0 : t.b_row1;
-        const int b_atom1 = (b_row1 / 128) * p.b_kt + t.b_k0 / BK;
+        const int b_atom1 = (b_row1 / 128) * p.b_kt + L::SF_ATOMS * (t.b_k0 / BK);
         if constexpr (MODE == GEMM_DGRAD) {
           // the epilogue of this tile reads the saved g and u of its 128 rows x 256 columns of F:
           // have L2 fetch them while the tile's MMAs run (in the blocked layout each 32-row block's
@@ -884,7 +965,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         for (int kb = 0, nsub = 0; kb < t.steps; kb += nsub) {
-          nsub = min(P_SUB, t.steps - kb);
+          nsub = min(L::SUB, t.steps - kb);
           if (!pair_wait(&empty[stage], phase ^ 1u, abort_flag, peer_abort, p, ERR_TIMEOUT_PRODUCER, lane)) {
             ok = false;
             break;
@@ -892,25 +973,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (lane == 0) {
             const uint32_t bar = leader_full + stage * 8;
             for (int j = 0; j < nsub; ++j) {
-              uint8_t* sA = smem + stage * P_STAGE_BYTES + j * P_SUBBUF_BYTES;
+              uint8_t* sA = smem + stage * L::STAGE_BYTES + j * L::SUBBUF_BYTES;
               const int k0 = (kb + j) * BK;
               if constexpr (MODE == GEMM_DGRAD)   // dy tiles are reused by every column tile: keep them in L2
                 tma_load_2d_pair_hint(sA, &tmA, bar, t.a_k0 + k0, t.a_row, a_policy);
               else
                 tma_load_2d_pair(sA, &tmA, bar, t.a_k0 + k0, t.a_row);
               tma_load_2d_pair(sA + A_BYTES, &tmB, bar, t.b_k0 + k0, b_own);
-              uint8_t* sS = sA + P_STEP_BYTES;   // scale atoms: 2 rows of 256 bytes each in the maps
-              tma_load_2d_pair(sS, &tmSA, bar, 0, 2 * (a_atom0 + kb + j));
-              tma_load_2d_pair(sS + SF_ATOM, &tmSB, bar, 0, 2 * (b_atom0 + kb + j));
-              tma_load_2d_pair(sS + 2 * SF_ATOM, &tmSB, bar, 0, 2 * (b_atom1 + kb + j));
+              // scale atoms: 2 rows of 256 bytes each in the maps; a box holds the step's SF_ATOMS atoms
+              uint8_t* sS = sA + P_STEP_BYTES;
+              const int ka = L::SF_ATOMS * (kb + j);
+              tma_load_2d_pair(sS, &tmSA, bar, 0, 2 * (a_atom0 + ka));
+              tma_load_2d_pair(sS + L::SF_ATOMS * SF_ATOM, &tmSB, bar, 0, 2 * (b_atom0 + ka));
+              tma_load_2d_pair(sS + 2 * L::SF_ATOMS * SF_ATOM, &tmSB, bar, 0, 2 * (b_atom1 + ka));
             }
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * nsub * (P_STEP_BYTES + P_SF_BYTES));
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * nsub * (P_STEP_BYTES + L::SF_BYTES));
           }
           __syncwarp();
           ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == P_STAGES) {
+          if (++stage == L::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
@@ -923,7 +1006,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // where every abort raised in either CTA is visible, it gives them a fixed 200 us to land
       // (they depend on nothing but memory) before a second cluster barrier lets either CTA exit.
       if (lane == 0 && leader)
-        for (int s = 0; s < P_STAGES; ++s)
+        for (int s = 0; s < L::STAGES; ++s)
           if ((issued_mask >> s) & 1u)
             if (!mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, p.drain_ns))
               atomicOr(p.err, ERR_TIMEOUT_DRAIN);
@@ -932,7 +1015,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == WARP_MMA && leader) {
       // ---------------- pair MMA issuer (leader CTA; the loop runs in lane 0 alone) ----------------
       if (lane == 0) {
-        const uint32_t idesc = idesc_mxf8_e4m3(2 * BM, 256);
+        const uint32_t idesc = FMT == FMT_NV ? idesc_nvf4(2 * BM, 256) : idesc_mxf8_e4m3(2 * BM, 256);
         int stage = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool issued = false, ok = true;
@@ -946,35 +1029,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (!pair_lane_wait(acc_empty, acc_phase ^ 1u, true, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) break;
           tc_fence_after();
-          for (int kb = 0; kb < steps; kb += P_SUB) {
+          for (int kb = 0; kb < steps; kb += L::SUB) {
             // full: the stage's tiles and scale atoms are in both CTAs' shared memory
             if (!pair_lane_wait(&full[stage], phase, false, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t st0 = smem_u32(smem + stage * P_STAGE_BYTES);
+            const uint32_t st0 = smem_u32(smem + stage * L::STAGE_BYTES);
 #pragma unroll
-            for (int j = 0; j < P_SUB; ++j) {
+            for (int j = 0; j < L::SUB; ++j) {
               if (j > 0 && kb + j >= steps) break;   // half stage at the end of an odd tile
-              const uint32_t a0 = st0 + j * P_SUBBUF_BYTES, b0 = a0 + A_BYTES, sf0 = a0 + P_STEP_BYTES;
-              const int slot = stage * P_SUB + j;
-              const uint32_t t_sfa = tmem + P_SFA_COL + 4 * slot;
-              const uint32_t t_sfb = tmem + P_SFB_COL + 8 * slot;
+              const uint32_t a0 = st0 + j * L::SUBBUF_BYTES, b0 = a0 + A_BYTES, sf0 = a0 + P_STEP_BYTES;
+              const int slot = stage * L::SUB + j;
+              const uint32_t t_sfa = tmem + L::SFA_COL + 4 * L::SF_ATOMS * slot;
+              const uint32_t t_sfb = tmem + L::SFB_COL + 8 * L::SF_ATOMS * slot;
               // scales of the step into TMEM (both CTAs, each from its own shared memory); the MMAs
               // below are issued after them by this thread and see them in order
-              tc_copy_sf_pair(t_sfa, sdesc_sf_atom(sf0));
-              tc_copy_sf_pair(t_sfb, sdesc_sf_atom(sf0 + SF_ATOM));
-              tc_copy_sf_pair(t_sfb + 4, sdesc_sf_atom(sf0 + 2 * SF_ATOM));
+              if constexpr (FMT == FMT_NV) {
+                // MMA k reads its own atoms: A's at t_sfa + 4k, B's two halves at t_sfb + 8k (+4)
 #pragma unroll
-              for (int k = 0; k < BK / 32; ++k) {
-                tc_mma_mxf8_pair(tmem + ACC_COL, sdesc_kmajor_sw128(a0 + 32 * k), sdesc_kmajor_sw128(b0 + 32 * k),
-                                 idesc_with_sf_id(idesc, k), t_sfa, t_sfb, ((kb + j) | k) != 0 ? 1u : 0u);
+                for (int a = 0; a < 4; ++a) {
+                  tc_copy_sf_pair(t_sfa + 4 * a, sdesc_sf_atom(sf0 + a * SF_ATOM));
+                  tc_copy_sf_pair(t_sfb + 8 * a, sdesc_sf_atom(sf0 + (4 + a) * SF_ATOM));
+                  tc_copy_sf_pair(t_sfb + 8 * a + 4, sdesc_sf_atom(sf0 + (8 + a) * SF_ATOM));
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  tc_mma_nvf4_pair(tmem + ACC_COL, sdesc_kmajor_sw128(a0 + 32 * k), sdesc_kmajor_sw128(b0 + 32 * k),
+                                   idesc, t_sfa + 4 * k, t_sfb + 8 * k, ((kb + j) | k) != 0 ? 1u : 0u);
+              } else {
+                tc_copy_sf_pair(t_sfa, sdesc_sf_atom(sf0));
+                tc_copy_sf_pair(t_sfb, sdesc_sf_atom(sf0 + SF_ATOM));
+                tc_copy_sf_pair(t_sfb + 4, sdesc_sf_atom(sf0 + 2 * SF_ATOM));
+#pragma unroll
+                for (int k = 0; k < BK / 32; ++k) {
+                  tc_mma_mxf8_pair(tmem + ACC_COL, sdesc_kmajor_sw128(a0 + 32 * k), sdesc_kmajor_sw128(b0 + 32 * k),
+                                   idesc_with_sf_id(idesc, k), t_sfa, t_sfb, ((kb + j) | k) != 0 ? 1u : 0u);
+                }
               }
             }
             tc_commit_pair_both(&empty[stage]);
             issued = true;
-            if (++stage == P_STAGES) {
+            if (++stage == L::STAGES) {
               stage = 0;
               phase ^= 1u;
             }
@@ -998,6 +1095,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int r = quarter * 32 + lane;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t leader_acc_empty = map_to_cta(acc_empty, 0);
+    float alpha = 1.0f, s_out = 1.0f;
+    if constexpr (FMT == FMT_NV) {   // dequantization of the product: 1 / (s_a s_b)
+      const float s_a = nv_encode_scale(p.nv_amax_a != nullptr ? *p.nv_amax_a : p.nv_amax_a_val);
+      const float s_b = nv_encode_scale(*p.nv_amax_b);
+      alpha = __frcp_rn(__fmul_rn(s_a, s_b));
+      s_out = nv_encode_scale(p.nv_out_amax);
+    }
     uint32_t acc_phase = 0;
     for (int u = first_unit; u < total_units; u += unit_stride) {
       TileInfo t;
@@ -1037,7 +1141,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (t.n * 256 + 128 * half < p.wg_n) {
           const int col0 = t.n * 256 + 128 * half;
           const int grow = t.e * p.wg_m + t.a_row + quarter * 32;   // row in the [E * wg_m, wg_n] view
-          uint8_t* wbuf = smem + P_DATA_BYTES + (warp - FIRST_EPI_WARP) * 2 * P_WG_BUF_BYTES;
+          uint8_t* wbuf = smem + L::DATA_BYTES + (warp - FIRST_EPI_WARP) * 2 * P_WG_BUF_BYTES;
 #pragma unroll
           for (int c = 0; c < 128; c += P_WG_CHUNK) {
             uint8_t* buf = wbuf + ((c / P_WG_CHUNK) & 1) * P_WG_BUF_BYTES;
@@ -1062,7 +1166,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // other, so at most one of them competes for issue slots at a time (1.5% faster).  Half 0
         // is never a tile ahead of half 1: both pass the epilogue barrier of every tile.
         if (MODE == GEMM_SWIGLU && half == 1) asm volatile("bar.sync %0, 64;" ::"r"(BAR_STAGGER + quarter) : "memory");
-        epilogue_tile<MODE>(p, t, v, r, half, 256);
+        epilogue_tile<MODE, FMT>(p, t, v, r, half, 256, alpha, s_out);
         if (MODE == GEMM_SWIGLU && half == 0) asm volatile("bar.arrive %0, 64;" ::"r"(BAR_STAGGER + quarter) : "memory");
       }
     }
@@ -1176,14 +1280,14 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// A tensor-core scale array (512-byte atoms) as a 2-D byte matrix of 256-byte rows, boxes of two rows:
-// box (0, 2a) is atom a.
-bool make_sf_map(CUtensorMap* m, const void* base, uint64_t atoms) {
+// A tensor-core scale array (512-byte atoms) as a 2-D byte matrix of 256-byte rows, boxes of
+// 2 * `box_atoms` rows: box (0, 2a) is atoms a .. a + box_atoms - 1.
+bool make_sf_map(CUtensorMap* m, const void* base, uint64_t atoms, uint32_t box_atoms = 1) {
   auto enc = tensor_map_encoder();
   if (!enc || atoms == 0) return false;
   cuuint64_t dims[2] = {256, 2 * atoms};
   cuuint64_t strides[1] = {256};
-  cuuint32_t box[2] = {256, 2};
+  cuuint32_t box[2] = {256, 2 * box_atoms};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1207,10 +1311,11 @@ bool make_dw_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols)
 struct DeviceInfo {
   int sms = 0;
   int pair_clusters[4] = {0, 0, 0, 0};   // co-resident CTA pairs of each pair-kernel mode (0: none)
+  int nv_pair_clusters[2] = {0, 0};      // same for the NVFP4 forward GEMMs
   bool attr_set = false;
 };
 
-template <int MODE>
+template <int MODE, int FMT = FMT_MX>
 cudaLaunchConfig_t pair_config(int clusters, cudaLaunchAttribute* attr, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1219,39 +1324,40 @@ cudaLaunchConfig_t pair_config(int clusters, cudaLaunchAttribute* attr, cudaStre
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = P_SMEM_BYTES;
+  cfg.dynamicSmemBytes = PairLayout<FMT>::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cfg;
 }
 
-template <int MODE>
+template <int MODE, int FMT = FMT_MX>
 int max_pair_clusters() {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config<MODE>(64, attr, nullptr);
+  cudaLaunchConfig_t cfg = pair_config<MODE, FMT>(64, attr, nullptr);
   int n = 0;
-  if (cudaFuncSetAttribute(k_grouped_gemm_pair<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, k_grouped_gemm_pair<MODE>, &cfg) != cudaSuccess) {
+  if (cudaFuncSetAttribute(k_grouped_gemm_pair<MODE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           PairLayout<FMT>::SMEM_BYTES) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, k_grouped_gemm_pair<MODE, FMT>, &cfg) != cudaSuccess) {
     cudaGetLastError();   // clear: the single-CTA kernels are used instead
     return 0;
   }
   return n;
 }
 
-template <int MODE>
+template <int MODE, int FMT = FMT_MX>
 cudaError_t launch_pair(int clusters, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                         cudaStream_t stream) {
+  constexpr uint32_t box_atoms = PairLayout<FMT>::SF_ATOMS;
   CUtensorMap sa, sb, d = a;   // d: the weight-gradient output (other modes do not use it)
-  if (!make_sf_map(&sa, p.a_sf, static_cast<uint64_t>(p.a_sf_tiles) * p.a_kt) ||
-      !make_sf_map(&sb, p.b_sf, static_cast<uint64_t>(p.b_sf_tiles) * p.b_kt))
+  if (!make_sf_map(&sa, p.a_sf, static_cast<uint64_t>(p.a_sf_tiles) * p.a_kt, box_atoms) ||
+      !make_sf_map(&sb, p.b_sf, static_cast<uint64_t>(p.b_sf_tiles) * p.b_kt, box_atoms))
     return cudaErrorInvalidValue;
   if (MODE == GEMM_WGRAD && !make_dw_map(&d, p.dw, static_cast<uint64_t>(p.E) * p.wg_m, p.wg_n))
     return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config<MODE>(clusters, attr, stream);
-  return cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair<MODE>, a, b, sa, sb, d, p);
+  cudaLaunchConfig_t cfg = pair_config<MODE, FMT>(clusters, attr, stream);
+  return cudaLaunchKernelEx(&cfg, k_grouped_gemm_pair<MODE, FMT>, a, b, sa, sb, d, p);
 }
 
 bool device_setup(DeviceInfo** out) {
@@ -1278,6 +1384,9 @@ bool device_setup(DeviceInfo** out) {
     // the backward runs on CTA pairs only
     d.pair_clusters[GEMM_DGRAD] = max_pair_clusters<GEMM_DGRAD>();
     d.pair_clusters[GEMM_WGRAD] = max_pair_clusters<GEMM_WGRAD>();
+    // the NVFP4 forward runs on CTA pairs only
+    d.nv_pair_clusters[GEMM_SWIGLU] = max_pair_clusters<GEMM_SWIGLU, FMT_NV>();
+    d.nv_pair_clusters[GEMM_OUT] = max_pair_clusters<GEMM_OUT, FMT_NV>();
     d.attr_set = true;
   }
   *out = &d;
@@ -1386,6 +1495,100 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
     k_grouped_gemm<GEMM_OUT><<<grid2, NUM_THREADS, SMEM_BYTES, stream>>>(mA2, mB2, p2);
     if (cudaGetLastError() != cudaSuccess) return MXFP8_ERR_CUDA;
   }
+  if (!mark(4)) return MXFP8_ERR_CUDA;
+  return MXFP8_OK;
+}
+
+int launch_nvfp4_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
+                             const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const float* w1_amax,
+                             const uint8_t* w2_q, const uint8_t* w2_sf, const float* w2_amax, float h_amax, void* y,
+                             void* workspace, const NvWsLayout& L, cudaStream_t stream, void* const* events) {
+  DeviceInfo* dev = nullptr;
+  if (!device_setup(&dev)) return MXFP8_ERR_CUDA;
+  if (dev->nv_pair_clusters[GEMM_SWIGLU] <= 0 || dev->nv_pair_clusters[GEMM_OUT] <= 0) return MXFP8_ERR_UNSUPPORTED;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SchedHeader* meta = reinterpret_cast<SchedHeader*>(ws + L.meta);
+  uint32_t* amax = reinterpret_cast<uint32_t*>(ws + L.amax);   // [0] max|x|, [1] max|h| seen
+  uint8_t* xq = ws + L.xq;
+  uint8_t* xsf = ws + L.xsf;
+  uint8_t* hq = ws + L.hq;
+  uint8_t* hsf = ws + L.hsf;
+  // packed E2M1: a row of K values is K / 2 bytes; the GEMMs' K step is 128 bytes = 256 values
+  CUtensorMap mA1, mB1, mA2, mB2;
+  if (!make_map(&mA1, xq, L.r_pad, H / 2) || !make_map(&mB1, w1_q, static_cast<uint64_t>(E) * 2 * F, H / 2) ||
+      !make_map(&mA2, hq, L.r_pad, F / 2) || !make_map(&mB2, w2_q, static_cast<uint64_t>(E) * H, F / 2))
+    return MXFP8_ERR_CUDA;
+  auto mark = [&](int i) {
+    return events == nullptr || events[i] == nullptr ||
+           cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess;
+  };
+  if (!mark(0)) return MXFP8_ERR_CUDA;
+  if (launch_schedule(split, E, R, meta, stream) != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (cudaMemsetAsync(amax + 1, 0, sizeof(uint32_t), stream) != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (!mark(1)) return MXFP8_ERR_CUDA;
+  if (launch_nv_amax_quantize_gather(x_sorted, R, H, meta, E, L.r_pad, amax, xq, xsf, stream) != cudaSuccess)
+    return MXFP8_ERR_CUDA;
+  if (!mark(2)) return MXFP8_ERR_CUDA;
+
+  const int max_mtiles = static_cast<int>(L.r_pad / BM);
+  GemmParams p1{};
+  p1.meta = meta;
+  p1.a_sf = xsf;
+  p1.b_sf = w1_sf;
+  p1.E = E;
+  p1.KT = static_cast<int>((H + 255) / 256);
+  p1.NT = static_cast<int>(F / 128);
+  p1.BN = 256;
+  p1.b_rows_per_expert = static_cast<int>(2 * F);
+  p1.F = static_cast<int>(F);
+  p1.n_fastest = 0;
+  p1.gates = gates;
+  p1.hq = hq;
+  p1.hsf = hsf;
+  p1.ldh = F;
+  p1.err = &meta->error;
+  p1.timeout_ns = pipeline_wait_ns();
+  p1.drain_ns = kWaitTimeoutNs;
+  p1.a_kt = static_cast<int>(L.x_kt);
+  p1.b_kt = static_cast<int>(L.x_kt);
+  p1.a_sf_tiles = max_mtiles;
+  p1.b_sf_tiles = static_cast<int>(static_cast<int64_t>(E) * 2 * F / BM);
+  p1.nv_amax_a = reinterpret_cast<const float*>(amax);
+  p1.nv_amax_b = w1_amax;
+  p1.nv_out_amax = h_amax;
+  p1.nv_out_seen = amax + 1;
+  p1.h_kt = L.h_kt;
+  const int c1 = static_cast<int>(std::min<int64_t>(dev->nv_pair_clusters[GEMM_SWIGLU],
+                                                    std::max<int64_t>(1, static_cast<int64_t>(max_mtiles / 2) * p1.NT)));
+  if (launch_pair<GEMM_SWIGLU, FMT_NV>(c1, mA1, mB1, p1, stream) != cudaSuccess) return MXFP8_ERR_CUDA;
+  if (!mark(3)) return MXFP8_ERR_CUDA;
+
+  GemmParams p2{};
+  p2.meta = meta;
+  p2.a_sf = hsf;
+  p2.b_sf = w2_sf;
+  p2.E = E;
+  p2.KT = static_cast<int>((F + 255) / 256);
+  p2.BN = 256;
+  p2.NT = static_cast<int>(H / 256);
+  p2.b_rows_per_expert = static_cast<int>(H);
+  p2.F = static_cast<int>(F);
+  p2.n_fastest = 1;
+  p2.y = static_cast<uint16_t*>(y);
+  p2.ldy = H;
+  p2.err = &meta->error;
+  p2.timeout_ns = p1.timeout_ns;
+  p2.drain_ns = kWaitTimeoutNs;
+  p2.a_kt = static_cast<int>(L.h_kt);
+  p2.b_kt = static_cast<int>(L.h_kt);
+  p2.a_sf_tiles = max_mtiles;
+  p2.b_sf_tiles = static_cast<int>(static_cast<int64_t>(E) * H / BM);
+  p2.nv_amax_a = nullptr;
+  p2.nv_amax_a_val = h_amax;
+  p2.nv_amax_b = w2_amax;
+  const int c2 = static_cast<int>(std::min<int64_t>(dev->nv_pair_clusters[GEMM_OUT],
+                                                    std::max<int64_t>(1, static_cast<int64_t>(max_mtiles / 2) * p2.NT)));
+  if (launch_pair<GEMM_OUT, FMT_NV>(c2, mA2, mB2, p2, stream) != cudaSuccess) return MXFP8_ERR_CUDA;
   if (!mark(4)) return MXFP8_ERR_CUDA;
   return MXFP8_OK;
 }

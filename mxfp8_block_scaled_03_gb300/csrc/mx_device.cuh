@@ -92,6 +92,53 @@ __device__ __forceinline__ int64_t sf_mma_offset(int64_t row, int64_t blk, int64
 }
 
 // ------------------------------------------------------------------------------------------
+// NVFP4 arithmetic (E2M1 elements, one E4M3 scale per 16 values, a per-tensor binary32 encode
+// scale 448 * 6 / amax): NVIDIA's published format, named as a recipe on the Llama 3 recipe page.
+// Every decision is taken in binary32 with explicitly rounded operations.
+// ------------------------------------------------------------------------------------------
+
+// Per-tensor encode scale from the tensor's largest magnitude: 2688 / amax (1 for an all-zero
+// tensor, at most FLT_MAX).
+__device__ __forceinline__ float nv_encode_scale(float amax) {
+  return amax == 0.0f ? 1.0f : fminf(__fdiv_rn(2688.0f, amax), 3.402823466e38f);
+}
+
+// E4M3 code of a non-negative binary32 value, round to nearest even, saturating at 448.
+__device__ __forceinline__ uint32_t e4m3_code(float t) { return e4m3x2(t, 0.0f) & 0xFFu; }
+
+// Value of an E4M3 code (non-negative codes 0x00..0x7E), exact: 2^(E-7) (1 + M/8), or M 2^-9.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  return e == 0 ? __uint_as_float(0x3B000000u) * static_cast<float>(m)        // 2^-9 * M
+                : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// Block scale and element multiplier of one 16-value block of NVFP4 from its largest magnitude:
+// S = E4M3(fl32(fl32(amax / 6) * s_enc)); r = fl32(s_enc / S) (0 when S = 0, at most FLT_MAX).
+__device__ __forceinline__ uint32_t nv_block_scale(float amax, float s_enc, float* r) {
+  const uint32_t code = e4m3_code(__fmul_rn(__fdiv_rn(amax, 6.0f), s_enc));
+  const float S = e4m3_value(code);
+  *r = S == 0.0f ? 0.0f : fminf(__fdiv_rn(s_enc, S), 3.402823466e38f);
+  return code;
+}
+
+// Eight binary32 values -> eight E2M1 codes in one word (value 2i in the low nibble of byte i,
+// value 2i+1 in its high nibble), round to nearest even, saturating at 6.
+__device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v3, float v4, float v5, float v6,
+                                           float v7) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+  return r;
+}
+
+// ------------------------------------------------------------------------------------------
 // Generic helpers
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -412,6 +459,27 @@ __device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_des
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf4nvf4 with block scaling (NVFP4): A and B E2M1 (format 1 of
+// this kind, bits 7-9 and 10-12), both K-major, UE4M3 scales (bit 23 clear), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28, dense K = 64 (bit 31 clear); the scale-factor ids stay 0 (with
+// four scales per row and MMA every byte of the 32-bit TMEM word is used).
+__host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Pair MMA on NVFP4 operands: D (+)= A * B^T with K = 64 (32 bytes of packed E2M1 per row), a
+// UE4M3 scale per 16 values of K (four per row: one 512-byte atom of A and two of B in TMEM).
+__device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");

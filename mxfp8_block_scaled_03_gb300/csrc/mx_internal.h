@@ -106,4 +106,28 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
                            float* dw1, float* dw2, void* workspace, const BwdWsLayout& L, cudaStream_t stream,
                            void* const* events, const int32_t* token_of_row = nullptr, int64_t x_rows = 0);
 
+// ---- NVFP4 forward (nvfp4.cu, grouped_gemm.cu) ----
+// Scale atoms per 128-row tile of an NVFP4 tensor-core scale array for K values per row: K is
+// padded to a multiple of 256 (one K step of the GEMMs), four 512-byte atoms per step.
+int64_t nv_sf_atoms_per_tile(int64_t K);
+// Workspace of nvfp4_grouped_mlp_fwd: schedule, two words (largest |x| and largest |h| of the
+// call, float bits), then in the expert-padded row space x codes [r_pad, H/2] and their scale
+// atoms, h codes [r_pad, F/2] and their scale atoms.
+struct NvWsLayout {
+  size_t meta, amax, xq, xsf, hq, hsf, total;
+  int64_t r_pad, x_kt, h_kt;
+};
+bool nv_ws_layout(int64_t R, int64_t H, int64_t F, int E, NvWsLayout* out);
+// Clears *amax_word, reduces max|x| into it, then quantizes the sorted rows into the padded row
+// space (zero rows past each expert's count), scale codes in the tensor-core layout.
+cudaError_t launch_nv_amax_quantize_gather(const void* x, int64_t R, int64_t H, const SchedHeader* meta, int E,
+                                           int64_t r_pad, uint32_t* amax_word, uint8_t* xq, uint8_t* xsf,
+                                           cudaStream_t stream);
+// Schedule, activation amax + quantize, GroupedLinear 1 + ScaledSwiGLU + NVFP4 requant, GroupedLinear 2;
+// returns an mxfp8_status.  events: NULL or 5 events recorded around the stages.
+int launch_nvfp4_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split,
+                             const float* gates, const uint8_t* w1_q, const uint8_t* w1_sf, const float* w1_amax,
+                             const uint8_t* w2_q, const uint8_t* w2_sf, const float* w2_amax, float h_amax, void* y,
+                             void* workspace, const NvWsLayout& L, cudaStream_t stream, void* const* events);
+
 }  // namespace mx

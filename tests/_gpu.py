@@ -14,10 +14,10 @@ def to_dev(a: np.ndarray, dev="cuda"):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
 
-def sf_mma_to_compact(buf: np.ndarray, rows: int, kb: int) -> np.ndarray:
-    """Tensor-core scale layout (512-byte atoms of 128 rows x 4 blocks, row-tile-major; row
-    32j+i, block b of an atom at 16i + 4j + b) -> compact [rows, kb]."""
-    kt = (kb + 3) // 4
+def sf_mma_to_compact(buf: np.ndarray, rows: int, kb: int, kt: int | None = None) -> np.ndarray:
+    """Tensor-core scale layout (512-byte atoms of 128 rows x 4 blocks, row-tile-major with kt
+    atoms per 128-row tile; row 32j+i, block b of an atom at 16i + 4j + b) -> compact [rows, kb]."""
+    kt = (kb + 3) // 4 if kt is None else kt
     r = np.arange(rows)[:, None]
     b = np.arange(kb)[None, :]
     off = ((r // 128) * kt + b // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
@@ -67,3 +67,49 @@ Y_REL_TOL = 5e-3
 Y_MAX_TOL = 1e-2
 HQ_MISMATCH_FRAC = 1e-3
 HQ_MAX_ULPS = 1.0
+
+
+# ---- NVFP4 ----------------------------------------------------------------------------------
+def nv_kt(K: int) -> int:
+    """Atoms per 128-row tile of an NVFP4 tensor-core scale array (K padded to 256)."""
+    return (K + 255) // 256 * 4
+
+
+def pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    """[.., K] codes one per byte -> [.., K/2] bytes, value 2i in the low nibble of byte i."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+def unpack_e2m1(packed: np.ndarray) -> np.ndarray:
+    b = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = b & 0xF
+    out[..., 1::2] = b >> 4
+    return out
+
+
+_E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def nv_dequant(codes: np.ndarray, sf: np.ndarray, s_enc: float) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.int64)
+    v = np.where(c & 8, -_E2M1[c & 7], _E2M1[c & 7])
+    S = e4m3_values()[np.asarray(sf, dtype=np.int64)]
+    return v * np.repeat(S, 16, axis=-1) / np.float64(np.float32(s_enc))
+
+
+def nv_compare_intermediate(hq_gpu, hs_gpu, hq_ref, hs_ref, s_enc):
+    """(fraction of values whose dequantized values differ, worst difference in units of the E2M1
+    step at the coarser of the two blocks' scales)."""
+    a = nv_dequant(hq_gpu, hs_gpu, s_enc)
+    b = nv_dequant(hq_ref, hs_ref, s_enc)
+    diff = np.abs(a - b)
+    S = np.repeat(np.maximum(e4m3_values()[np.asarray(hs_gpu, dtype=np.int64)],
+                             e4m3_values()[np.asarray(hs_ref, dtype=np.int64)]), 16, axis=-1)
+    unit = S / np.float64(np.float32(s_enc))
+    mag = np.maximum(np.abs(a), np.abs(b)) / np.maximum(unit, 1e-300)
+    step = np.where(mag < 2, 0.5, np.where(mag < 4, 1.0, 2.0)) * unit
+    frac = float(np.mean(diff != 0))
+    worst = float(np.max(np.where(diff > 0, diff / np.maximum(step, 1e-300), 0.0))) if diff.size else 0.0
+    return frac, worst
