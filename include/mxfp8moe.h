@@ -255,6 +255,11 @@ int grouped_mlp_fwd_train(const void* x_sorted, int64_t R, int64_t H, int64_t F,
                           const uint8_t* w2_sf, void* y, void* saved, size_t saved_bytes, void* workspace,
                           size_t workspace_bytes, void* stream);
 size_t grouped_mlp_bwd_workspace_size(int64_t R, int64_t H, int64_t F, int E);
+/* Byte offsets of two pieces of a grouped_mlp_bwd workspace, for inspection by tests: [0] error
+ * word, [1] [dG | dU] as bf16 [R_pad, 2F], [2] h as bf16 [R_pad, F] (both in the expert-padded row
+ * space, zero on padding rows), [3] R_pad (not an offset).  out: 4 entries (host).  Returns
+ * MXFP8_OK or MXFP8_ERR_INVALID_ARG. */
+int grouped_mlp_bwd_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_t* out);
 int grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
                     const float* gates, const void* saved, size_t saved_bytes, const uint8_t* w1t_q,
                     const uint8_t* w1t_sf, const uint8_t* w2t_q, const uint8_t* w2t_sf, const void* dy, void* dx,

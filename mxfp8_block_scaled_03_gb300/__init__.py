@@ -33,7 +33,7 @@ __all__ = [
     "moe_permute_workspace_size", "moe_combine", "moe_gather_rows", "mxfp8_check_device_error", "mxfp8_quantize_colwise_t",
     "grouped_mlp_saved_bytes", "grouped_mlp_fwd_train", "grouped_mlp_bwd_workspace_size", "grouped_mlp_bwd",
     "grouped_mlp_fwd_tokens_train", "grouped_mlp_bwd_tokens", "mxfp8_status_string", "mxfp8_abi_version",
-    "mxfp8_mma_peak", "nvfp4_sf_bytes", "nvfp4_quantize", "nvfp4_grouped_mlp_workspace_size",
+    "mxfp8_mma_peak", "grouped_mlp_bwd_workspace_layout", "nvfp4_sf_bytes", "nvfp4_quantize", "nvfp4_grouped_mlp_workspace_size",
     "nvfp4_grouped_mlp_workspace_layout", "nvfp4_grouped_mlp_fwd",
 ]
 
@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
             L.grouped_mlp_fwd_train.argtypes = [P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, sz, P, sz, P]
             L.grouped_mlp_bwd_workspace_size.restype = sz
             L.grouped_mlp_bwd_workspace_size.argtypes = [i64, i64, i64, i32]
+            L.grouped_mlp_bwd_workspace_layout.restype = i32
+            L.grouped_mlp_bwd_workspace_layout.argtypes = [i64, i64, i64, i32, P]
             L.grouped_mlp_bwd.restype = i32
             L.grouped_mlp_bwd.argtypes = [P, i64, i64, i64, i32, P, P, P, sz, P, P, P, P, P, P, P, P, P, P, sz, P]
             L.grouped_mlp_bwd_timed.restype = i32
@@ -457,6 +459,13 @@ def moe_gather_rows(src, index, out=None, stream=None):
     _check(lib().moe_gather_rows(_ptr(src), int(src.shape[0]), row_bytes, _ptr(index), n, _ptr(out), _stream(stream)),
            "moe_gather_rows")
     return out
+
+
+def grouped_mlp_bwd_workspace_layout(R: int, H: int, F: int, E: int) -> list[int]:
+    """[error word, dGU bf16 [R_pad, 2F], h bf16 [R_pad, F], R_pad] of a backward workspace."""
+    out = (ctypes.c_uint64 * 4)()
+    _check(lib().grouped_mlp_bwd_workspace_layout(R, H, F, E, out), "grouped_mlp_bwd_workspace_layout")
+    return list(out)
 
 
 def nvfp4_sf_bytes(M: int, K: int, sf_layout: int = SF_COMPACT) -> int:

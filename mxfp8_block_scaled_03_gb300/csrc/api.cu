@@ -216,6 +216,16 @@ size_t grouped_mlp_bwd_workspace_size(int64_t R, int64_t H, int64_t F, int E) {
   return L.total;
 }
 
+int grouped_mlp_bwd_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_t* out) {
+  BwdWsLayout L;
+  if (out == nullptr || !bwd_ws_layout(R, H, F, E, &L)) return MXFP8_ERR_INVALID_ARG;
+  out[0] = L.meta;
+  out[1] = L.dgu;
+  out[2] = L.hb;
+  out[3] = static_cast<uint64_t>(L.r_pad);
+  return MXFP8_OK;
+}
+
 static int grouped_mlp_bwd_impl(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E,
                                 const int32_t* split_sizes, const float* gates, const void* saved,
                                 size_t saved_bytes, const uint8_t* w1t_q, const uint8_t* w1t_sf,

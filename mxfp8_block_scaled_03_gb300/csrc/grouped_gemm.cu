@@ -121,6 +121,8 @@ struct GemmParams {
   int b_rows_per_expert;   // 2F (GEMM_SWIGLU) or H (GEMM_OUT)
   int F;                   // GEMM_SWIGLU: row offset of the up projection inside an expert
   int n_fastest;           // tile order inside an expert: 1 = column tiles fastest, 0 = row tiles
+  int b_keep;              // pair kernel: B's tiles are loaded with an L2 evict-last policy (the
+                           // forward GroupedLinear 2 re-reads each expert's W2 in every wave of tiles)
   // GEMM_SWIGLU epilogue
   const float* gates;
   uint8_t* hq;
@@ -939,7 +941,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_PRODUCER) {
       // ---------------- tile producer (both CTAs; lane 0 issues) ----------------
       const uint32_t leader_full = map_to_cta(full, 0);
-      const uint64_t a_policy = l2_policy_evict_last();
+      const uint64_t keep_policy = l2_policy_evict_last();
       uint32_t issued_mask = 0, issued_parity = 0;
       int stage = 0;
       uint32_t phase = 0;
@@ -976,10 +978,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               uint8_t* sA = smem + stage * L::STAGE_BYTES + j * L::SUBBUF_BYTES;
               const int k0 = (kb + j) * BK;
               if constexpr (MODE == GEMM_DGRAD)   // dy tiles are reused by every column tile: keep them in L2
-                tma_load_2d_pair_hint(sA, &tmA, bar, t.a_k0 + k0, t.a_row, a_policy);
+                tma_load_2d_pair_hint(sA, &tmA, bar, t.a_k0 + k0, t.a_row, keep_policy);
               else
                 tma_load_2d_pair(sA, &tmA, bar, t.a_k0 + k0, t.a_row);
-              tma_load_2d_pair(sA + A_BYTES, &tmB, bar, t.b_k0 + k0, b_own);
+              if (MODE == GEMM_OUT && p.b_keep)
+                tma_load_2d_pair_hint(sA + A_BYTES, &tmB, bar, t.b_k0 + k0, b_own, keep_policy);
+              else
+                tma_load_2d_pair(sA + A_BYTES, &tmB, bar, t.b_k0 + k0, b_own);
               // scale atoms: 2 rows of 256 bytes each in the maps; a box holds the step's SF_ATOMS atoms
               uint8_t* sS = sA + P_STEP_BYTES;
               const int ka = L::SF_ATOMS * (kb + j);
@@ -1477,6 +1482,7 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p2.b_rows_per_expert = static_cast<int>(H);
   p2.F = static_cast<int>(F);
   p2.n_fastest = 1;
+  p2.b_keep = 1;
   p2.y = static_cast<uint16_t*>(y);
   p2.ldy = H;
   p2.err = &meta->error;
@@ -1574,6 +1580,7 @@ int launch_nvfp4_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t
   p2.b_rows_per_expert = static_cast<int>(H);
   p2.F = static_cast<int>(F);
   p2.n_fastest = 1;
+  p2.b_keep = 1;
   p2.y = static_cast<uint16_t*>(y);
   p2.ldy = H;
   p2.err = &meta->error;
