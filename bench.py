@@ -717,6 +717,11 @@ def run_native(args, world, rank, local):
             print(json.dumps({"workload": args.workload, "ms_per_step": step_ms, "value": value,
                               "roofline": roofline}), flush=True)
         return
+    if args.only == "nvfp4":
+        nv = nvfp4_forward(mx, fwd, args.steps, args.warmup, peaks)
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, "nvfp4": nv}), flush=True)
+        return
 
     # ---- the measured MXFP8 peak: the larger of cuBLASLt at 8192^3 and the library's MMA loop ----
     lib = library_mxfp8_gemms(R, H, F, dev)
@@ -961,9 +966,9 @@ def main():
                     help="length of the timed oracle call behind cpu_baseline")
     ap.add_argument("--workload", choices=["mixtral", "llama", "fine", "tiny"], default=WORKLOAD,
                     help="workload of the timed step (the headline line uses mixtral)")
-    ap.add_argument("--only", choices=["all", "fwd", "bwd"], default="all",
-                    help="fwd / bwd: time the forward (or forward + backward) only and print a short line "
-                         "(profiling runs)")
+    ap.add_argument("--only", choices=["all", "fwd", "bwd", "nvfp4"], default="all",
+                    help="fwd / bwd / nvfp4: time the MXFP8 forward (after it: the backward, or the NVFP4 "
+                         "forward) only and print a short line (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
