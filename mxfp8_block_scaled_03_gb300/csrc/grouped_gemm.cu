@@ -241,6 +241,15 @@ __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint4 v)
                : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 16 registers per thread -> 16 consecutive TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
 
 template <uint32_t N>
 __device__ __forceinline__ void regs_dec() {
@@ -755,9 +764,15 @@ static_assert(2 * 128 * P_REGS_LOW + 256 * P_REGS_HIGH == NUM_THREADS * 128, "re
 
 // Shared-memory and TMEM layout of the pair kernel per format.  A stage holds SUB K steps; a
 // step's sub-buffer holds the CTA's own A tile, its half of the B tile and the step's scale atoms
-// (own A atoms, then the atoms of both B halves).  One TMEM scale slot per sub-buffer.  NVFP4's
-// larger scale slots (48 columns) leave TMEM room for 4 slots next to the 256-column accumulator,
-// hence 2 stages.
+// (own A atoms, then the atoms of both B halves).  One TMEM scale slot per sub-buffer.
+//   MXFP8: the MMA thread copies the step's 3 atoms into the slot (tcgen05.cp); A: 4 columns
+//          (row 32j+i of the atom at lane i of every quarter, column j), B: 8 (two atoms).
+//   NVFP4: each CTA's four otherwise idle role warps write the slot with tcgen05.st, each into its
+//          own TMEM lane quarter (twelve tcgen05.cp per step in the MMA thread's stream cost a
+//          quarter of the GEMM time).  The image is the one the copies would leave: MMA k's A atom
+//          at SFA + 4k (row 32j+i at lane i of every quarter, column j), its two B atoms at
+//          SFB + 8k (+4); every scale address stays a multiple of 4 columns.  With 48 columns per
+//          slot, TMEM holds 4 slots beside the 256-column accumulator, hence 2 stages of 2 steps.
 template <int FMT>
 struct PairLayout {
   static constexpr int SF_ATOMS = FMT == FMT_NV ? 4 : 1;      // scale atoms per 128 rows per K step
@@ -769,12 +784,16 @@ struct PairLayout {
   static constexpr int SF_SLOTS = STAGES * SUB;
   static constexpr int DATA_BYTES = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFFSET = DATA_BYTES + P_EPI_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 3;
+  // full, empty per stage; NVFP4 also sf_full (this CTA's scale atoms landed) and sf_ready (both
+  // CTAs' scales are in TMEM) per stage; acc_full, acc_empty, drained
+  static constexpr int NUM_BARS = (FMT == FMT_NV ? 4 : 2) * STAGES + 3;
   static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 8 + 1024;
-  static constexpr uint32_t SFA_COL = 256;                         // 4 * SF_ATOMS columns per slot
-  static constexpr uint32_t SFB_COL = SFA_COL + 4 * SF_ATOMS * SF_SLOTS;   // 8 * SF_ATOMS per slot
+  static constexpr uint32_t SFA_SLOT_COLS = FMT == FMT_NV ? 16 : 4;
+  static constexpr uint32_t SFB_SLOT_COLS = FMT == FMT_NV ? 32 : 8;
+  static constexpr uint32_t SFA_COL = 256;
+  static constexpr uint32_t SFB_COL = SFA_COL + SFA_SLOT_COLS * SF_SLOTS;
   static_assert(P_STEP_BYTES % 1024 == 0 && SUBBUF_BYTES % 1024 == 0, "pair stages keep 1024-byte alignment");
-  static_assert(SFB_COL + 8 * SF_ATOMS * SF_SLOTS <= TMEM_COLS, "pair TMEM budget");
+  static_assert(SFB_COL + SFB_SLOT_COLS * SF_SLOTS <= TMEM_COLS, "pair TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "pair shared memory budget");
 };
 
@@ -901,7 +920,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* acc_full = empty + L::STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drained = acc_empty + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drained + 1);
+  uint64_t* sf_full = drained + 1;            // NVFP4 only
+  uint64_t* sf_ready = sf_full + L::STAGES;   // NVFP4 only (waited on in the leader)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drained + 1 + (FMT == FMT_NV ? 2 * L::STAGES : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -913,6 +934,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      if constexpr (FMT == FMT_NV) {
+        mbar_init(&sf_full[s], 1);
+        mbar_init(&sf_ready[s], 2 * NUM_SF_WARPS);
+      }
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * NUM_EPI_WARPS);
@@ -986,13 +1011,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               else
                 tma_load_2d_pair(sA + A_BYTES, &tmB, bar, t.b_k0 + k0, b_own);
               // scale atoms: 2 rows of 256 bytes each in the maps; a box holds the step's SF_ATOMS atoms
+              // (NVFP4: onto this CTA's own sf_full, which its scale warps wait on)
               uint8_t* sS = sA + P_STEP_BYTES;
               const int ka = L::SF_ATOMS * (kb + j);
-              tma_load_2d_pair(sS, &tmSA, bar, 0, 2 * (a_atom0 + ka));
-              tma_load_2d_pair(sS + L::SF_ATOMS * SF_ATOM, &tmSB, bar, 0, 2 * (b_atom0 + ka));
-              tma_load_2d_pair(sS + 2 * L::SF_ATOMS * SF_ATOM, &tmSB, bar, 0, 2 * (b_atom1 + ka));
+              if constexpr (FMT == FMT_NV) {
+                tma_load_2d(sS, &tmSA, &sf_full[stage], 0, 2 * (a_atom0 + ka));
+                tma_load_2d(sS + L::SF_ATOMS * SF_ATOM, &tmSB, &sf_full[stage], 0, 2 * (b_atom0 + ka));
+                tma_load_2d(sS + 2 * L::SF_ATOMS * SF_ATOM, &tmSB, &sf_full[stage], 0, 2 * (b_atom1 + ka));
+              } else {
+                tma_load_2d_pair(sS, &tmSA, bar, 0, 2 * (a_atom0 + ka));
+                tma_load_2d_pair(sS + SF_ATOM, &tmSB, bar, 0, 2 * (b_atom0 + ka));
+                tma_load_2d_pair(sS + 2 * SF_ATOM, &tmSB, bar, 0, 2 * (b_atom1 + ka));
+              }
             }
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * nsub * (P_STEP_BYTES + L::SF_BYTES));
+            if constexpr (FMT == FMT_NV) {
+              if (leader) mbar_arrive_expect_tx(&full[stage], 2 * nsub * P_STEP_BYTES);
+              mbar_arrive_expect_tx(&sf_full[stage], nsub * L::SF_BYTES);
+            } else if (leader) {
+              mbar_arrive_expect_tx(&full[stage], 2 * nsub * (P_STEP_BYTES + L::SF_BYTES));
+            }
           }
           __syncwarp();
           ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
@@ -1015,6 +1052,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if ((issued_mask >> s) & 1u)
             if (!mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, nullptr, p.drain_ns))
               atomicOr(p.err, ERR_TIMEOUT_DRAIN);
+      if (FMT == FMT_NV && lane == 0)   // this CTA's own scale copies
+        for (int s = 0; s < L::STAGES; ++s)
+          if ((issued_mask >> s) & 1u)
+            if (!mbar_wait_bounded(&sf_full[s], (issued_parity >> s) & 1u, nullptr, p.drain_ns))
+              atomicOr(p.err, ERR_TIMEOUT_DRAIN);
       prod_issued = issued_mask;
       __syncwarp();
     } else if (warp == WARP_MMA && leader) {
@@ -1035,8 +1077,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!pair_lane_wait(acc_empty, acc_phase ^ 1u, true, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) break;
           tc_fence_after();
           for (int kb = 0; kb < steps; kb += L::SUB) {
-            // full: the stage's tiles and scale atoms are in both CTAs' shared memory
+            // full: the stage's tiles and scale atoms are in both CTAs' shared memory (NVFP4: the
+            // tiles; sf_ready: both CTAs' scale warps have written the stage's scales into TMEM)
             if (!pair_lane_wait(&full[stage], phase, false, abort_flag, peer_abort, p, ERR_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            if (FMT == FMT_NV && !pair_lane_wait(&sf_ready[stage], phase, true, abort_flag, peer_abort, p,
+                                                 ERR_TIMEOUT_MMA)) {
               ok = false;
               break;
             }
@@ -1047,23 +1095,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (j > 0 && kb + j >= steps) break;   // half stage at the end of an odd tile
               const uint32_t a0 = st0 + j * L::SUBBUF_BYTES, b0 = a0 + A_BYTES, sf0 = a0 + P_STEP_BYTES;
               const int slot = stage * L::SUB + j;
-              const uint32_t t_sfa = tmem + L::SFA_COL + 4 * L::SF_ATOMS * slot;
-              const uint32_t t_sfb = tmem + L::SFB_COL + 8 * L::SF_ATOMS * slot;
-              // scales of the step into TMEM (both CTAs, each from its own shared memory); the MMAs
-              // below are issued after them by this thread and see them in order
+              const uint32_t t_sfa = tmem + L::SFA_COL + L::SFA_SLOT_COLS * slot;
+              const uint32_t t_sfb = tmem + L::SFB_COL + L::SFB_SLOT_COLS * slot;
               if constexpr (FMT == FMT_NV) {
-                // MMA k reads its own atoms: A's at t_sfa + 4k, B's two halves at t_sfb + 8k (+4)
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                  tc_copy_sf_pair(t_sfa + 4 * a, sdesc_sf_atom(sf0 + a * SF_ATOM));
-                  tc_copy_sf_pair(t_sfb + 8 * a, sdesc_sf_atom(sf0 + (4 + a) * SF_ATOM));
-                  tc_copy_sf_pair(t_sfb + 8 * a + 4, sdesc_sf_atom(sf0 + (8 + a) * SF_ATOM));
-                }
+                // scales already in TMEM (scale warps): MMA k's A atom at t_sfa + 4k, B's at t_sfb + 8k
+                (void)sf0;
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                   tc_mma_nvf4_pair(tmem + ACC_COL, sdesc_kmajor_sw128(a0 + 32 * k), sdesc_kmajor_sw128(b0 + 32 * k),
                                    idesc, t_sfa + 4 * k, t_sfb + 8 * k, ((kb + j) | k) != 0 ? 1u : 0u);
               } else {
+                // scales of the step into TMEM (both CTAs, each from its own shared memory); the MMAs
+                // below are issued after them by this thread and see them in order
                 tc_copy_sf_pair(t_sfa, sdesc_sf_atom(sf0));
                 tc_copy_sf_pair(t_sfb, sdesc_sf_atom(sf0 + SF_ATOM));
                 tc_copy_sf_pair(t_sfb + 4, sdesc_sf_atom(sf0 + 2 * SF_ATOM));
@@ -1091,6 +1134,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       __syncwarp();
+    } else if (FMT == FMT_NV && warp < NUM_SF_WARPS) {
+      // ---------------- NVFP4 scale staging (both CTAs; warp q writes TMEM lane quarter q) ----------------
+      // Per step, lane i of every warp: the 16 bytes of row i of each A atom k (rows i, 32+i, 64+i,
+      // 96+i) -> columns SFA + 4k .. +3, and of each B atom (half h, MMA k) -> SFB + 8k + 4h .. +3,
+      // in the warp's own lane quarter: every quarter gets the same image.  The stage's scales land
+      // on this CTA's sf_full; when both of its steps are written, each warp arrives on the leader's
+      // sf_ready.
+      const uint32_t q = static_cast<uint32_t>(warp & 3);
+      const uint32_t t_lanes = tmem + ((32u * q) << 16);
+      const uint32_t leader_sf_ready = map_to_cta(sf_ready, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = first_unit; ok && u < total_units; u += unit_stride) {
+        const int steps = p.KT;
+        for (int kb = 0; kb < steps; kb += L::SUB) {
+          if (!pair_wait(&sf_full[stage], phase, abort_flag, peer_abort, p, ERR_TIMEOUT_SF, lane)) {
+            ok = false;
+            break;
+          }
+#pragma unroll 1
+          for (int j = 0; j < L::SUB; ++j) {
+            if (j > 0 && kb + j >= steps) break;   // half stage at the end of an odd tile
+            const uint8_t* sS = smem + stage * L::STAGE_BYTES + j * L::SUBBUF_BYTES + P_STEP_BYTES;
+            const int slot = stage * L::SUB + j;
+            uint32_t a[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint4 w = *reinterpret_cast<const uint4*>(sS + k * SF_ATOM + 16 * lane);
+              a[4 * k + 0] = w.x;
+              a[4 * k + 1] = w.y;
+              a[4 * k + 2] = w.z;
+              a[4 * k + 3] = w.w;
+            }
+            tmem_st_32x32b_x16(t_lanes + L::SFA_COL + L::SFA_SLOT_COLS * slot, a);
+#pragma unroll
+            for (int k0 = 0; k0 < 4; k0 += 2) {   // B atoms of MMAs k0, k0 + 1: 16 columns per store
+              uint32_t b[16];
+#pragma unroll
+              for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const uint4 w = *reinterpret_cast<const uint4*>(sS + (4 + 4 * h + k0 + k) * SF_ATOM + 16 * lane);
+                  b[8 * k + 4 * h + 0] = w.x;
+                  b[8 * k + 4 * h + 1] = w.y;
+                  b[8 * k + 4 * h + 2] = w.z;
+                  b[8 * k + 4 * h + 3] = w.w;
+                }
+              tmem_st_32x32b_x16(t_lanes + L::SFB_COL + L::SFB_SLOT_COLS * slot + 8 * k0, b);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader)
+              mbar_arrive(&sf_ready[stage]);
+            else
+              mbar_arrive_remote(leader_sf_ready + 8u * static_cast<uint32_t>(stage));
+          }
+          if (++stage == L::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
     }
   } else {
     regs_inc<P_REGS_HIGH>();
