@@ -121,8 +121,13 @@ struct GemmParams {
   int b_rows_per_expert;   // 2F (GEMM_SWIGLU) or H (GEMM_OUT)
   int F;                   // GEMM_SWIGLU: row offset of the up projection inside an expert
   int n_fastest;           // tile order inside an expert: 1 = column tiles fastest, 0 = row tiles
-  int b_keep;              // pair kernel: B's tiles are loaded with an L2 evict-last policy (the
-                           // forward GroupedLinear 2 re-reads each expert's W2 in every wave of tiles)
+  int group_m;             // pair kernel with n_fastest: row-tile pairs per group (0: no groups).
+                           // Inside an expert, groups of group_m row pairs run one after the other
+                           // and, in a group, its row pairs fastest: the tiles in flight cover
+                           // group_m row bands x (clusters / group_m) weight column tiles, so each
+                           // band stays in L2 across all column tiles and each weight column tile is
+                           // read once per group instead of once per wave of tiles
+  int64_t y_rows;          // GEMM_OUT: rows of y (the TMA store map's extent)
   // GEMM_SWIGLU epilogue
   const float* gates;
   uint8_t* hq;
@@ -776,8 +781,8 @@ static_assert(2 * 128 * P_REGS_LOW + 256 * P_REGS_HIGH == NUM_THREADS * 128, "re
 template <int FMT>
 struct PairLayout {
   static constexpr int SF_ATOMS = FMT == FMT_NV ? 4 : 1;      // scale atoms per 128 rows per K step
-  static constexpr int STAGES = FMT == FMT_NV ? 2 : 3;
-  static constexpr int SUB = 2;                               // K steps per stage
+  static constexpr int STAGES = FMT == FMT_NV ? 5 : 3;
+  static constexpr int SUB = FMT == FMT_NV ? 1 : 2;          // K steps per stage
   static constexpr int SF_BYTES = 3 * SF_ATOMS * SF_ATOM;
   static constexpr int SUBBUF_BYTES = P_STEP_BYTES + (SF_BYTES + 1023) / 1024 * 1024;
   static constexpr int STAGE_BYTES = SUB * SUBBUF_BYTES;
@@ -813,7 +818,13 @@ __device__ __forceinline__ void decode_pair_unit(int u, int rank, const GemmPara
   const int pairs = (__ldg(mt_off + e + 1) >> 1) - q0;
   const int local = u - q0 * p.NT;
   int n, q;
-  if (p.n_fastest) {
+  if (p.n_fastest && p.group_m > 0) {
+    const int g = local / (p.group_m * p.NT);          // group of group_m row pairs
+    const int in_g = min(p.group_m, pairs - g * p.group_m);
+    const int w = local - g * p.group_m * p.NT;
+    n = w / in_g;
+    q = g * p.group_m + (w - n * in_g);
+  } else if (p.n_fastest) {
     q = local / p.NT;
     n = local - q * p.NT;
   } else {
@@ -1006,10 +1017,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_load_2d_pair_hint(sA, &tmA, bar, t.a_k0 + k0, t.a_row, keep_policy);
               else
                 tma_load_2d_pair(sA, &tmA, bar, t.a_k0 + k0, t.a_row);
-              if (MODE == GEMM_OUT && p.b_keep)
-                tma_load_2d_pair_hint(sA + A_BYTES, &tmB, bar, t.b_k0 + k0, b_own, keep_policy);
-              else
-                tma_load_2d_pair(sA + A_BYTES, &tmB, bar, t.b_k0 + k0, b_own);
+              tma_load_2d_pair(sA + A_BYTES, &tmB, bar, t.b_k0 + k0, b_own);
               // scale atoms: 2 rows of 256 bytes each in the maps; a box holds the step's SF_ATOMS atoms
               // (NVFP4: onto this CTA's own sf_full, which its scale warps wait on)
               uint8_t* sS = sA + P_STEP_BYTES;
@@ -1274,6 +1282,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
+      } else if (MODE == GEMM_OUT) {
+        // y: 16 bf16 columns at a time.  A warp whose 32 rows are all real rows of the expert writes
+        // them by TMA stores from a double-buffered 1 KB staging area: a warp instruction writes 512
+        // contiguous bytes of shared memory and the rows leave as whole lines (row-per-lane 32-byte
+        // global stores touch 32 lines per instruction and throttled the epilogue of short-K
+        // tiles).  A warp whose rows run past the expert's last row stores its real rows directly:
+        // y is not padded, the next rows belong to the next expert.
+        const bool via_tma = p.y_rows > 0 && quarter * 32 + 31 < t.valid;
+        const int col0 = t.n * 256 + 128 * half;
+        const int grow = t.src_row0 + quarter * 32;
+        uint8_t* wbuf = smem + L::DATA_BYTES + (warp - FIRST_EPI_WARP) * 2 * P_WG_BUF_BYTES;
+        uint16_t* yrow = p.y + static_cast<int64_t>(t.src_row0 + r) * p.ldy + col0;
+        auto val = [&](int i) {
+          if constexpr (FMT == FMT_NV) return __fmul_rn(__uint_as_float(v[i]), alpha);
+          return __uint_as_float(v[i]);
+        };
+#pragma unroll
+        for (int c = 0; c < 128; c += 16) {
+          uint4 o[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int cc = c + 8 * k;
+            o[k].x = pack_bf16x2(val(cc + 0), val(cc + 1));
+            o[k].y = pack_bf16x2(val(cc + 2), val(cc + 3));
+            o[k].z = pack_bf16x2(val(cc + 4), val(cc + 5));
+            o[k].w = pack_bf16x2(val(cc + 6), val(cc + 7));
+          }
+          if (via_tma) {
+            uint8_t* buf = wbuf + ((c / 16) & 1) * P_WG_BUF_BYTES;
+            if (lane == 0) bulk_wait_read_le1();   // the store that last used this buffer has read it
+            __syncwarp();
+            // row `lane`: two 16-byte chunks, 32B swizzle (chunk j of row i at j ^ ((i >> 2) & 1))
+            const int sw = (lane >> 2) & 1;
+            *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * sw) = o[0];
+            *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * (sw ^ 1)) = o[1];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, buf, col0 + c, grow);
+              bulk_commit_group();
+            }
+          } else if (r < t.valid) {
+            st_global_32B(yrow + c, o[0], o[1]);
+          }
+        }
       } else {
         // GroupedLinear 1: the two warps of a lane quarter share a scheduler with each other and
         // (for one quarter) with the MMA thread; they run their SwiGLU/quantize math one after the
@@ -1284,7 +1337,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (MODE == GEMM_SWIGLU && half == 0) asm volatile("bar.arrive %0, 64;" ::"r"(BAR_STAGGER + quarter) : "memory");
       }
     }
-    if (MODE == GEMM_WGRAD && lane == 0) bulk_wait_all();   // stores complete before the CTA exits
+    if ((MODE == GEMM_WGRAD || MODE == GEMM_OUT) && lane == 0) bulk_wait_all();   // stores complete before exit
   }
 
   tc_fence_before();
@@ -1410,6 +1463,20 @@ bool make_sf_map(CUtensorMap* m, const void* base, uint64_t atoms, uint32_t box_
 
 // The fp32 weight gradient [E * wg_m, wg_n] as the target of TMA stores: boxes of 32 rows x 8
 // columns (32-byte rows, 32B swizzle), matching the epilogue's staging buffers.
+// y [rows, cols] bf16 as the target of TMA stores: boxes of 32 rows x 16 columns (32-byte rows, 32B
+// swizzle), matching the GEMM_OUT epilogue's staging buffers.
+bool make_y_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  auto enc = tensor_map_encoder();
+  if (!enc || rows == 0 || cols == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_dw_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
   auto enc = tensor_map_encoder();
   if (!enc || rows == 0 || cols == 0) return false;
@@ -1468,6 +1535,8 @@ cudaError_t launch_pair(int clusters, const CUtensorMap& a, const CUtensorMap& b
       !make_sf_map(&sb, p.b_sf, static_cast<uint64_t>(p.b_sf_tiles) * p.b_kt, box_atoms))
     return cudaErrorInvalidValue;
   if (MODE == GEMM_WGRAD && !make_dw_map(&d, p.dw, static_cast<uint64_t>(p.E) * p.wg_m, p.wg_n))
+    return cudaErrorInvalidValue;
+  if (MODE == GEMM_OUT && p.y_rows > 0 && !make_y_map(&d, p.y, static_cast<uint64_t>(p.y_rows), p.ldy))
     return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config<MODE, FMT>(clusters, attr, stream);
@@ -1591,7 +1660,8 @@ int launch_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t F, in
   p2.b_rows_per_expert = static_cast<int>(H);
   p2.F = static_cast<int>(F);
   p2.n_fastest = 1;
-  p2.b_keep = 1;
+  p2.group_m = 8;
+  p2.y_rows = R;
   p2.y = static_cast<uint16_t*>(y);
   p2.ldy = H;
   p2.err = &meta->error;
@@ -1689,7 +1759,8 @@ int launch_nvfp4_grouped_mlp(const void* x_sorted, int64_t R, int64_t H, int64_t
   p2.b_rows_per_expert = static_cast<int>(H);
   p2.F = static_cast<int>(F);
   p2.n_fastest = 1;
-  p2.b_keep = 1;
+  p2.group_m = 8;
+  p2.y_rows = R;
   p2.y = static_cast<uint16_t*>(y);
   p2.ldy = H;
   p2.err = &meta->error;
@@ -1865,6 +1936,7 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   px.n_fastest = 1;
   px.y = static_cast<uint16_t*>(dx);
   px.ldy = H;
+  px.y_rows = R;
   if ((st = run_pair<GEMM_OUT>(dev, pairs * px.NT, mDgu, mW1t, px, stream)) != MXFP8_OK) return st;
   if (!mark(4)) return MXFP8_ERR_CUDA;
 
