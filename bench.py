@@ -692,10 +692,10 @@ def run_native(args, world, rank, local):
             b1.record()
             torch.cuda.synchronize()
             bwd_ms = b0.elapsed_time(b1) / nb
-            names = ["quantize_dy_x", "dgrad2_swiglu_bwd", "quantize_dgu_h_dgate", "dgrad1", "wgrad2", "wgrad1"]
+            names = ["quantize_dy_x", "dgrad2_swiglu_bwd_quant", "dgate_reduce", "dgrad1", "wgrad2", "wgrad1"]
             stage = {n: sum(e[j].elapsed_time(e[j + 1]) for e in bev) / nb for j, n in enumerate(names)}
             bflops = 12.0 * R * H * F
-            gemm_tf = {"dgrad2_swiglu_bwd": 2.0 * R * H * F, "dgrad1": 4.0 * R * H * F, "wgrad2": 2.0 * R * H * F,
+            gemm_tf = {"dgrad2_swiglu_bwd_quant": 2.0 * R * H * F, "dgrad1": 4.0 * R * H * F, "wgrad2": 2.0 * R * H * F,
                        "wgrad1": 4.0 * R * H * F}
             bwd = {"ms": bwd_ms, "tflops": bflops / (bwd_ms * 1e-3) / 1e12, "flops_per_step": bflops,
                    "stage_ms": stage,

@@ -246,8 +246,8 @@ int grouped_mlp_fwd_noalloc(const void* x_sorted, int64_t R, int64_t H, int64_t 
  * expert without rows gets zero weight gradients).  Split errors and timeouts are reported in
  * the workspace error word as for the forward.
  * grouped_mlp_bwd_timed additionally records 7 caller-created events (stage_events[0..6]) around
- * its stages: quantizations of dy and x | dh + ScaledSwiGLU backward | quantizations of dGU and
- * h, dgate | dx | dW2 | dW1.
+ * its stages: quantizations of dy and x | dh + ScaledSwiGLU backward with dGU and h quantized in
+ * its epilogue | dgate reduction | dx | dW2 | dW1.
  */
 size_t grouped_mlp_saved_bytes(int64_t R, int64_t H, int64_t F, int E);
 int grouped_mlp_fwd_train(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
@@ -255,10 +255,16 @@ int grouped_mlp_fwd_train(const void* x_sorted, int64_t R, int64_t H, int64_t F,
                           const uint8_t* w2_sf, void* y, void* saved, size_t saved_bytes, void* workspace,
                           size_t workspace_bytes, void* stream);
 size_t grouped_mlp_bwd_workspace_size(int64_t R, int64_t H, int64_t F, int E);
-/* Byte offsets of two pieces of a grouped_mlp_bwd workspace, for inspection by tests: [0] error
- * word, [1] [dG | dU] as bf16 [R_pad, 2F], [2] h as bf16 [R_pad, F] (both in the expert-padded row
- * space, zero on padding rows), [3] R_pad (not an offset).  out: 4 entries (host).  Returns
- * MXFP8_OK or MXFP8_ERR_INVALID_ARG. */
+/* Byte offsets of the pieces of a grouped_mlp_bwd workspace that hold the quantized [dG | dU]
+ * and h the dh GEMM's epilogue writes, for inspection by tests.  All live in the expert-padded
+ * row space of R_pad rows (padding rows are zero values); codes are E4M3, scale bytes UE8M0 in
+ * the tensor-core layout (mxfp8_quantize, MXFP8_SF_MMA) of the matrix named:
+ *   [0] error word
+ *   [1] [dG | dU] row-wise codes [R_pad, 2F]        [2] their scale bytes ([R_pad, 2F])
+ *   [3] [dG | dU] column-wise codes, transposed [2F, R_pad]   [4] their scale bytes ([2F, R_pad])
+ *   [5] h column-wise codes, transposed [F, R_pad]  [6] their scale bytes ([F, R_pad])
+ *   [7] R_pad (not an offset)
+ * out: 8 entries (host).  Returns MXFP8_OK or MXFP8_ERR_INVALID_ARG. */
 int grouped_mlp_bwd_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uint64_t* out);
 int grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F, int E, const int32_t* split_sizes,
                     const float* gates, const void* saved, size_t saved_bytes, const uint8_t* w1t_q,

@@ -462,8 +462,11 @@ def moe_gather_rows(src, index, out=None, stream=None):
 
 
 def grouped_mlp_bwd_workspace_layout(R: int, H: int, F: int, E: int) -> list[int]:
-    """[error word, dGU bf16 [R_pad, 2F], h bf16 [R_pad, F], R_pad] of a backward workspace."""
-    out = (ctypes.c_uint64 * 4)()
+    """Byte offsets in a backward workspace: [error word, dGU row-wise codes [R_pad, 2F], their
+    scale bytes, dGU column-wise codes transposed [2F, R_pad], their scale bytes, h column-wise
+    codes transposed [F, R_pad], their scale bytes, R_pad]; scale bytes in the tensor-core
+    layout."""
+    out = (ctypes.c_uint64 * 8)()
     _check(lib().grouped_mlp_bwd_workspace_layout(R, H, F, E, out), "grouped_mlp_bwd_workspace_layout")
     return list(out)
 

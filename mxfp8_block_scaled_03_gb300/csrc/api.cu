@@ -220,9 +220,13 @@ int grouped_mlp_bwd_workspace_layout(int64_t R, int64_t H, int64_t F, int E, uin
   BwdWsLayout L;
   if (out == nullptr || !bwd_ws_layout(R, H, F, E, &L)) return MXFP8_ERR_INVALID_ARG;
   out[0] = L.meta;
-  out[1] = L.dgu;
-  out[2] = L.hb;
-  out[3] = static_cast<uint64_t>(L.r_pad);
+  out[1] = L.dguq;
+  out[2] = L.dgusf;
+  out[3] = L.dguT;
+  out[4] = L.dguTsf;
+  out[5] = L.hT;
+  out[6] = L.hTsf;
+  out[7] = static_cast<uint64_t>(L.r_pad);
   return MXFP8_OK;
 }
 

@@ -150,8 +150,14 @@ struct GemmParams {
   uint16_t* gu_out;
   // GEMM_DGRAD epilogue
   const uint16_t* gu;      // saved [G | U]
-  uint16_t* dgu;           // [dG | dU] bf16 [R_pad, 2F]
-  uint16_t* hb;            // h bf16 [R_pad, F]
+  uint8_t* dguq;           // [dG | dU] row-wise MXFP8 codes [R_pad, 2F]
+  uint8_t* dgusf;          //   their scale bytes (tensor-core layout of [R_pad, 2F])
+  uint8_t* dguT;           // [dG | dU] column-wise MXFP8, codes transposed [2F, R_pad]
+  uint8_t* dguTsf;         //   their scale bytes (tensor-core layout of [2F, R_pad])
+  uint8_t* hT;             // h column-wise MXFP8, codes transposed [F, R_pad]
+  uint8_t* hTsf;           //   their scale bytes (tensor-core layout of [F, R_pad])
+  int64_t r_pad;           // rows of the padded row space (columns of the transposed codes)
+  int64_t t_kt;            // r_pad / 128: scale atoms per 128-row tile of the transposed matrices
   float* dgate_part;       // [R_pad, F / 128] partial sums of the routing-weight gradient
   // GEMM_WGRAD
   int wg_mt, wg_nt;        // 256-row tiles of A's rows (M / 256) and of B's rows (N / 256)
@@ -282,9 +288,53 @@ __device__ __forceinline__ int64_t gu_offset(int64_t prow, int64_t j, int64_t tw
 //   NVFP4 (FMT_NV): accumulators are first multiplied by alpha = 1 / (s_a s_b), the product of the
 //                operands' per-tensor decode scales; GEMM_SWIGLU requantizes h to NVFP4 under the
 //                encode scale s_out (four 16-value blocks per thread, E4M3 block scales).
+// One MXFP8 block of 32 bf16 values (pairs x2[i] = values 2i, 2i + 1) -> 32 E4M3 codes stored at
+// dst (32-byte aligned); returns the block's UE8M0 scale byte.
+__device__ __forceinline__ uint32_t quantize_block32_to(const uint32_t (&x2)[16], uint8_t* dst) {
+  uint32_t m2 = absmax_bf16x2(x2[0]);
+#pragma unroll
+  for (int i = 1; i < 16; ++i) m2 = absmax_bf16x2(m2, x2[i]);
+  const uint32_t sfb = e8m0_from_amax(fmaxf(bf16_lo(m2), bf16_hi(m2)));
+  const float inv = e8m0_inverse_scale(sfb);
+  uint32_t q[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    q[k] = e4m3x2(bf16_lo(x2[2 * k]) * inv, bf16_hi(x2[2 * k]) * inv) |
+           (e4m3x2(bf16_lo(x2[2 * k + 1]) * inv, bf16_hi(x2[2 * k + 1]) * inv) << 16);
+  st_global_32B(dst, make_uint4(q[0], q[1], q[2], q[3]), make_uint4(q[4], q[5], q[6], q[7]));
+  return sfb;
+}
+
+// Column-wise MXFP8 blocks of a warp: lane l holds 32 bf16 values of its row, the warp's 32
+// lanes being 32 consecutive rows.  The 32 x 32 block passes through the warp's 2 KB of shared
+// memory (rows of 64 bytes; 16-byte chunk j of row i stored at chunk j ^ ((i >> 1) & 3), so that
+// both the row writes and the column reads are free of bank conflicts).  colblock_put writes
+// chunk j (columns 8j .. 8j + 7, as four bf16 pairs) of the lane's row; after all four chunks,
+// colblock_quantize has lane l read column l and write its 32 E4M3 codes (rows in order) to dst
+// (32-byte aligned) and its UE8M0 scale byte to *sf.  The caller keeps a __syncwarp between the
+// last colblock_quantize of a buffer's previous use and the next colblock_put.
+__device__ __forceinline__ void colblock_put(uint8_t* buf, int lane, int j, uint4 w) {
+  *reinterpret_cast<uint4*>(buf + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) = w;
+}
+
+__device__ __forceinline__ void colblock_quantize(const uint8_t* buf, int lane, uint8_t* dst, uint8_t* sf) {
+  __syncwarp();   // every lane's row is in place
+  const int cj = lane >> 3, cw = 2 * (lane & 7);   // chunk and byte of column `lane` in a row
+  uint32_t c2[16];                                 // column `lane`, rows (2i, 2i + 1) as bf16 pairs
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int o = 16 * (cj ^ (i & 3)) + cw;        // rows 2i and 2i + 1 share the swizzle
+    c2[i] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(buf + (2 * i) * 64 + o)) |
+            (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(buf + (2 * i + 1) * 64 + o)) << 16);
+  }
+  *sf = static_cast<uint8_t>(quantize_block32_to(c2, dst));
+  __syncwarp();   // the buffer may be written again
+}
+
 template <int MODE, int FMT = FMT_MX>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& t, const uint32_t* v, int r,
-                                              int half, int BN, float alpha = 1.0f, float s_out = 1.0f) {
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& t, uint32_t* v, int r,
+                                              int half, int BN, float alpha = 1.0f, float s_out = 1.0f,
+                                              uint8_t* wbuf = nullptr, uint32_t t_park = 0) {
   if (MODE == GEMM_SWIGLU && FMT == FMT_NV) {
     const bool real = r < t.valid;
     const float gate = real ? (p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f) : 0.0f;
@@ -393,40 +443,62 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     // v = dh for 128 columns f of F.  From the saved bf16 pre-activations g, u and the gate:
     //   s = silu(g) = g * sig(g),  s' = sig(g) * (1 + g * (1 - sig(g)))
     //   dG = dh * gate * u * s',  dU = dh * gate * s,  h = gate * s * u,  dgate += dh * s * u
-    // dG, dU and h are stored as bf16 (zeros on padding rows, so the column-wise quantizations
-    // and the weight gradients see zero rows there).
+    // dG, dU and h are rounded to bf16 (the tensors the backward hands between its GEMMs) and leave
+    // this epilogue quantized the way the next GEMMs read them:
+    //   [dG | dU] row-wise (blocks of 32 along 2F of this thread's row) -> codes [r_pad, 2F] and
+    //     scale bytes, the dx GEMM's A operand;
+    //   [dG | dU] and h column-wise (blocks of 32 rows: this warp's 32 lanes, one 32-row block of
+    //     the expert because experts start at multiples of 256 padded rows) -> transposed codes
+    //     [2F, r_pad] / [F, r_pad] and scale bytes, the weight-gradient GEMMs' operands.  Each
+    //     32 x 32 block goes through the warp's 2 KB of shared memory: lanes write their rows, then
+    //     lane l reads column l, takes its block scale and writes its 32 codes as one contiguous
+    //     32-byte piece of a transposed row.
+    // Padding rows carry zeros (gate 0, dh 0), so column blocks see zero rows there and their
+    // row-wise codes are zero.
     const int64_t F = p.ldh;
     const int64_t prow = t.pad_row0 + r;
     const int f0 = t.n * 256 + 128 * half;
-    if (f0 >= F) return;   // the half of the last column tile that lies past F
-    uint16_t* dg_row = p.dgu + prow * 2 * F + f0;
-    uint16_t* h_row = p.hb + prow * F + f0;
-    float part = 0.0f;
-    if (r < t.valid) {
-      const float gate = p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f;
-      const uint64_t gate2 = f2_pack(gate, gate), one2 = f2_pack(1.0f, 1.0f), mone2 = f2_pack(-1.0f, -1.0f);
-      uint64_t part2 = f2_pack(0.0f, 0.0f);
-      // blocked layout (gu_offset), prefetched into L2 at the tile's start
+    if (f0 >= F) return;   // the half of the last column tile that lies past F (whole warps)
+    const bool real = r < t.valid;
+    const float gate = real ? (p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f) : 0.0f;
+    const uint64_t gate2 = f2_pack(gate, gate), one2 = f2_pack(1.0f, 1.0f), mone2 = f2_pack(-1.0f, -1.0f);
+    uint64_t part2 = f2_pack(0.0f, 0.0f);
+    uint32_t rsf_g = 0, rsf_u = 0;                 // row-wise scale bytes of this row's dG / dU blocks
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int64_t prow0 = prow - lane;             // first row of the warp's 32-row block
+#pragma unroll 1
+    for (int b = 0; b < 4; ++b) {                  // 32 columns f0 + 32b .. (in v[0 .. 31])
+      uint32_t dg[16], du[16];                     // bf16 pairs of columns (2i, 2i + 1) of the block
+      if (b == 1) {
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 16) {
-        // the four 16-byte loads of 16 columns go out together
-        uint4 gw2[2], uw2[2];
-        gw2[0] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, f0 + c0, 2 * F)));
-        gw2[1] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, f0 + c0 + 8, 2 * F)));
-        uw2[0] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + f0 + c0, 2 * F)));
-        uw2[1] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + f0 + c0 + 8, 2 * F)));
-        uint4 odg[2], odu[2], oh[2];
+        for (int i = 0; i < 32; ++i) v[i] = v[32 + i];
+      } else if (b >= 2) {                         // the upper 64 columns back from TMEM
+        tmem_ld_32x32b_x32(t_park + 32 * (b - 2), v);
+        tmem_ld_wait();
+      }
+#pragma unroll
+      for (int c16 = 0; c16 < 2; ++c16) {
+        uint4 gw2[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+        uint4 uw2[2] = {gw2[0], gw2[0]};
+        const int fc = f0 + 32 * b + 16 * c16;
+        if (real) {   // blocked layout (gu_offset), prefetched into L2 at the tile's start
+          gw2[0] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, fc, 2 * F)));
+          gw2[1] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, fc + 8, 2 * F)));
+          uw2[0] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + fc, 2 * F)));
+          uw2[1] = __ldcs(reinterpret_cast<const uint4*>(p.gu + gu_offset(prow, F + fc + 8, 2 * F)));
+        }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int c = c0 + 8 * hh;
           const uint32_t gw[4] = {gw2[hh].x, gw2[hh].y, gw2[hh].z, gw2[hh].w};
           const uint32_t uw[4] = {uw2[hh].x, uw2[hh].y, uw2[hh].z, uw2[hh].w};
-          uint32_t pdg[4], pdu[4], ph[4];
+          uint32_t hp[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {   // column pairs (c + 2i, c + 2i + 1) in f32x2 arithmetic
+          for (int i = 0; i < 4; ++i) {   // column pairs in f32x2 arithmetic
+            const int k = 8 * c16 + 4 * hh + i;   // pair index inside the 32-column block
+            const int c = 2 * k;                  // accumulator column (in v)
             const uint64_t g = f2_pack(bf16_lo(gw[i]), bf16_hi(gw[i]));
             const uint64_t u = f2_pack(bf16_lo(uw[i]), bf16_hi(uw[i]));
-            const uint64_t dh = f2_pack(__uint_as_float(v[c + 2 * i]), __uint_as_float(v[c + 2 * i + 1]));
+            const uint64_t dh = f2_pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1]));
             const uint64_t d = f2_add(f2_pack(__expf(-f2_lo(g)), __expf(-f2_hi(g))), one2);   // 1 + e^-g
             const uint64_t sig = f2_pack(__fdividef(1.0f, f2_lo(d)), __fdividef(1.0f, f2_hi(d)));
             const uint64_t sl = f2_mul(g, sig);                                    // silu(g)
@@ -437,29 +509,35 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
             const uint64_t dgv = f2_mul(f2_mul(dhg, u), dsl);
             const uint64_t duv = f2_mul(dhg, sl);
             const uint64_t hv = f2_mul(gate2, su);
-            pdg[i] = pack_bf16x2(f2_lo(dgv), f2_hi(dgv));
-            pdu[i] = pack_bf16x2(f2_lo(duv), f2_hi(duv));
-            ph[i] = pack_bf16x2(f2_lo(hv), f2_hi(hv));
+            dg[k] = pack_bf16x2(f2_lo(dgv), f2_hi(dgv));
+            du[k] = pack_bf16x2(f2_lo(duv), f2_hi(duv));
+            hp[i] = pack_bf16x2(f2_lo(hv), f2_hi(hv));
           }
-          odg[hh] = make_uint4(pdg[0], pdg[1], pdg[2], pdg[3]);
-          odu[hh] = make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]);
-          oh[hh] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+          colblock_put(wbuf, lane, 2 * c16 + hh, make_uint4(hp[0], hp[1], hp[2], hp[3]));   // h goes first
         }
-        st_global_32B_cs(dg_row + c0, odg[0], odg[1]);
-        st_global_32B_cs(dg_row + F + c0, odu[0], odu[1]);
-        st_global_32B_cs(h_row + c0, oh[0], oh[1]);
       }
-      part = f2_lo(part2) + f2_hi(part2);
-    } else {
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 4
-      for (int c = 0; c < 128; c += 16) {
-        st_global_32B_cs(dg_row + c, z, z);
-        st_global_32B_cs(dg_row + F + c, z, z);
-        st_global_32B_cs(h_row + c, z, z);
-      }
+      const int64_t fb = f0 + 32 * b;
+      const int64_t cblk = prow0 >> 5;
+      // h column-wise; [dG | dU] row-wise (this row's block of each) and column-wise
+      colblock_quantize(wbuf, lane, p.hT + (fb + lane) * p.r_pad + prow0,
+                        p.hTsf + sf_mma_offset(fb + lane, cblk, p.t_kt));
+      rsf_g |= quantize_block32_to(dg, p.dguq + prow * 2 * F + fb) << (8 * b);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        colblock_put(wbuf, lane, j, make_uint4(dg[4 * j], dg[4 * j + 1], dg[4 * j + 2], dg[4 * j + 3]));
+      colblock_quantize(wbuf, lane, p.dguT + (fb + lane) * p.r_pad + prow0,
+                        p.dguTsf + sf_mma_offset(fb + lane, cblk, p.t_kt));
+      rsf_u |= quantize_block32_to(du, p.dguq + prow * 2 * F + F + fb) << (8 * b);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        colblock_put(wbuf, lane, j, make_uint4(du[4 * j], du[4 * j + 1], du[4 * j + 2], du[4 * j + 3]));
+      colblock_quantize(wbuf, lane, p.dguT + (F + fb + lane) * p.r_pad + prow0,
+                        p.dguTsf + sf_mma_offset(F + fb + lane, cblk, p.t_kt));
     }
-    p.dgate_part[prow * (F / 128) + f0 / 128] = part;
+    // row-wise scale bytes: blocks f0/32 .. +3 of dG and (F + f0)/32 .. +3 of dU, one word each
+    *reinterpret_cast<uint32_t*>(p.dgusf + sf_mma_offset(prow, f0 / 32, 2 * F / 128)) = rsf_g;
+    *reinterpret_cast<uint32_t*>(p.dgusf + sf_mma_offset(prow, (F + f0) / 32, 2 * F / 128)) = rsf_u;
+    p.dgate_part[prow * (F / 128) + f0 / 128] = f2_lo(part2) + f2_hi(part2);
   } else {
     if (r < t.valid) {
       const int ncols = BN / 2;
@@ -763,6 +841,9 @@ constexpr int P_STEP_BYTES = 2 * 128 * BK;                    // own A tile + ow
 constexpr int P_WG_CHUNK = 8;                                  // fp32 columns per TMA store
 constexpr int P_WG_BUF_BYTES = 32 * P_WG_CHUNK * 4;            // 1 KB
 constexpr int P_EPI_BYTES = NUM_EPI_WARPS * 2 * P_WG_BUF_BYTES;
+// GEMM_DGRAD (MXFP8): TMEM columns past the scale slots where each epilogue warp parks the upper
+// 64 of its 128 accumulator columns (64 * half + 0 .. 63).
+constexpr uint32_t P_PARK_COL = 384;
 constexpr uint32_t P_REGS_LOW = 64;
 constexpr uint32_t P_REGS_HIGH = 192;
 static_assert(2 * 128 * P_REGS_LOW + 256 * P_REGS_HIGH == NUM_THREADS * 128, "register split must equal the launch pool");
@@ -799,6 +880,8 @@ struct PairLayout {
   static constexpr uint32_t SFB_COL = SFA_COL + SFA_SLOT_COLS * SF_SLOTS;
   static_assert(P_STEP_BYTES % 1024 == 0 && SUBBUF_BYTES % 1024 == 0, "pair stages keep 1024-byte alignment");
   static_assert(SFB_COL + SFB_SLOT_COLS * SF_SLOTS <= TMEM_COLS, "pair TMEM budget");
+  static_assert(FMT != FMT_MX || (SFB_COL + SFB_SLOT_COLS * SF_SLOTS <= P_PARK_COL && P_PARK_COL + 128 <= TMEM_COLS),
+                "GEMM_DGRAD parking columns");
   static_assert(SMEM_BYTES <= 232448, "pair shared memory budget");
 };
 
@@ -1252,6 +1335,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_ld_32x32b_x32(t_row + ACC_COL + 128 * half + 96, v + 96);
       }
       tmem_ld_wait();
+      if constexpr (MODE == GEMM_DGRAD) {
+        // the upper 64 of the 128 columns wait in TMEM columns no MMA writes (registers hold 64
+        // fewer values through the first half of the epilogue)
+        tmem_st_32x32b_x16(t_row + P_PARK_COL + 64 * half, v + 64);
+        tmem_st_32x32b_x16(t_row + P_PARK_COL + 64 * half + 16, v + 80);
+        tmem_st_32x32b_x16(t_row + P_PARK_COL + 64 * half + 32, v + 96);
+        tmem_st_32x32b_x16(t_row + P_PARK_COL + 64 * half + 48, v + 112);
+        tmem_st_wait();
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(leader_acc_empty);   // the leader may overwrite TMEM
@@ -1333,7 +1425,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // other, so at most one of them competes for issue slots at a time (1.5% faster).  Half 0
         // is never a tile ahead of half 1: both pass the epilogue barrier of every tile.
         if (MODE == GEMM_SWIGLU && half == 1) asm volatile("bar.sync %0, 64;" ::"r"(BAR_STAGGER + quarter) : "memory");
-        epilogue_tile<MODE, FMT>(p, t, v, r, half, 256, alpha, s_out);
+        epilogue_tile<MODE, FMT>(p, t, v, r, half, 256, alpha, s_out,
+                                 smem + L::DATA_BYTES + (warp - FIRST_EPI_WARP) * 2 * P_WG_BUF_BYTES,
+                                 t_row + P_PARK_COL + 64 * half);
         if (MODE == GEMM_SWIGLU && half == 0) asm volatile("bar.arrive %0, 64;" ::"r"(BAR_STAGGER + quarter) : "memory");
       }
     }
@@ -1825,13 +1919,11 @@ bool bwd_ws_layout(int64_t R, int64_t H, int64_t F, int E, BwdWsLayout* out) {
   L.dyTsf = al(L.dyT + rp * H);
   L.xT = al(L.dyTsf + rp * H / 32);
   L.xTsf = al(L.xT + rp * H);
-  L.dgu = al(L.xTsf + rp * H / 32);
-  L.dguq = al(L.dgu + rp * 2 * F * 2);
+  L.dguq = al(L.xTsf + rp * H / 32);
   L.dgusf = al(L.dguq + rp * 2 * F);
   L.dguT = al(L.dgusf + rp * 2 * F / 32);
   L.dguTsf = al(L.dguT + rp * 2 * F);
-  L.hb = al(L.dguTsf + rp * 2 * F / 32);
-  L.hT = al(L.hb + rp * F * 2);
+  L.hT = al(L.dguTsf + rp * 2 * F / 32);
   L.hTsf = al(L.hT + rp * F);
   L.part = al(L.hTsf + rp * F / 32);
   L.total = al(L.part + rp * (F / 128) * sizeof(float));
@@ -1882,7 +1974,8 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   base.drain_ns = kWaitTimeoutNs;
   int st;
 
-  // 1: dh = dy W2 (W2 quantized along H) with the ScaledSwiGLU backward -> dGU, h, dgate parts
+  // 1: dh = dy W2 (W2 quantized along H) with the ScaledSwiGLU backward -> dGU row-wise and
+  //    column-wise, h column-wise (MXFP8), dgate parts
   GemmParams pd = base;
   pd.a_sf = ws + L.dysf;
   pd.b_sf = w2t_sf;
@@ -1900,19 +1993,20 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   pd.gates = gates;
   pd.ldh = F;
   pd.gu = saved_gu;
-  pd.dgu = reinterpret_cast<uint16_t*>(ws + L.dgu);
-  pd.hb = reinterpret_cast<uint16_t*>(ws + L.hb);
+  pd.dguq = ws + L.dguq;
+  pd.dgusf = ws + L.dgusf;
+  pd.dguT = ws + L.dguT;
+  pd.dguTsf = ws + L.dguTsf;
+  pd.hT = ws + L.hT;
+  pd.hTsf = ws + L.hTsf;
+  pd.r_pad = rp;
+  pd.t_kt = rp / BM;
   pd.dgate_part = reinterpret_cast<float*>(ws + L.part);
   if ((st = run_pair<GEMM_DGRAD>(dev, pairs * pd.NT, mDy, mW2t, pd, stream)) != MXFP8_OK) return st;
   if (!mark(2)) return MXFP8_ERR_CUDA;
 
-  // 2: quantizations of dGU (row-wise for dx and column-wise for dW1, one pass) and of h (column-wise
-  //    for dW2)
-  if (launch_quantize_t(ws + L.dgu, rp, 2 * F, rp, true, ws + L.dguT, ws + L.dguTsf, nullptr, E, nullptr, 0,
-                        stream, ws + L.dguq, ws + L.dgusf) != cudaSuccess ||
-      launch_quantize_t(ws + L.hb, rp, F, rp, true, ws + L.hT, ws + L.hTsf, nullptr, E, nullptr, 0, stream) !=
-          cudaSuccess)
-    return MXFP8_ERR_CUDA;
+  // 2: the routing-weight gradient from the dh epilogue's partial sums (dGU and h left that epilogue
+  //    already quantized, row-wise and column-wise)
   if (dgates != nullptr) {
     k_dgate_reduce<<<static_cast<unsigned>((R + 255) / 256 > 0 ? (R + 255) / 256 : 1), 256, 0, stream>>>(
         meta, E, R, static_cast<int>(F / 128), reinterpret_cast<const float*>(ws + L.part), dgates);

@@ -84,6 +84,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// max of |a| and |b| per bf16 half (sign bits cleared, so the maximum is exact).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a & 0x7FFF7FFFu), "r"(b & 0x7FFF7FFFu));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a) { return a & 0x7FFF7FFFu; }
+
 // Byte offset of (row, block) in the tensor-core scale-factor layout: 512-byte atoms of
 // 128 rows x 4 blocks, atoms ordered row-tile-major with `kt` atoms per row tile; inside an atom
 // row 32*j + i, block b sits at 16*i + 4*j + b.

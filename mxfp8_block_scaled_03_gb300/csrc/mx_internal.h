@@ -43,14 +43,13 @@ bool ws_layout(int64_t R, int64_t H, int64_t F, int E, WsLayout* out);
 //   dyq/dysf    dy row-wise (blocks along H), tensor-core scale layout        [r_pad, H]
 //   dyT/dyTsf   dy column-wise, codes transposed (blocks along rows)          [H, r_pad]
 //   xT/xTsf     x column-wise, transposed                                    [H, r_pad]
-//   dgu         [dG | dU] bf16                                               [r_pad, 2F]
 //   dguq/dgusf  dGU row-wise                                                 [r_pad, 2F]
 //   dguT/dguTsf dGU column-wise, transposed                                  [2F, r_pad]
-//   hb          h bf16                                                       [r_pad, F]
 //   hT/hTsf     h column-wise, transposed                                    [F, r_pad]
+// (dGU and h are written quantized by the dh GEMM's epilogue; no bf16 copy is kept.)
 //   part        partial sums of the routing-weight gradient (float)          [r_pad, F/128]
 struct BwdWsLayout {
-  size_t meta, dyq, dysf, dyT, dyTsf, xT, xTsf, dgu, dguq, dgusf, dguT, dguTsf, hb, hT, hTsf, part, total;
+  size_t meta, dyq, dysf, dyT, dyTsf, xT, xTsf, dguq, dgusf, dguT, dguTsf, hT, hTsf, part, total;
   int64_t r_pad;
 };
 bool bwd_ws_layout(int64_t R, int64_t H, int64_t F, int E, BwdWsLayout* out);

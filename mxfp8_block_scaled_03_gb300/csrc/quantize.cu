@@ -44,15 +44,6 @@ struct QuantArgs {
   const int32_t* tok;       // gather mode: source row of every sorted row (NULL: the sorted row itself)
 };
 
-// max of |a| and |b| per bf16 half (sign bits cleared, so the maximum is exact).
-__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a & 0x7FFF7FFFu), "r"(b & 0x7FFF7FFFu));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a) { return a & 0x7FFF7FFFu; }
-
 __device__ __forceinline__ float max_halves(uint32_t m) { return fmaxf(bf16_lo(m), bf16_hi(m)); }
 
 // 8 bf16 (one uint4) times a common inverse scale -> 8 codes.

@@ -73,7 +73,7 @@ def lib() -> ctypes.CDLL:
             L.ora_moe_permute.argtypes = [P, P, i64, ctypes.c_int, ctypes.c_int, P, P, P, P]
             L.ora_grouped_mlp_bwd_rows.restype = ctypes.c_int
             L.ora_grouped_mlp_bwd_rows.argtypes = [P, i64, i64, i64, ctypes.c_int, P, P, P, P, P, P, P, P, P,
-                                                   P, i64, P, P, P, P, ctypes.c_int, ctypes.c_int]
+                                                   P, i64, P, P, P, P, P, ctypes.c_int, ctypes.c_int]
             L.ora_grouped_mlp_bwd_dw.restype = ctypes.c_int
             L.ora_grouped_mlp_bwd_dw.argtypes = [P, i64, i64, i64, ctypes.c_int, P, P, P, P, P, P, P,
                                                  ctypes.c_int, P, i64, P, ctypes.c_int, ctypes.c_int]
@@ -246,8 +246,9 @@ def quantize_transposed(w_bf16: np.ndarray, E: int, nthreads: int | None = None)
 
 
 def grouped_mlp_bwd_rows(x_bf16, split_sizes, gates, w1q, w1sf, w2tq, w2tsf, w1tq, w1tsf, dy_bf16, rows,
-                         nthreads=None, quant=True):
-    """Backward rows in binary64: (dx [n, H], dgate [n], dGU bf16 bits [n, 2F], h bf16 bits [n, F]).
+                         nthreads=None, quant=True, want_gu=False):
+    """Backward rows in binary64: (dx [n, H], dgate [n], dGU bf16 bits [n, 2F], h bf16 bits [n, F]),
+    and with want_gu also the forward's saved pre-activations [g | u] as bf16 bits [n, 2F].
     quant=False turns every quantization and bf16 rounding of x, dy and the intermediates into the
     identity (a test hook; the weights are always taken from their codes).
 
@@ -266,13 +267,14 @@ def grouped_mlp_bwd_rows(x_bf16, split_sizes, gates, w1q, w1sf, w2tq, w2tsf, w1t
     dgate = np.empty(n, dtype=np.float64)
     dgu = np.empty((n, 2 * F), dtype=np.uint16)
     hb = np.empty((n, F), dtype=np.uint16)
+    gu = np.empty((n, 2 * F), dtype=np.uint16) if want_gu else None
     arrs = [np.ascontiguousarray(a, dtype=np.uint8) for a in (w1q, w1sf, w2tq, w2tsf, w1tq, w1tsf)]
     rc = lib().ora_grouped_mlp_bwd_rows(_ptr(x), R, H, F, E, _ptr(split), _ptr(g), *[_ptr(a) for a in arrs],
                                         _ptr(dy), _ptr(rows), n, _ptr(dx), _ptr(dgate), _ptr(dgu), _ptr(hb),
-                                        1 if quant else 0, nthreads or default_threads())
+                                        _ptr(gu), 1 if quant else 0, nthreads or default_threads())
     if rc != OK:
         raise ValueError(f"oracle grouped_mlp_bwd_rows rejected the arguments (status {rc})")
-    return dx, dgate, dgu, hb
+    return (dx, dgate, dgu, hb, gu) if want_gu else (dx, dgate, dgu, hb)
 
 
 def grouped_mlp_bwd_dw(x_bf16, split_sizes, gates, w1q, w1sf, w2tq, w2tsf, dy_bf16, which: int, entries,

@@ -434,7 +434,7 @@ typedef struct {
     const int64_t* off; const float* gates;
     double code_val[256], scale_val[256];
     const uint8_t *w1q, *w1sf, *w2tq, *w2tsf, *w1tq, *w1tsf;
-    const int64_t* rows; double *dx, *dgate; uint16_t *dgu_out, *h_out;
+    const int64_t* rows; double *dx, *dgate; uint16_t *dgu_out, *h_out, *gu_out;
     /* entries of the weight gradients */
     int which; const int64_t* ent; double* dw;
     /* 1: quantize and round as documented; 0: every quantization and bf16 rounding of x, dy and
@@ -529,6 +529,10 @@ static void ora_bwd_rows_range(void* p, int64_t i0, int64_t i1) {
         for (j = 0; j < F; ++j) {
             double g, u, dh, sig, sl, dsl;
             ora_row_gu(c, e, a, j, &g, &u);
+            if (c->gu_out) {
+                c->gu_out[i * 2 * F + j] = ora_double_to_bf16_bits(g);
+                c->gu_out[i * 2 * F + F + j] = ora_double_to_bf16_bits(u);
+            }
             dh = ora_row_dh(c, e, dyq, j);
             sig = 1.0 / (1.0 + exp(-g));
             sl = g * sig;
@@ -631,7 +635,7 @@ int ora_grouped_mlp_bwd_rows(const uint16_t* x, int64_t R, int64_t H, int64_t F,
                              const float* gates, const uint8_t* w1q, const uint8_t* w1sf, const uint8_t* w2tq,
                              const uint8_t* w2tsf, const uint8_t* w1tq, const uint8_t* w1tsf, const uint16_t* dy,
                              const int64_t* rows, int64_t nrows, double* dx, double* dgate, uint16_t* dgu,
-                             uint16_t* h, int quant, int nthreads) {
+                             uint16_t* h, uint16_t* gu, int quant, int nthreads) {
     ora_bwd_ctx c;
     int64_t i;
     int rc = ora_bwd_setup(&c, x, R, H, F, E, split, gates, w1q, w1sf, w2tq, w2tsf, dy);
@@ -643,6 +647,7 @@ int ora_grouped_mlp_bwd_rows(const uint16_t* x, int64_t R, int64_t H, int64_t F,
     for (i = 0; i < nrows; ++i)
         if (rows[i] < 0 || rows[i] >= R) { free((void*)c.off); return ORA_BAD_ARG; }
     c.w1tq = w1tq; c.w1tsf = w1tsf; c.rows = rows; c.dx = dx; c.dgate = dgate; c.dgu_out = dgu; c.h_out = h;
+    c.gu_out = gu;
     c.quant = quant != 0;
     ora_parallel(ora_bwd_rows_range, &c, nrows, nthreads);
     free((void*)c.off);

@@ -185,7 +185,7 @@ def test_quantized_backward_matches_independent_restatement(oracle):
     gates = rng.uniform(0.1, 1.0, R).astype(np.float32)
     wq = _weights(oracle, w1, w2, E)
     rows = np.arange(R)
-    dx_o, dgate_o, dgu_o, h_o = oracle.grouped_mlp_bwd_rows(x, split, gates, *wq, dy, rows)
+    dx_o, dgate_o, dgu_o, h_o, gu_o = oracle.grouped_mlp_bwd_rows(x, split, gates, *wq, dy, rows, want_gu=True)
     dw2_o = oracle.grouped_mlp_bwd_dw(x, split, gates, *wq[:4], dy, 2, _all_entries(E, H, F))
     dw1_o = oracle.grouped_mlp_bwd_dw(x, split, gates, *wq[:4], dy, 1, _all_entries(E, 2 * F, H))
 
@@ -198,6 +198,7 @@ def test_quantized_backward_matches_independent_restatement(oracle):
     dgate = np.zeros(R)
     dgu = np.zeros((R, 2 * F))
     hb = np.zeros((R, F))
+    gub = np.zeros((R, 2 * F))
     dw2 = np.zeros((E, H, F))
     dw1 = np.zeros((E, 2 * F, H))
     T = torch.from_numpy
@@ -211,6 +212,7 @@ def test_quantized_backward_matches_independent_restatement(oracle):
         a = _rowq(xf[r0:r1])
         g = ind.bf16_round((T(a) @ T(W1q[:F]).T).numpy())
         u = ind.bf16_round((T(a) @ T(W1q[F:]).T).numpy())
+        gub[r0:r1] = np.concatenate([g, u], axis=1)
         gt = gates[r0:r1].astype(np.float64)[:, None]
         sig = 1.0 / (1.0 + np.exp(-g))
         s = g * sig
@@ -227,6 +229,7 @@ def test_quantized_backward_matches_independent_restatement(oracle):
 
     assert np.array_equal(f64(dgu_o), dgu)
     assert np.array_equal(f64(h_o), hb)
+    assert np.array_equal(f64(gu_o), gub)   # the forward's saved pre-activations
     np.testing.assert_allclose(dx_o, dx, rtol=1e-12, atol=1e-12 * np.abs(dx).max())
     np.testing.assert_allclose(dgate_o, dgate, rtol=1e-12, atol=1e-12 * np.abs(dgate).max())
     np.testing.assert_allclose(dw2_o, dw2.ravel(), rtol=1e-12, atol=1e-12 * np.abs(dw2).max())
