@@ -152,10 +152,10 @@ struct GemmParams {
   const uint16_t* gu;      // saved [G | U]
   uint8_t* dguq;           // [dG | dU] row-wise MXFP8 codes [R_pad, 2F]
   uint8_t* dgusf;          //   their scale bytes (tensor-core layout of [R_pad, 2F])
-  uint8_t* dguT;           // [dG | dU] column-wise MXFP8, codes transposed [2F, R_pad]
-  uint8_t* dguTsf;         //   their scale bytes (tensor-core layout of [2F, R_pad])
-  uint8_t* hT;             // h column-wise MXFP8, codes transposed [F, R_pad]
-  uint8_t* hTsf;           //   their scale bytes (tensor-core layout of [F, R_pad])
+  uint8_t* dguT;           // [dG | dU] and then h column-wise MXFP8, codes transposed: one
+                           // [3F, R_pad] matrix (the target of the epilogue's bulk tensor stores)
+  uint8_t* dguTsf;         //   scale bytes of [dG | dU] (tensor-core layout of [2F, R_pad])
+  uint8_t* hTsf;           //   scale bytes of h (tensor-core layout of [F, R_pad])
   int64_t r_pad;           // rows of the padded row space (columns of the transposed codes)
   int64_t t_kt;            // r_pad / 128: scale atoms per 128-row tile of the transposed matrices
   float* dgate_part;       // [R_pad, F / 128] partial sums of the routing-weight gradient
@@ -288,19 +288,25 @@ __device__ __forceinline__ int64_t gu_offset(int64_t prow, int64_t j, int64_t tw
 //   NVFP4 (FMT_NV): accumulators are first multiplied by alpha = 1 / (s_a s_b), the product of the
 //                operands' per-tensor decode scales; GEMM_SWIGLU requantizes h to NVFP4 under the
 //                encode scale s_out (four 16-value blocks per thread, E4M3 block scales).
-// One MXFP8 block of 32 bf16 values (pairs x2[i] = values 2i, 2i + 1) -> 32 E4M3 codes stored at
-// dst (32-byte aligned); returns the block's UE8M0 scale byte.
-__device__ __forceinline__ uint32_t quantize_block32_to(const uint32_t (&x2)[16], uint8_t* dst) {
+// One MXFP8 block of 32 bf16 values (pairs x2[i] = values 2i, 2i + 1) -> 32 E4M3 codes (q[k]: values
+// 4k .. 4k + 3, lowest byte first); returns the block's UE8M0 scale byte.
+__device__ __forceinline__ uint32_t quantize_block32(const uint32_t (&x2)[16], uint32_t (&q)[8]) {
   uint32_t m2 = absmax_bf16x2(x2[0]);
 #pragma unroll
   for (int i = 1; i < 16; ++i) m2 = absmax_bf16x2(m2, x2[i]);
   const uint32_t sfb = e8m0_from_amax(fmaxf(bf16_lo(m2), bf16_hi(m2)));
   const float inv = e8m0_inverse_scale(sfb);
-  uint32_t q[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k)
     q[k] = e4m3x2(bf16_lo(x2[2 * k]) * inv, bf16_hi(x2[2 * k]) * inv) |
            (e4m3x2(bf16_lo(x2[2 * k + 1]) * inv, bf16_hi(x2[2 * k + 1]) * inv) << 16);
+  return sfb;
+}
+
+// The same, codes stored at dst (32-byte aligned).
+__device__ __forceinline__ uint32_t quantize_block32_to(const uint32_t (&x2)[16], uint8_t* dst) {
+  uint32_t q[8];
+  const uint32_t sfb = quantize_block32(x2, q);
   st_global_32B(dst, make_uint4(q[0], q[1], q[2], q[3]), make_uint4(q[4], q[5], q[6], q[7]));
   return sfb;
 }
@@ -308,16 +314,25 @@ __device__ __forceinline__ uint32_t quantize_block32_to(const uint32_t (&x2)[16]
 // Column-wise MXFP8 blocks of a warp: lane l holds 32 bf16 values of its row, the warp's 32
 // lanes being 32 consecutive rows.  The 32 x 32 block passes through the warp's 2 KB of shared
 // memory (rows of 64 bytes; 16-byte chunk j of row i stored at chunk j ^ ((i >> 1) & 3), so that
-// both the row writes and the column reads are free of bank conflicts).  colblock_put writes
-// chunk j (columns 8j .. 8j + 7, as four bf16 pairs) of the lane's row; after all four chunks,
-// colblock_quantize has lane l read column l and write its 32 E4M3 codes (rows in order) to dst
-// (32-byte aligned) and its UE8M0 scale byte to *sf.  The caller keeps a __syncwarp between the
-// last colblock_quantize of a buffer's previous use and the next colblock_put.
+// both the row writes and the column reads are free of bank conflicts):
+//   colblock_acquire  waits until the buffer's previous bulk store has read it (before the first
+//                     colblock_put of a block);
+//   colblock_put      writes chunk j (columns 8j .. 8j + 7, as four bf16 pairs) of the lane's row;
+//   colblock_quantize (after all four chunks) has lane l read column l, take its block scale
+//                     (returned, the UE8M0 byte of column l) and put its 32 E4M3 codes (rows in
+//                     order) as row l of a 32 x 32-byte tile in the same buffer (32B swizzle:
+//                     16-byte chunk j of row l at j ^ ((l >> 2) & 1)), which one lane then writes
+//                     with a bulk tensor store to (x, y) of the transposed code matrix `tm`.
+__device__ __forceinline__ void colblock_acquire(int lane) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+}
+
 __device__ __forceinline__ void colblock_put(uint8_t* buf, int lane, int j, uint4 w) {
   *reinterpret_cast<uint4*>(buf + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) = w;
 }
 
-__device__ __forceinline__ void colblock_quantize(const uint8_t* buf, int lane, uint8_t* dst, uint8_t* sf) {
+__device__ __forceinline__ uint32_t colblock_quantize(uint8_t* buf, int lane, const CUtensorMap* tm, int x, int y) {
   __syncwarp();   // every lane's row is in place
   const int cj = lane >> 3, cw = 2 * (lane & 7);   // chunk and byte of column `lane` in a row
   uint32_t c2[16];                                 // column `lane`, rows (2i, 2i + 1) as bf16 pairs
@@ -327,14 +342,26 @@ __device__ __forceinline__ void colblock_quantize(const uint8_t* buf, int lane, 
     c2[i] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(buf + (2 * i) * 64 + o)) |
             (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(buf + (2 * i + 1) * 64 + o)) << 16);
   }
-  *sf = static_cast<uint8_t>(quantize_block32_to(c2, dst));
-  __syncwarp();   // the buffer may be written again
+  uint32_t q[8];
+  const uint32_t sfb = quantize_block32(c2, q);
+  __syncwarp();   // all columns are read: the buffer takes the codes
+  const int sw = (lane >> 2) & 1;
+  *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * sw) = make_uint4(q[0], q[1], q[2], q[3]);
+  *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * (sw ^ 1)) = make_uint4(q[4], q[5], q[6], q[7]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tm, buf, x, y);
+    bulk_commit_group();
+  }
+  return sfb;
 }
 
 template <int MODE, int FMT = FMT_MX>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& t, uint32_t* v, int r,
                                               int half, int BN, float alpha = 1.0f, float s_out = 1.0f,
-                                              uint8_t* wbuf = nullptr, uint32_t t_park = 0) {
+                                              uint8_t* wbuf = nullptr, uint32_t t_park = 0,
+                                              const CUtensorMap* tmT = nullptr) {
   if (MODE == GEMM_SWIGLU && FMT == FMT_NV) {
     const bool real = r < t.valid;
     const float gate = real ? (p.gates ? __ldg(p.gates + t.src_row0 + r) : 1.0f) : 0.0f;
@@ -476,6 +503,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
         tmem_ld_32x32b_x32(t_park + 32 * (b - 2), v);
         tmem_ld_wait();
       }
+      colblock_acquire(lane);
 #pragma unroll
       for (int c16 = 0; c16 < 2; ++c16) {
         uint4 gw2[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
@@ -516,23 +544,27 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
           colblock_put(wbuf, lane, 2 * c16 + hh, make_uint4(hp[0], hp[1], hp[2], hp[3]));   // h goes first
         }
       }
-      const int64_t fb = f0 + 32 * b;
+      const int fb = f0 + 32 * b;
       const int64_t cblk = prow0 >> 5;
-      // h column-wise; [dG | dU] row-wise (this row's block of each) and column-wise
-      colblock_quantize(wbuf, lane, p.hT + (fb + lane) * p.r_pad + prow0,
-                        p.hTsf + sf_mma_offset(fb + lane, cblk, p.t_kt));
+      const int x = static_cast<int>(prow0);
+      // h column-wise; [dG | dU] row-wise (this row's block of each) and column-wise.  Transposed
+      // codes: rows [0, F) dG, [F, 2F) dU, [2F, 3F) h of one [3F, r_pad] matrix.
+      p.hTsf[sf_mma_offset(fb + lane, cblk, p.t_kt)] =
+          static_cast<uint8_t>(colblock_quantize(wbuf, lane, tmT, x, static_cast<int>(2 * F) + fb));
       rsf_g |= quantize_block32_to(dg, p.dguq + prow * 2 * F + fb) << (8 * b);
+      colblock_acquire(lane);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         colblock_put(wbuf, lane, j, make_uint4(dg[4 * j], dg[4 * j + 1], dg[4 * j + 2], dg[4 * j + 3]));
-      colblock_quantize(wbuf, lane, p.dguT + (fb + lane) * p.r_pad + prow0,
-                        p.dguTsf + sf_mma_offset(fb + lane, cblk, p.t_kt));
+      p.dguTsf[sf_mma_offset(fb + lane, cblk, p.t_kt)] =
+          static_cast<uint8_t>(colblock_quantize(wbuf, lane, tmT, x, fb));
       rsf_u |= quantize_block32_to(du, p.dguq + prow * 2 * F + F + fb) << (8 * b);
+      colblock_acquire(lane);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         colblock_put(wbuf, lane, j, make_uint4(du[4 * j], du[4 * j + 1], du[4 * j + 2], du[4 * j + 3]));
-      colblock_quantize(wbuf, lane, p.dguT + (F + fb + lane) * p.r_pad + prow0,
-                        p.dguTsf + sf_mma_offset(F + fb + lane, cblk, p.t_kt));
+      p.dguTsf[sf_mma_offset(F + fb + lane, cblk, p.t_kt)] =
+          static_cast<uint8_t>(colblock_quantize(wbuf, lane, tmT, x, static_cast<int>(F) + fb));
     }
     // row-wise scale bytes: blocks f0/32 .. +3 of dG and (F + f0)/32 .. +3 of dU, one word each
     *reinterpret_cast<uint32_t*>(p.dgusf + sf_mma_offset(prow, f0 / 32, 2 * F / 128)) = rsf_g;
@@ -1427,11 +1459,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (MODE == GEMM_SWIGLU && half == 1) asm volatile("bar.sync %0, 64;" ::"r"(BAR_STAGGER + quarter) : "memory");
         epilogue_tile<MODE, FMT>(p, t, v, r, half, 256, alpha, s_out,
                                  smem + L::DATA_BYTES + (warp - FIRST_EPI_WARP) * 2 * P_WG_BUF_BYTES,
-                                 t_row + P_PARK_COL + 64 * half);
+                                 t_row + P_PARK_COL + 64 * half, &tmD);
         if (MODE == GEMM_SWIGLU && half == 0) asm volatile("bar.arrive %0, 64;" ::"r"(BAR_STAGGER + quarter) : "memory");
       }
     }
-    if ((MODE == GEMM_WGRAD || MODE == GEMM_OUT) && lane == 0) bulk_wait_all();   // stores complete before exit
+    if ((MODE == GEMM_WGRAD || MODE == GEMM_OUT || MODE == GEMM_DGRAD) && lane == 0)
+      bulk_wait_all();   // stores complete before exit
   }
 
   tc_fence_before();
@@ -1571,6 +1604,20 @@ bool make_y_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The backward's transposed column-wise codes [rows, cols] bytes as the target of TMA stores:
+// boxes of 32 rows x 32 bytes (32B swizzle), matching the dh epilogue's staging tiles.
+bool make_t_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  auto enc = tensor_map_encoder();
+  if (!enc || rows == 0 || cols == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_dw_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
   auto enc = tensor_map_encoder();
   if (!enc || rows == 0 || cols == 0) return false;
@@ -1624,13 +1671,16 @@ template <int MODE, int FMT = FMT_MX>
 cudaError_t launch_pair(int clusters, const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                         cudaStream_t stream) {
   constexpr uint32_t box_atoms = PairLayout<FMT>::SF_ATOMS;
-  CUtensorMap sa, sb, d = a;   // d: the weight-gradient output (other modes do not use it)
+  CUtensorMap sa, sb, d = a;   // d: the store target of GEMM_WGRAD (dW), GEMM_OUT (y), GEMM_DGRAD
+                               // (transposed codes of dGU and h)
   if (!make_sf_map(&sa, p.a_sf, static_cast<uint64_t>(p.a_sf_tiles) * p.a_kt, box_atoms) ||
       !make_sf_map(&sb, p.b_sf, static_cast<uint64_t>(p.b_sf_tiles) * p.b_kt, box_atoms))
     return cudaErrorInvalidValue;
   if (MODE == GEMM_WGRAD && !make_dw_map(&d, p.dw, static_cast<uint64_t>(p.E) * p.wg_m, p.wg_n))
     return cudaErrorInvalidValue;
   if (MODE == GEMM_OUT && p.y_rows > 0 && !make_y_map(&d, p.y, static_cast<uint64_t>(p.y_rows), p.ldy))
+    return cudaErrorInvalidValue;
+  if (MODE == GEMM_DGRAD && !make_t_map(&d, p.dguT, static_cast<uint64_t>(3 * p.ldh), static_cast<uint64_t>(p.r_pad)))
     return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config<MODE, FMT>(clusters, attr, stream);
@@ -1922,9 +1972,9 @@ bool bwd_ws_layout(int64_t R, int64_t H, int64_t F, int E, BwdWsLayout* out) {
   L.dguq = al(L.xTsf + rp * H / 32);
   L.dgusf = al(L.dguq + rp * 2 * F);
   L.dguT = al(L.dgusf + rp * 2 * F / 32);
-  L.dguTsf = al(L.dguT + rp * 2 * F);
-  L.hT = al(L.dguTsf + rp * 2 * F / 32);
-  L.hTsf = al(L.hT + rp * F);
+  L.hT = L.dguT + rp * 2 * F;                     // right after dGU's codes: one [3F, r_pad] matrix
+  L.dguTsf = al(L.hT + rp * F);
+  L.hTsf = al(L.dguTsf + rp * 2 * F / 32);
   L.part = al(L.hTsf + rp * F / 32);
   L.total = al(L.part + rp * (F / 128) * sizeof(float));
   *out = L;
@@ -1997,7 +2047,6 @@ int launch_grouped_mlp_bwd(const void* x_sorted, int64_t R, int64_t H, int64_t F
   pd.dgusf = ws + L.dgusf;
   pd.dguT = ws + L.dguT;
   pd.dguTsf = ws + L.dguTsf;
-  pd.hT = ws + L.hT;
   pd.hTsf = ws + L.hTsf;
   pd.r_pad = rp;
   pd.t_kt = rp / BM;
