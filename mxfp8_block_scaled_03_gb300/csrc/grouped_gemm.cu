@@ -291,15 +291,17 @@ __device__ __forceinline__ int64_t gu_offset(int64_t prow, int64_t j, int64_t tw
 // One MXFP8 block of 32 bf16 values (pairs x2[i] = values 2i, 2i + 1) -> 32 E4M3 codes (q[k]: values
 // 4k .. 4k + 3, lowest byte first); returns the block's UE8M0 scale byte.
 __device__ __forceinline__ uint32_t quantize_block32(const uint32_t (&x2)[16], uint32_t (&q)[8]) {
-  uint32_t m2 = absmax_bf16x2(x2[0]);
+  // block amax on packed magnitudes (the running maximum is already non-negative)
+  uint32_t m2 = x2[0] & 0x7FFF7FFFu;
 #pragma unroll
-  for (int i = 1; i < 16; ++i) m2 = absmax_bf16x2(m2, x2[i]);
+  for (int i = 1; i < 16; ++i) asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(x2[i] & 0x7FFF7FFFu));
   const uint32_t sfb = e8m0_from_amax(fmaxf(bf16_lo(m2), bf16_hi(m2)));
   const float inv = e8m0_inverse_scale(sfb);
+  const uint64_t inv2 = f2_pack(inv, inv);
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    q[k] = e4m3x2(bf16_lo(x2[2 * k]) * inv, bf16_hi(x2[2 * k]) * inv) |
-           (e4m3x2(bf16_lo(x2[2 * k + 1]) * inv, bf16_hi(x2[2 * k + 1]) * inv) << 16);
+  for (int k = 0; k < 8; ++k)   // the exact power-of-two scaling, two values per instruction
+    q[k] = e4m3x2_f2(f2_mul(f2_pack(bf16_lo(x2[2 * k]), bf16_hi(x2[2 * k])), inv2)) |
+           (e4m3x2_f2(f2_mul(f2_pack(bf16_lo(x2[2 * k + 1]), bf16_hi(x2[2 * k + 1])), inv2)) << 16);
   return sfb;
 }
 
