@@ -19,7 +19,10 @@
 //   4. k_grouped_gemm_pair<GEMM_OUT>     per pair tile (expert e, 256 rows, 256 columns of H):
 //                    y = h_q W2[e]^T -> bf16, stored only for the expert's real rows.
 // Backward (launch_grouped_mlp_bwd): GEMM_DGRAD (dh = dy W2 with the ScaledSwiGLU backward in the
-// epilogue), GEMM_OUT (dx = dGU W1), GEMM_WGRAD (dW2, dW1 over each expert's rows).
+// epilogue, which writes dGU and h already quantized: dGU row-wise for dx, dGU and h column-wise
+// with transposed codes for the weight gradients), GEMM_OUT (dx = dGU W1), GEMM_WGRAD (dW2, dW1
+// over each expert's rows).  NVFP4 forward (launch_nvfp4_grouped_mlp): the FMT_NV instances of the
+// two forward GEMMs.
 //
 // Main kernel (k_grouped_gemm_pair, persistent clusters of two CTAs on two SMs, 512 threads each):
 // one tcgen05.mma.cta_group::2 computes a 256 x 256 tile, each CTA loading its own 128 rows of A
@@ -867,11 +870,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // (A separate 16-slot scale ring, filled by four tcgen05.st warps and a second producer and
 // synchronized by three more barrier kinds, was about 3% slower on GroupedLinear 1.)
 // Warp roles: warp 4 producer (both CTAs), warp 5 MMA issuer (leader CTA; the MMA warp of the
-// second CTA only takes part in the TMEM allocation), warps 8-15 epilogue; the other role warps idle.
+// second CTA only takes part in the TMEM allocation), warps 8-15 epilogue, warps 0-3 NVFP4 scale
+// staging (FMT_NV); the other role warps idle.
 // ---------------------------------------------------------------------------------------------
 constexpr int P_STEP_BYTES = 2 * 128 * BK;                    // own A tile + own half of the B tile
-// GEMM_WGRAD epilogue: each epilogue warp stages its 32 rows x 8 fp32 columns in one of two 1 KB
-// buffers (32-byte rows, 32B swizzle) that a TMA store then writes out
+// Epilogue staging: each epilogue warp owns 2 KB of shared memory, used as two 1 KB buffers of
+// 32 rows x 32 bytes (32B swizzle) that TMA stores write out (GEMM_WGRAD: 8 fp32 columns; GEMM_OUT:
+// 16 bf16 columns of y), or as one 32 x 32 bf16 block that GEMM_DGRAD transposes through
 constexpr int P_WG_CHUNK = 8;                                  // fp32 columns per TMA store
 constexpr int P_WG_BUF_BYTES = 32 * P_WG_CHUNK * 4;            // 1 KB
 constexpr int P_EPI_BYTES = NUM_EPI_WARPS * 2 * P_WG_BUF_BYTES;
