@@ -106,7 +106,10 @@ size_t grouped_mlp_workspace_size(int64_t R, int64_t H, int64_t F, int E);
  *   y           (device) bf16 [R, H] output, rows in x_sorted's order; fully overwritten.
  *   workspace   (device) at least grouped_mlp_workspace_size(R, H, F, E) bytes, 256-byte
  *               aligned.  It must not be shared by two calls in flight at the same time.
- * Requirements: R >= 0, 1 <= E <= 1024, H % 128 == 0, F % 128 == 0, H, F >= 128.
+ * Requirements: R >= 0, 1 <= E <= 1024, H % 128 == 0, F % 128 == 0, H, F >= 128.  With R == 0
+ * (no routed rows, e.g. an expert-parallel rank that received no tokens) x_sorted and y may be
+ * NULL; the call still checks split_sizes on the device.  The same holds for the row buffers of
+ * the other grouped-MLP calls below (x, the output gradient, dx, token_of_row).
  * The call never reads split_sizes on the host.  If they do not sum to R (or one is negative),
  * the kernels do no work, y is left unspecified and the workspace's error word reports
  * MXFP8_ERR_SPLIT_MISMATCH.

@@ -14,6 +14,8 @@ namespace mx {
 namespace {
 constexpr size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// A buffer of `rows` rows: 16-byte aligned, and non-NULL unless it holds no rows.
+bool rows_ok(const void* p, int64_t rows) { return p == nullptr ? rows == 0 : aligned16(p); }
 }  // namespace
 
 bool ws_layout(int64_t R, int64_t H, int64_t F, int E, WsLayout* out) {
@@ -114,10 +116,12 @@ static int grouped_mlp_fwd_impl(const void* x_sorted, int64_t R, int64_t H, int6
   if (H % 128 != 0 || F % 128 != 0) return MXFP8_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(E) * 2 * F > INT32_MAX || static_cast<int64_t>(E) * H > INT32_MAX)
     return MXFP8_ERR_UNSUPPORTED;
-  const void* ptrs[] = {x_sorted, split_sizes, w1_q, w1_sf, w2_q, w2_sf, y, workspace};
+  const void* ptrs[] = {split_sizes, w1_q, w1_sf, w2_q, w2_sf, workspace};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return MXFP8_ERR_INVALID_ARG;
-  if (gates != nullptr && !aligned16(gates)) return MXFP8_ERR_INVALID_ARG;
+  // row buffers: required when they hold rows (a call without routed rows may pass NULL)
+  if (!rows_ok(x_sorted, token_of_row != nullptr ? x_rows : R) || !rows_ok(y, R) || !rows_ok(gates, 0))
+    return MXFP8_ERR_INVALID_ARG;
   WsLayout L;
   if (!ws_layout(R, H, F, E, &L)) return MXFP8_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < L.total) return MXFP8_ERR_WORKSPACE;
@@ -148,7 +152,7 @@ int grouped_mlp_fwd_tokens(const void* x_tokens, int64_t T, const int32_t* token
                            int64_t F, int E, const int32_t* split_sizes, const float* gates_sorted,
                            const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q, const uint8_t* w2_sf,
                            void* y_rows, void* workspace, size_t workspace_bytes, void* stream) {
-  if (T < 0 || token_of_row == nullptr || !aligned16(token_of_row)) return MXFP8_ERR_INVALID_ARG;
+  if (T < 0 || !rows_ok(token_of_row, R)) return MXFP8_ERR_INVALID_ARG;
   return grouped_mlp_fwd_impl(x_tokens, R, H, F, E, split_sizes, gates_sorted, w1_q, w1_sf, w2_q, w2_sf, y_rows,
                               workspace, workspace_bytes, stream, nullptr, token_of_row, T);
 }
@@ -241,10 +245,13 @@ static int grouped_mlp_bwd_impl(const void* x_sorted, int64_t R, int64_t H, int6
   if (H % 256 != 0 || F % 128 != 0) return MXFP8_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(E) * 2 * F > INT32_MAX || static_cast<int64_t>(E) * H > INT32_MAX)
     return MXFP8_ERR_UNSUPPORTED;
-  const void* ptrs[] = {x_sorted, split_sizes, saved, w1t_q, w1t_sf, w2t_q, w2t_sf, dy, dx, dw1, dw2, workspace};
+  const void* ptrs[] = {split_sizes, saved, w1t_q, w1t_sf, w2t_q, w2t_sf, dw1, dw2, workspace};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return MXFP8_ERR_INVALID_ARG;
-  if ((gates != nullptr && !aligned16(gates)) || (dgates != nullptr && !aligned16(dgates)))
+  // row buffers: required when they hold rows (a call without routed rows may pass NULL)
+  const int64_t src_rows = token_of_row != nullptr ? x_rows : R;
+  if (!rows_ok(x_sorted, src_rows) || !rows_ok(dy, src_rows) || !rows_ok(dx, R) || !rows_ok(gates, 0) ||
+      !rows_ok(dgates, 0))
     return MXFP8_ERR_INVALID_ARG;
   BwdWsLayout L;
   if (!bwd_ws_layout(R, H, F, E, &L)) return MXFP8_ERR_UNSUPPORTED;
@@ -278,7 +285,7 @@ int grouped_mlp_fwd_tokens_train(const void* x_tokens, int64_t T, const int32_t*
                                  const uint8_t* w1_q, const uint8_t* w1_sf, const uint8_t* w2_q, const uint8_t* w2_sf,
                                  void* y_rows, void* saved, size_t saved_bytes, void* workspace,
                                  size_t workspace_bytes, void* stream) {
-  if (T < 0 || token_of_row == nullptr || !aligned16(token_of_row) || saved == nullptr) return MXFP8_ERR_INVALID_ARG;
+  if (T < 0 || !rows_ok(token_of_row, R) || saved == nullptr) return MXFP8_ERR_INVALID_ARG;
   return grouped_mlp_fwd_impl(x_tokens, R, H, F, E, split_sizes, gates_sorted, w1_q, w1_sf, w2_q, w2_sf, y_rows,
                               workspace, workspace_bytes, stream, nullptr, token_of_row, T, saved, saved_bytes);
 }
@@ -288,7 +295,7 @@ int grouped_mlp_bwd_tokens(const void* x_tokens, int64_t T, const int32_t* token
                            size_t saved_bytes, const uint8_t* w1t_q, const uint8_t* w1t_sf, const uint8_t* w2t_q,
                            const uint8_t* w2t_sf, const void* d_out_tokens, void* dx_rows, float* dgates_sorted,
                            float* dw1, float* dw2, void* workspace, size_t workspace_bytes, void* stream) {
-  if (T < 0 || token_of_row == nullptr) return MXFP8_ERR_INVALID_ARG;
+  if (T < 0 || !rows_ok(token_of_row, R)) return MXFP8_ERR_INVALID_ARG;
   return grouped_mlp_bwd_impl(x_tokens, R, H, F, E, split_sizes, gates_sorted, saved, saved_bytes, w1t_q, w1t_sf,
                               w2t_q, w2t_sf, d_out_tokens, dx_rows, dgates_sorted, dw1, dw2, workspace,
                               workspace_bytes, stream, nullptr, token_of_row, T);

@@ -85,6 +85,10 @@ def test_host_argument_checks(lib):
     assert g(*bad) == 1                                                                   # E
     bad = list(args); bad[5] = None
     assert g(*bad) == 1                                                                   # split_sizes
+    bad = list(args); bad[0] = None
+    assert g(*bad) == 1                                                                   # null x with rows
+    bad = list(args); bad[11] = None
+    assert g(*bad) == 1                                                                   # null y with rows
     bad = list(args); bad[13] = 1000
     assert g(*bad) == 3                                                                   # workspace too small
     bad = list(args); bad[12] = P((1 << 20) + 16)

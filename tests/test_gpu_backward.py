@@ -288,3 +288,30 @@ def test_mixtral_backward_sampled(mx, oracle):
     w = W.moe_workload("mixtral")
     rows = W.sample_rows(w.split_sizes, seed=0, first=8, last=8, rand=8, tile=128)
     _assert_bwd_parity(mx, oracle, w, rows, 160, all_blocks=False)
+
+
+def test_no_routed_rows_forward_and_backward(mx):
+    """R = 0 (every expert empty, as on an expert-parallel rank that received no tokens): the
+    forward, the training forward and the backward accept empty row buffers, report no device
+    error, and the weight gradients are exactly zero."""
+    import torch
+    w = W.custom_moe([0, 0, 0], H=256, F=256, seed=31)
+    x = G.to_dev_bf16(w.x_sorted)
+    split = G.to_dev(w.split_sizes)
+    g = G.to_dev(w.gates)
+    w1 = G.to_dev_bf16(w.w1)
+    w2 = G.to_dev_bf16(w.w2)
+    w1q, w1s, _, _ = mx.mxfp8_quantize(w1, sf_layout=mx.SF_MMA)
+    w2q, w2s, _, _ = mx.mxfp8_quantize(w2, sf_layout=mx.SF_MMA)
+    ws = torch.zeros(mx.grouped_mlp_workspace_size(0, w.H, w.F, w.E), dtype=torch.uint8, device="cuda")
+    y = mx.grouped_mlp_fwd(x, split, g, w1q, w1s, w2q, w2s, workspace=ws)
+    assert tuple(y.shape) == (0, w.H) and mx.mxfp8_check_device_error(ws) == (0, 0)
+    y, saved = mx.grouped_mlp_fwd_train(x, split, g, w1q, w1s, w2q, w2s, workspace=ws)
+    assert mx.mxfp8_check_device_error(ws) == (0, 0)
+    w1tq, w1ts = mx.mxfp8_quantize_colwise_t(w1)
+    w2tq, w2ts = mx.mxfp8_quantize_colwise_t(w2)
+    dx, dg, dw1, dw2, bws = mx.grouped_mlp_bwd(x, split, g, saved, w1tq, w1ts, w2tq, w2ts,
+                                               G.to_dev_bf16(_dy(w, 1)))
+    assert mx.mxfp8_check_device_error(bws) == (0, 0)
+    assert tuple(dx.shape) == (0, w.H)
+    assert not bool(dw1.any()) and not bool(dw2.any())
