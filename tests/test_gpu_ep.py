@@ -187,3 +187,26 @@ def test_ep_layer_forward_and_backward_match_oracle(mx, nccl_group, oracle, name
                            ("dx", dx[toks], dx_ref), ("d gates", dg[toks], dg_ref)):
         rel, mxe = G.y_errors(got, ref)
         assert rel <= G.Y_REL_TOL and mxe <= G.Y_MAX_TOL, f"{what}: rel {rel:.3e} max {mxe:.3e}"
+
+
+def test_ep_layer_without_tokens(mx, nccl_group):
+    """A rank with no tokens (T = 0, so it also owns no routed rows): the expert-parallel layer's
+    forward, training forward and backward run through the empty exchanges and the empty grouped
+    MLP calls, return empty outputs and zero weight gradients."""
+    import torch
+    from mxfp8_block_scaled_03_gb300 import ep
+    w = W.moe_workload("tiny")
+    x = torch.zeros((0, w.H), dtype=torch.bfloat16, device="cuda")
+    ex = torch.zeros((0, w.topk), dtype=torch.int32, device="cuda")
+    g = torch.zeros((0, w.topk), dtype=torch.float32, device="cuda")
+    wts = _weights(mx, w)
+    w1t = mx.mxfp8_quantize_colwise_t(G.to_dev_bf16(w.w1))
+    w2t = mx.mxfp8_quantize_colwise_t(G.to_dev_bf16(w.w2))
+    out = ep.ep_moe_forward(x, ex, g, wts, w.E)
+    out_t, ctx = ep.ep_moe_forward_train(x, ex, g, wts, w.E)
+    dx, dg, dw1, dw2 = ep.ep_moe_backward(torch.zeros((0, w.H), dtype=torch.bfloat16, device="cuda"), ctx,
+                                          (w1t[0], w1t[1], w2t[0], w2t[1]))
+    torch.cuda.synchronize()
+    assert tuple(out.shape) == (0, w.H) and tuple(out_t.shape) == (0, w.H) and tuple(dx.shape) == (0, w.H)
+    assert dg.numel() == 0
+    assert not bool(dw1.any()) and not bool(dw2.any())
