@@ -191,8 +191,8 @@ def test_ep_layer_forward_and_backward_match_oracle(mx, nccl_group, oracle, name
 
 def test_ep_layer_without_tokens(mx, nccl_group):
     """A rank with no tokens (T = 0, so it also owns no routed rows): the expert-parallel layer's
-    forward, training forward and backward run through the empty exchanges and the empty grouped
-    MLP calls, return empty outputs and zero weight gradients."""
+    forward, training forward and backward run through the empty exchanges and return empty
+    outputs; the weight gradients are None (no row reached the rank's experts) or zero."""
     import torch
     from mxfp8_block_scaled_03_gb300 import ep
     w = W.moe_workload("tiny")
@@ -209,4 +209,5 @@ def test_ep_layer_without_tokens(mx, nccl_group):
     torch.cuda.synchronize()
     assert tuple(out.shape) == (0, w.H) and tuple(out_t.shape) == (0, w.H) and tuple(dx.shape) == (0, w.H)
     assert dg.numel() == 0
-    assert not bool(dw1.any()) and not bool(dw2.any())
+    for dw in (dw1, dw2):
+        assert dw is None or not bool(dw.any())
