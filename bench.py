@@ -483,12 +483,15 @@ def forward_summary(fwd, step_ms, kern_ms, fp8_peak, mma_peak, world=1):
 def quantize_sweep(mx, dev, peaks, steps):
     """Stand-alone MXFP8 quantize of the sweep's three bf16 matrices, row-wise and row + column.
     Inputs that fit in L2 (the two smaller shapes) are timed one launch at a time with L2 flushed
-    (a 512 MiB buffer written) before each; the largest (470 MB) is timed over back-to-back
-    launches, its input far above L2."""
+    before each by reading a 512 MiB buffer (a read leaves L2 holding clean lines; a written
+    flush buffer would leave about L2's size of dirty lines whose write-back then competes with
+    the timed launch's reads); the largest (470 MB) is timed over back-to-back launches, its
+    input far above L2."""
     import numpy as np
     import torch
     from mxfp8_block_scaled_03_gb300 import workloads as W
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.ones(512 << 20, dtype=torch.uint8, device=dev)
+    flush64 = flush.view(torch.int64)
     out = []
     for (M, K) in ((4096, 4096), (8192, 4096), (16384, 14336)):
         x = torch.from_numpy(W.quant_matrix(M, K, seed=0).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -502,7 +505,7 @@ def quantize_sweep(mx, dev, peaks, steps):
             if small:
                 tot = 0.0
                 for _ in range(n):
-                    flush.fill_(1)
+                    torch.amax(flush64)
                     e0, e1 = _events(2)
                     e0.record()
                     mx.mxfp8_quantize(x, rowwise=True, colwise=col, out=buf)
@@ -522,10 +525,10 @@ def quantize_sweep(mx, dev, peaks, steps):
             gbs = nbytes / (ms * 1e-3) / 1e9
             out.append({"shape": [M, K], "directions": dirs, "ms": ms, "achieved": gbs, "unit": "GB/s",
                         "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
-                        "l2": "flushed before each launch" if small else "no flush: input above L2"})
+                        "l2": "flushed (512 MiB read) before each launch" if small else "no flush: input above L2"})
             del buf
         del x
-    del flush
+    del flush, flush64
     torch.cuda.empty_cache()
     return out
 
