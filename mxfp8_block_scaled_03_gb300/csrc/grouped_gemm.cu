@@ -875,10 +875,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // ---------------------------------------------------------------------------------------------
 constexpr int P_STEP_BYTES = 2 * 128 * BK;                    // own A tile + own half of the B tile
 // Epilogue staging: each epilogue warp owns 2 KB of shared memory, used as two 1 KB buffers of
-// 32 rows x 32 bytes (32B swizzle) that TMA stores write out (GEMM_WGRAD: 8 fp32 columns; GEMM_OUT:
-// 16 bf16 columns of y), or as one 32 x 32 bf16 block that GEMM_DGRAD transposes through
-constexpr int P_WG_CHUNK = 8;                                  // fp32 columns per TMA store
-constexpr int P_WG_BUF_BYTES = 32 * P_WG_CHUNK * 4;            // 1 KB
+// 32 rows x 32 bytes (32B swizzle) for TMA stores of 16 bf16 columns of y (GEMM_OUT), as one 2 KB
+// buffer of 32 rows x 16 fp32 columns for the weight gradients' TMA stores (GEMM_WGRAD), or as one
+// 32 x 32 bf16 block that GEMM_DGRAD transposes through
+constexpr int P_WG_BUF_BYTES = 1024;                           // per warp: two of these
+constexpr int P_WG_CHUNK = 16;                                 // GEMM_WGRAD: fp32 columns per TMA store
 constexpr int P_EPI_BYTES = NUM_EPI_WARPS * 2 * P_WG_BUF_BYTES;
 // GEMM_DGRAD (MXFP8): TMEM columns past the scale slots where each epilogue warp parks the upper
 // 64 of its 128 accumulator columns (64 * half + 0 .. 63).
@@ -1388,23 +1389,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive_remote(leader_acc_empty);   // the leader may overwrite TMEM
       acc_phase ^= 1u;
       if constexpr (MODE == GEMM_WGRAD) {
-        // 128 fp32 columns of this warp's 32 rows, 8 columns per TMA store from a double-buffered
-        // 1 KB staging area: a warp instruction writes 512 contiguous bytes of shared memory, where
-        // row-per-lane global stores touched 32 rows per instruction and held the epilogue up.
+        // 128 fp32 columns of this warp's 32 rows, 16 columns per TMA store from the warp's 2 KB
+        // staging buffer (row-per-lane global stores touched 32 rows per instruction and held the
+        // epilogue up; eight 2 KB stores per tile half beat sixteen 1 KB ones double-buffered, and
+        // thirty-two 512-byte ones four-buffered were slower still: the stores' count matters).
         if (t.n * 256 + 128 * half < p.wg_n) {
           const int col0 = t.n * 256 + 128 * half;
           const int grow = t.e * p.wg_m + t.a_row + quarter * 32;   // row in the [E * wg_m, wg_n] view
           uint8_t* wbuf = smem + L::DATA_BYTES + (warp - FIRST_EPI_WARP) * 2 * P_WG_BUF_BYTES;
 #pragma unroll
           for (int c = 0; c < 128; c += P_WG_CHUNK) {
-            uint8_t* buf = wbuf + ((c / P_WG_CHUNK) & 1) * P_WG_BUF_BYTES;
-            if (lane == 0) bulk_wait_read_le1();   // the store that last used this buffer has read it
+            uint8_t* buf = wbuf;
+            if (lane == 0) bulk_wait_read_all();   // the previous store has read the buffer
             __syncwarp();
-            // row `lane`: two 16-byte chunks, 32B swizzle (chunk j of row i at j ^ ((i >> 2) & 1))
-            const int sw = (lane >> 2) & 1;
-            *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * sw) = make_uint4(v[c], v[c + 1], v[c + 2], v[c + 3]);
-            *reinterpret_cast<uint4*>(buf + lane * 32 + 16 * (sw ^ 1)) =
-                make_uint4(v[c + 4], v[c + 5], v[c + 6], v[c + 7]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)   // row `lane`: four 16-byte chunks (64 bytes)
+              *reinterpret_cast<uint4*>(buf + lane * 64 + 16 * j) =
+                  make_uint4(v[c + 4 * j], v[c + 4 * j + 1], v[c + 4 * j + 2], v[c + 4 * j + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -1595,8 +1596,8 @@ bool make_sf_map(CUtensorMap* m, const void* base, uint64_t atoms, uint32_t box_
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The fp32 weight gradient [E * wg_m, wg_n] as the target of TMA stores: boxes of 32 rows x 8
-// columns (32-byte rows, 32B swizzle), matching the epilogue's staging buffers.
+// The fp32 weight gradient [E * wg_m, wg_n] as the target of TMA stores: boxes of 32 rows x 16
+// columns (64-byte rows, no swizzle), matching the epilogue's staging buffer.
 // y [rows, cols] bf16 as the target of TMA stores: boxes of 32 rows x 16 columns (32-byte rows, 32B
 // swizzle), matching the GEMM_OUT epilogue's staging buffers.
 bool make_y_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
@@ -1633,7 +1634,7 @@ bool make_dw_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols)
   cuuint32_t box[2] = {static_cast<cuuint32_t>(P_WG_CHUNK), 32};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
