@@ -1402,9 +1402,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint8_t* buf = wbuf;
             if (lane == 0) bulk_wait_read_all();   // the previous store has read the buffer
             __syncwarp();
+            // row `lane`: four 16-byte chunks (64 bytes), 64B swizzle (chunk j of row i at
+            // j ^ ((i >> 1) & 3)), so that the eight rows of each shared-memory wavefront fall in
+            // distinct banks (unswizzled 64-byte rows put four of them in one bank group)
 #pragma unroll
-            for (int j = 0; j < 4; ++j)   // row `lane`: four 16-byte chunks (64 bytes)
-              *reinterpret_cast<uint4*>(buf + lane * 64 + 16 * j) =
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(buf + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) =
                   make_uint4(v[c + 4 * j], v[c + 4 * j + 1], v[c + 4 * j + 2], v[c + 4 * j + 3]);
             fence_proxy_async_smem();
             __syncwarp();
@@ -1596,8 +1599,6 @@ bool make_sf_map(CUtensorMap* m, const void* base, uint64_t atoms, uint32_t box_
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The fp32 weight gradient [E * wg_m, wg_n] as the target of TMA stores: boxes of 32 rows x 16
-// columns (64-byte rows, no swizzle), matching the epilogue's staging buffer.
 // y [rows, cols] bf16 as the target of TMA stores: boxes of 32 rows x 16 columns (32-byte rows, 32B
 // swizzle), matching the GEMM_OUT epilogue's staging buffers.
 bool make_y_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
@@ -1626,6 +1627,8 @@ bool make_t_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The fp32 weight gradient [E * wg_m, wg_n] as the target of TMA stores: boxes of 32 rows x 16
+// columns (64-byte rows, 64B swizzle), matching the GEMM_WGRAD epilogue's staging buffer.
 bool make_dw_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
   auto enc = tensor_map_encoder();
   if (!enc || rows == 0 || cols == 0) return false;
@@ -1634,7 +1637,7 @@ bool make_dw_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols)
   cuuint32_t box[2] = {static_cast<cuuint32_t>(P_WG_CHUNK), 32};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
