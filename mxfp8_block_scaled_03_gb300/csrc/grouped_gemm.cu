@@ -339,13 +339,14 @@ __device__ __forceinline__ void colblock_put(uint8_t* buf, int lane, int j, uint
 
 __device__ __forceinline__ uint32_t colblock_quantize(uint8_t* buf, int lane, const CUtensorMap* tm, int x, int y) {
   __syncwarp();   // every lane's row is in place
-  const int cj = lane >> 3, cw = 2 * (lane & 7);   // chunk and byte of column `lane` in a row
+  const int cj = lane >> 3, cw = 4 * ((lane & 7) >> 1);   // chunk and word of column `lane` in a row
+  const uint32_t sel = (lane & 1) ? 0x7632u : 0x5410u;      // its half of the word, from both rows
   uint32_t c2[16];                                 // column `lane`, rows (2i, 2i + 1) as bf16 pairs
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int o = 16 * (cj ^ (i & 3)) + cw;        // rows 2i and 2i + 1 share the swizzle
-    c2[i] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(buf + (2 * i) * 64 + o)) |
-            (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(buf + (2 * i + 1) * 64 + o)) << 16);
+    c2[i] = __byte_perm(*reinterpret_cast<const uint32_t*>(buf + (2 * i) * 64 + o),
+                        *reinterpret_cast<const uint32_t*>(buf + (2 * i + 1) * 64 + o), sel);
   }
   uint32_t q[8];
   const uint32_t sfb = quantize_block32(c2, q);
