@@ -294,10 +294,12 @@ __device__ __forceinline__ int64_t gu_offset(int64_t prow, int64_t j, int64_t tw
 // One MXFP8 block of 32 bf16 values (pairs x2[i] = values 2i, 2i + 1) -> 32 E4M3 codes (q[k]: values
 // 4k .. 4k + 3, lowest byte first); returns the block's UE8M0 scale byte.
 __device__ __forceinline__ uint32_t quantize_block32(const uint32_t (&x2)[16], uint32_t (&q)[8]) {
-  // block amax on packed magnitudes (the running maximum is already non-negative)
-  uint32_t m2 = x2[0] & 0x7FFF7FFFu;
+  // block amax on packed magnitudes: max.xorsign.abs keeps the larger magnitude of each half
+  // (its sign, the XOR of the operands' signs, is cleared at the end)
+  uint32_t m2 = x2[0];
 #pragma unroll
-  for (int i = 1; i < 16; ++i) asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(x2[i] & 0x7FFF7FFFu));
+  for (int i = 1; i < 16; ++i) asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(x2[i]));
+  m2 &= 0x7FFF7FFFu;
   const uint32_t sfb = e8m0_from_amax(fmaxf(bf16_lo(m2), bf16_hi(m2)));
   const float inv = e8m0_inverse_scale(sfb);
   const uint64_t inv2 = f2_pack(inv, inv);
@@ -474,7 +476,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     }
   } else if (MODE == GEMM_DGRAD) {
     // v = dh for 128 columns f of F.  From the saved bf16 pre-activations g, u and the gate:
-    //   s = silu(g) = g * sig(g),  s' = sig(g) * (1 + g * (1 - sig(g)))
+    //   s = silu(g) = g * sig(g),  s' = sig(g) * (1 + g * (1 - sig(g))) = sig(g) + s * (1 - sig(g))
     //   dG = dh * gate * u * s',  dU = dh * gate * s,  h = gate * s * u,  dgate += dh * s * u
     // dG, dU and h are rounded to bf16 (the tensors the backward hands between its GEMMs) and leave
     // this epilogue quantized the way the next GEMMs read them:
@@ -537,7 +539,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
             const uint64_t sig = f2_pack(__fdividef(1.0f, f2_lo(d)), __fdividef(1.0f, f2_hi(d)));
             const uint64_t sl = f2_mul(g, sig);                                    // silu(g)
             const uint64_t su = f2_mul(sl, u);                                     // silu(g) u
-            const uint64_t dsl = f2_mul(sig, f2_fma(g, f2_fma(sig, mone2, one2), one2));   // silu'(g)
+            const uint64_t dsl = f2_fma(sl, f2_fma(sig, mone2, one2), sig);   // silu'(g) = sig + silu(g)(1 - sig)
             const uint64_t dhg = f2_mul(dh, gate2);
             part2 = f2_fma(dh, su, part2);
             const uint64_t dgv = f2_mul(f2_mul(dhg, u), dsl);
