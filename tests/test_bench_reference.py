@@ -69,3 +69,18 @@ def test_reference_arm_two_ranks_rank0_only():
     assert len(lines0) == 1
     _check_line(json.loads(lines0[0]), 2)
     assert not [x for x in out[1].splitlines() if x.startswith("{")]
+
+
+def test_stored_dram_counters_match_the_kernel_sources():
+    """profiles/traffic.json (the ncu DRAM bytes the bench line's roofline `traffic` reports) is
+    keyed to a hash of the kernel sources' code; a kernel edit without a new capture would make
+    the bench report null traffic, so the committed state must match."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        stored = json.load(f)
+    assert stored["kernel_hash"] == bench.kernel_hash()
+    t = bench.load_traffic()
+    for key in ("grouped_linear1_bytes_per_launch", "grouped_linear2_bytes_per_launch", "quantize_bytes_per_launch"):
+        assert t[key] == stored[key] and t[key] > 0
